@@ -1,0 +1,184 @@
+"""CPU oracle of the MoE layer forward pass (ctypes front of `oracle.c`).
+
+TEST INFRASTRUCTURE ONLY: the tests, the package entry file's smoke check and
+the benchmark's CPU-baseline leg may import this module; the product path never
+does.  Every function converts its inputs to float64 (exact for bf16/fp32
+storage) and calls the plain C implementation in `oracle.c`, which shares no
+code with the CUDA path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/liboracle.so (gcc, OpenMP, no fast-math, no contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+                               "-fPIC", "-shared", "-o", _LIB, _SRC, "-lm"])
+    return _LIB
+
+
+def _lib_():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        i64, i32, vp, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double
+        lib.oracle_softplus.argtypes = [dbl]
+        lib.oracle_softplus.restype = dbl
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = i32
+        lib.oracle_gate_flat.argtypes = [i64, i32, i32, i32] + [vp] * 9
+        lib.oracle_gate_flat.restype = i32
+        lib.oracle_gate_hier.argtypes = [i64, i32, i32, i32, i32, i32] + [vp] * 8
+        lib.oracle_gate_hier.restype = i32
+        lib.oracle_route.argtypes = [i64, i32, i32] + [vp] * 8
+        lib.oracle_route.restype = i32
+        lib.oracle_expert.argtypes = [i32, i32] + [vp] * 7
+        lib.oracle_expert.restype = None
+        lib.oracle_experts_combine.argtypes = [i64, i32, i32, i32, i32] + [vp] * 8
+        lib.oracle_experts_combine.restype = i32
+        lib.oracle_forward.argtypes = [i64, i32, i32, i32, i32, i32, i32] + [vp] * 18
+        lib.oracle_forward.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _f64(a):
+    """Exact float64 copy of a numpy array or torch tensor (None passes through)."""
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor
+        import torch
+        a = a.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i32(a):
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def num_threads() -> int:
+    return _lib_().oracle_num_threads()
+
+
+def softplus(z: float) -> float:
+    return _lib_().oracle_softplus(float(z))
+
+
+def gate_flat(x, Wg, Wn, bg, eps, k: int):
+    """Flat noisy top-k gate.  Returns idx [T,k] int32, G [T,k], H [T,n], margin [T]."""
+    x, Wg, Wn, bg, eps = map(_f64, (x, Wg, Wn, bg, eps))
+    T, d = x.shape
+    n = Wg.shape[1]
+    idx = np.zeros((T, k), np.int32)
+    G = np.zeros((T, k))
+    H = np.zeros((T, n))
+    margin = np.zeros(T)
+    rc = _lib_().oracle_gate_flat(T, d, n, k, _p(x), _p(Wg), _p(Wn), _p(bg), _p(eps), _p(idx),
+                                  _p(G), _p(H), _p(margin))
+    if rc:
+        raise ValueError("oracle_gate_flat: bad arguments")
+    return idx, G, H, margin
+
+
+def gate_hier(x, Wg, Wn, bg, eps, groups: int, k_groups: int, k: int):
+    """Hierarchical noisy gate.  Returns idx [T,k] int32, G [T,k], margin [T]."""
+    x, Wg, Wn, bg, eps = map(_f64, (x, Wg, Wn, bg, eps))
+    T, d = x.shape
+    n = Wg.shape[1] - groups
+    if k % k_groups or n % groups:
+        raise ValueError("k must be a multiple of k_groups and n of groups")
+    idx = np.zeros((T, k), np.int32)
+    G = np.zeros((T, k))
+    margin = np.zeros(T)
+    rc = _lib_().oracle_gate_hier(T, d, groups, n // groups, k_groups, k // k_groups, _p(x),
+                                  _p(Wg), _p(Wn), _p(bg), _p(eps), _p(idx), _p(G), _p(margin))
+    if rc:
+        raise ValueError("oracle_gate_hier: bad arguments")
+    return idx, G, margin
+
+
+def route(idx, G, n: int):
+    """Routing.  Returns counts, offsets, perm, inv_perm, importance, cv2."""
+    idx = _i32(idx)
+    G = _f64(G)
+    T, k = idx.shape
+    S = T * k
+    counts = np.zeros(n, np.int32)
+    offsets = np.zeros(n + 1, np.int32)
+    perm = np.zeros(max(S, 1), np.int32)
+    inv_perm = np.zeros(max(S, 1), np.int32)
+    importance = np.zeros(n)
+    cv2 = ctypes.c_double(0.0)
+    rc = _lib_().oracle_route(T, n, k, _p(idx), _p(G), _p(counts), _p(offsets), _p(perm),
+                              _p(inv_perm), _p(importance), ctypes.addressof(cv2))
+    if rc:
+        raise ValueError("oracle_route: bad arguments")
+    return counts, offsets, perm[:S], inv_perm[:S], importance, cv2.value
+
+
+def expert(x_row, W1e, b1e, W2e, b2e):
+    """E(x) for one token and one expert (W1e [h,d], W2e [d,h])."""
+    x_row, W1e, b1e, W2e, b2e = map(_f64, (x_row, W1e, b1e, W2e, b2e))
+    h, d = W1e.shape
+    a = np.zeros(h)
+    out = np.zeros(d)
+    _lib_().oracle_expert(d, h, _p(x_row), _p(W1e), _p(b1e), _p(W2e), _p(b2e), _p(a), _p(out))
+    return out
+
+
+def experts_combine(x, idx, G, W1, b1, W2, b2):
+    """y[t] = sum_j G[t,j] E_{idx[t,j]}(x_t)."""
+    x, G, W1, b1, W2, b2 = map(_f64, (x, G, W1, b1, W2, b2))
+    idx = _i32(idx)
+    T, d = x.shape
+    n, h, _ = W1.shape
+    k = idx.shape[1]
+    y = np.zeros((T, d))
+    rc = _lib_().oracle_experts_combine(T, d, h, n, k, _p(x), _p(idx), _p(G), _p(W1), _p(b1),
+                                        _p(W2), _p(b2), _p(y))
+    if rc:
+        raise ValueError("oracle_experts_combine: bad arguments")
+    return y
+
+
+def forward(x, Wg, Wn, bg, eps, W1, b1, W2, b2, k: int, groups: int = 0, k_groups: int = 0):
+    """The whole layer.  Returns a dict with y, G, idx, importance, cv2, counts, offsets,
+    perm, inv_perm (all numpy; floats in float64)."""
+    x, Wg, Wn, bg, eps, W1, b1, W2, b2 = map(_f64, (x, Wg, Wn, bg, eps, W1, b1, W2, b2))
+    T, d = x.shape
+    n, h, _ = W1.shape
+    S = T * k
+    out = dict(
+        y=np.zeros((T, d)), G=np.zeros((T, k)), idx=np.zeros((T, k), np.int32),
+        importance=np.zeros(n), counts=np.zeros(n, np.int32), offsets=np.zeros(n + 1, np.int32),
+        perm=np.zeros(max(S, 1), np.int32), inv_perm=np.zeros(max(S, 1), np.int32))
+    cv2 = ctypes.c_double(0.0)
+    rc = _lib_().oracle_forward(
+        T, d, h, n, k, groups, k_groups, _p(x), _p(Wg), _p(Wn), _p(bg), _p(eps), _p(W1), _p(b1),
+        _p(W2), _p(b2), _p(out["y"]), _p(out["G"]), _p(out["idx"]), _p(out["importance"]),
+        ctypes.addressof(cv2), _p(out["counts"]), _p(out["offsets"]), _p(out["perm"]),
+        _p(out["inv_perm"]))
+    if rc:
+        raise ValueError("oracle_forward: bad arguments")
+    out["cv2"] = cv2.value
+    out["perm"] = out["perm"][:S]
+    out["inv_perm"] = out["inv_perm"][:S]
+    return out
