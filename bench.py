@@ -1,0 +1,436 @@
+"""Benchmark of the MoE layer forward pass (moe_forward through the C ABI).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step is one full forward pass (gate, dispatch, expert FFNs, combine) over
+one batch of the workload (default: flat_n256_k4, T=16384 tokens, d=512,
+h=1024, n=256 experts, k=4, bf16 FFN, fp32 gating, noisy).  Inputs are
+synthetic and seeded; x/eps rotate over several device copies so that the
+timed loop never re-reads them from L2 (the 537 MB of expert weights are
+larger than the 126 MB L2 by themselves).  Rank 0 prints one JSON line.
+
+Under torchrun every rank runs its own batch (weak scaling, no collective on
+the data path); value = all ranks' tokens / the slowest rank's time.
+`--impl reference` times the CPU oracle on the host cores instead (a bounded
+sample of tokens per step), printing the same kind of line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparsely_gated_mixture_top_b300 import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer tokens/sec (fused forward, 1xB300 per rank)"
+UNIT = "tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="flat_n256_k4", choices=sorted(wl.WORKLOADS))
+    p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target CPU seconds of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# Peaks and algorithmic work
+# ---------------------------------------------------------------------------
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return dict(hbm=float(m["hbm_gbs"]), bf16=float(m["bf16_tflops"]),
+                    bf16_sustained=float(m["bf16_tflops_sustained"]), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
+
+
+def algorithmic(w: wl.Workload, counts: np.ndarray) -> dict:
+    """Algorithmic bytes and FLOPs of one forward pass, from the run's own counts."""
+    eb = 2 if w.dtype == "bf16" else 4
+    hit = int((counts > 0).sum())
+    weights = hit * (2 * w.d * w.h * eb + 4 * (w.d + w.h))
+    S = w.T * w.k
+    x_b = w.T * w.d * eb
+    y_b = w.T * w.d * eb
+    if w.groups == 0:
+        eps_b = w.T * w.n * 4 if w.noisy else 0
+        gate_cols = w.n
+    else:
+        m = w.n // w.groups
+        eps_b = w.T * (w.groups + w.k_groups * m) * 4 if w.noisy else 0
+        gate_cols = w.groups + w.n
+    wg_b = 2 * w.d * gate_cols * 4
+    small = S * 8 + w.n * 8
+    layer_bytes = weights + x_b + y_b + eps_b + wg_b + small
+    ffn_bytes = weights + x_b + S * w.d * eb     # weights hit, x rows once, expert rows out
+    flops = 4.0 * S * w.d * w.h
+    return dict(layer_bytes=layer_bytes, ffn_bytes=ffn_bytes, flops=flops, experts_hit=hit)
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample_rate(w: wl.Workload, seconds: float, max_tokens: int | None = None):
+    """Time the oracle forward on the first tokens of the workload; returns
+    (tokens/s, cores, tokens per sample, seconds).  Weight conversion to fp64
+    happens before the clock starts."""
+    import oracle
+    inp = wl.make_inputs(w, tokens=slice(0, min(w.T, 64)))
+    W1 = oracle._f64(inp["W1"])
+    W2 = oracle._f64(inp["W2"])
+    b1, b2 = oracle._f64(inp["b1"]), oracle._f64(inp["b2"])
+
+    def run(ntok):
+        part = wl.make_inputs(w, experts=False, tokens=slice(0, ntok))
+        x, eps = oracle._f64(part["x"]), oracle._f64(part["eps"])
+        t0 = time.perf_counter()
+        oracle.forward(x, part["Wg"], part["Wn"], part["bg"], eps if w.noisy else None, W1, b1, W2,
+                       b2, w.k, w.groups, w.k_groups)
+        return time.perf_counter() - t0
+
+    probe = min(w.T, 32)
+    dt = run(probe)
+    ntok = max(1, min(w.T, int(probe * seconds / max(dt, 1e-6))))
+    if max_tokens:
+        ntok = min(ntok, max_tokens)
+    dt = run(ntok)
+    return ntok / dt, oracle.num_threads(), ntok, dt
+
+
+def reference_arm(args, w: wl.Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    total_budget = 150.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    rate, cores, ntok, dt = oracle_sample_rate(w, seconds=min(per_step, 20.0))
+    import oracle
+    inp = wl.make_inputs(w, tokens=slice(0, 64))
+    W1, W2 = oracle._f64(inp["W1"]), oracle._f64(inp["W2"])
+    b1, b2 = oracle._f64(inp["b1"]), oracle._f64(inp["b2"])
+    part = wl.make_inputs(w, experts=False, tokens=slice(0, ntok))
+    x = oracle._f64(part["x"])
+    eps = oracle._f64(part["eps"]) if w.noisy else None
+    Wg, Wn = oracle._f64(part["Wg"]), oracle._f64(part["Wn"])
+    bg = oracle._f64(part["bg"])
+
+    def step():
+        oracle.forward(x, Wg, Wn, bg, eps, W1, b1, W2, b2, w.k, w.groups, w.k_groups)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = ntok * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {ntok} tokens of the workload per step (fp64 C oracle, "
+                                   f"OpenMP; weights converted to fp64 before timing)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w: wl.Workload) -> dict:
+    return {"workload": w.name, "T": w.T, "d": w.d, "h": w.h, "n": w.n, "k": w.k,
+            "groups": w.groups, "k_groups": w.k_groups, "noisy": w.noisy,
+            "ffn_dtype": w.dtype, "gate_dtype": "f32"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def launches_per_step(w: wl.Workload) -> int:
+    gate, dispatch, combine = 2, 6, 1
+    ffn = 4 if w.dtype == "bf16" else 3
+    return gate + dispatch + ffn + combine
+
+
+def main():
+    args = parse()
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from sparsely_gated_mixture_top_b300 import binding as B
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    wr = w.with_(seed=w.seed + 7919 * rank) if rank else w   # each rank its own batch
+    host = wl.make_inputs(w)                                   # weights shared by all ranks
+    if rank:
+        part = wl.make_inputs(wr, experts=False)
+        host["x"], host["eps"] = part["x"], part["eps"]
+    dinp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+
+    # rotating copies of the per-step inputs (x, eps): together with the
+    # weights they exceed L2, so no step reads another step's inputs from L2
+    per_set = host["x"].numel() * host["x"].element_size() + (
+        host["eps"].numel() * 4 if host["eps"] is not None else 0)
+    nsets = max(2, min(8, math.ceil(256e6 / max(per_set, 1))))
+    sets = [(dinp["x"], dinp["eps"])]
+    for i in range(1, nsets):
+        p = wl.make_inputs(wr.with_(seed=wr.seed + 104729 * i), experts=False)
+        sets.append((p["x"].to(dev), p["eps"].to(dev) if p["eps"] is not None else None))
+
+    s = B.shape_of(w)
+    ws = B.workspace(s, dev)
+    out = B.outputs(s, dev)
+
+    def fwd(i):
+        x, eps = sets[i % nsets]
+        B.moe_forward(s, x, dinp["Wg"], dinp["Wn"], dinp["bg"], eps, dinp["W1"], dinp["b1"],
+                      dinp["W2"], dinp["b2"], out["y"], out["G"], out["idx"], out["importance"],
+                      out["cv2"], out["counts"], ws, stream)
+
+    for i in range(args.warmup):
+        fwd(i)
+    torch.cuda.synchronize(dev)
+    status = B.moe_check(ws, stream)
+    if status != B.MOE_OK:
+        raise RuntimeError(f"device error during warm-up: {B.status_string(status)}")
+
+    # ---- main timed region: K fused forward passes --------------------------
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        fwd(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    status = B.moe_check(ws, stream)
+    if status != B.MOE_OK:
+        raise RuntimeError(f"device error in the timed region: {B.status_string(status)}")
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    tokens = w.T * args.steps * world
+    value = tokens / (ms / 1e3)
+    counts = out["counts"].cpu().numpy()
+    alg = algorithmic(w, counts)
+    pk = peaks()
+
+    # ---- stage timing: the expert FFN stage, same inputs, component calls ---
+    S = w.T * w.k
+    comp = dict(idx=out["idx"], G=out["G"], counts=out["counts"],
+                offsets=torch.empty(w.n + 1, dtype=torch.int32, device=dev),
+                perm=torch.empty(S, dtype=torch.int32, device=dev),
+                inv_perm=torch.empty(S, dtype=torch.int32, device=dev),
+                Y=torch.empty((S, w.d), dtype=out["y"].dtype, device=dev))
+    ksteps = max(1, args.steps // 2)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(ksteps)]
+    torch.cuda.synchronize(dev)
+    for i in range(ksteps):
+        x, eps = sets[i % nsets]
+        B.moe_gate(s, x, dinp["Wg"], dinp["Wn"], dinp["bg"], eps, comp["idx"], comp["G"], ws,
+                   stream)
+        B.moe_dispatch(s, comp["idx"], comp["G"], comp["counts"], comp["offsets"], comp["perm"],
+                       comp["inv_perm"], out["importance"], out["cv2"], ws, stream)
+        ev[i][0].record(stream)
+        B.moe_expert_ffn(s, x, comp["perm"], comp["offsets"], dinp["W1"], dinp["b1"], dinp["W2"],
+                         dinp["b2"], comp["Y"], ws, stream)
+        ev[i][1].record(stream)
+        B.moe_combine(s, comp["Y"], comp["inv_perm"], comp["G"], out["y"], ws, stream)
+    torch.cuda.synchronize(dev)
+    ffn_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    ffn_bound_hbm = alg["ffn_bytes"] / (pk["hbm"] * 1e9) >= alg["flops"] / (pk["bf16"] * 1e12)
+    if ffn_bound_hbm:
+        achieved = alg["ffn_bytes"] / (ffn_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s"}
+    else:
+        achieved = alg["flops"] / (ffn_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = "expert FFN stage (moe_expert_ffn: gather + 2 grouped tcgen05 GEMMs)"
+    roof["ms_per_launch"] = ffn_ms
+    roof["peak_source"] = pk["source"] + " (burst)"
+
+    t_roof = max(alg["layer_bytes"] / (pk["hbm"] * 1e9), alg["flops"] / (pk["bf16"] * 1e12))
+    layer_roof = {"bound": "hbm" if alg["layer_bytes"] / (pk["hbm"] * 1e9) >= alg["flops"] / (
+                      pk["bf16"] * 1e12) else "tensor",
+                  "t_roof_us": t_roof * 1e6, "t_meas_us": ms_step * 1e3,
+                  "frac": t_roof / (ms_step / 1e3), "algorithmic_bytes": alg["layer_bytes"],
+                  "flops": alg["flops"], "experts_hit": alg["experts_hit"]}
+
+    # ---- end to end: host buffers in, results out, through moe_forward ------
+    e2e = None
+    if rank == 0 or world > 1:
+        pin_x = [st[0].cpu().pin_memory() for st in sets[:2]]
+        pin_e = [st[1].cpu().pin_memory() if st[1] is not None else None for st in sets[:2]]
+        hy = torch.empty(out["y"].shape, dtype=out["y"].dtype, pin_memory=True)
+        hG = torch.empty(out["G"].shape, dtype=torch.float32, pin_memory=True)
+        hi = torch.empty(out["idx"].shape, dtype=torch.int32, pin_memory=True)
+        him = torch.empty(w.n, dtype=torch.float32, pin_memory=True)
+        hc = torch.empty(w.n, dtype=torch.int32, pin_memory=True)
+        hcv = torch.empty(1, dtype=torch.float32, pin_memory=True)
+        dx, de = torch.empty_like(dinp["x"]), (torch.empty_like(dinp["eps"]) if dinp["eps"] is not None else None)
+        h2d = pin_x[0].numel() * pin_x[0].element_size() + (pin_e[0].numel() * 4 if pin_e[0] is not None else 0)
+        d2h = sum(t.numel() * t.element_size() for t in (hy, hG, hi, him, hc, hcv))
+
+        def e2e_step(i):
+            dx.copy_(pin_x[i % 2], non_blocking=True)
+            if de is not None:
+                de.copy_(pin_e[i % 2], non_blocking=True)
+            B.moe_forward(s, dx, dinp["Wg"], dinp["Wn"], dinp["bg"], de, dinp["W1"], dinp["b1"],
+                          dinp["W2"], dinp["b2"], out["y"], out["G"], out["idx"],
+                          out["importance"], out["cv2"], out["counts"], ws, stream)
+            hy.copy_(out["y"], non_blocking=True)
+            hG.copy_(out["G"], non_blocking=True)
+            hi.copy_(out["idx"], non_blocking=True)
+            him.copy_(out["importance"], non_blocking=True)
+            hc.copy_(out["counts"], non_blocking=True)
+            hcv.copy_(out["cv2"], non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(b)
+        if dist:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": w.T * args.e2e_steps * world / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": args.e2e_steps, "api": "moe_forward (pinned host x/eps in, y/G/idx/"
+                                                "importance/cv2/counts out)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, ntok, dt = oracle_sample_rate(w, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {ntok} tokens of the workload, one fp64 oracle forward "
+                         f"({dt:.1f} s; weights converted to fp64 before timing)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if w.dtype == "bf16" else "f32", "data": "synthetic (seeded counter-based normal)",
+            "config": dict(config_of(w), l2=f"{nsets} rotating x/eps sets ({nsets * per_set / 1e6:.0f} MB)"
+                           f" + {alg['layer_bytes'] / 1e9:.2f} GB algorithmic bytes per step > 126 MB L2"),
+            "tflops": alg["flops"] / (ms_step / 1e3) / 1e12,
+            "layer_roofline": layer_roof,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step(w) * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * moe.h -- C ABI of the Sparsely-Gated Mixture-of-Experts layer forward pass
+ * on one NVIDIA B300 (sm_103a).
+ *
+ * The layer (Shazeer et al. 2017, "Outrageously Large Neural Networks: The
+ * Sparsely-Gated Mixture-of-Experts Layer"), as the lesson page
+ * "MoE:稀疏门控混合专家" states it:
+ *   section 三 "门控怎么挑": a gate matrix W_g with one column per expert
+ *     scores each token; KeepTopK sets all but the k best scores to -inf; a
+ *     softmax turns the survivors into weights G(x) that sum to 1.  With
+ *     thousands of experts the choice is two-level (MoE-N-h): pick the best
+ *     groups first, then the best experts inside each chosen group.
+ *   section 四 "为什么要加噪声": the score is noisy,
+ *     H(x)_i = (x.W_g)_i + eps_i * softplus((x.W_noise)_i), eps redrawn each time.
+ *   section 二 "一层 MoE 长什么样": each expert E_i is a feed-forward net with
+ *     one hidden ReLU layer, and y = sum_i G(x)_i E_i(x); experts with weight 0
+ *     are not computed.
+ * The ai-papers.xuzou.cn card "Outrageously Large Neural Networks - 中文验证版"
+ * (section 瓶颈) adds that each expert sees about k*b/n rows, and (section
+ * 方法适配) that an importance loss and a load loss keep the experts balanced;
+ * this library returns the importance vector, its CV^2 and the per-expert
+ * counts that those terms are built from.
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc'd or torch CUDA
+ *     memory of the current device), row-major, 16-byte aligned.  The caller
+ *     allocates and owns every buffer, including the workspace; the library
+ *     never allocates or frees device memory and keeps no global mutable state
+ *     (calls with distinct workspaces may run concurrently on different streams).
+ *   - `stream` is a cudaStream_t (passed as void*); NULL is the legacy default
+ *     stream.  Calls enqueue work and return without synchronising.
+ *   - Host-detectable errors (bad shape, NULL or misaligned pointer, workspace
+ *     too small, unsupported size) return a negative moe_status synchronously
+ *     and enqueue nothing.  Errors found on the device (an expert index out of
+ *     range, a bounded wait that ran out) are recorded in the workspace's error
+ *     word; moe_check() reads it.  Nothing crosses the ABI as an exception.
+ *   - Results are deterministic: identical inputs give bit-identical outputs
+ *     (no floating-point atomics, fixed reduction orders, stable permutation).
+ *
+ * Layouts (C = n for flat gating, C = G + n for hierarchical gating; S = T*k
+ * slots, slot s = t*k + j is the j-th expert choice of token t):
+ *   x        [T, d]     dtype (MOE_BF16 or MOE_F32)
+ *   Wg, Wn   [d, C]     fp32.  Hierarchical: columns 0..G-1 score the groups,
+ *                        then G blocks of m = n/G columns, block g scoring the
+ *                        experts g*m .. g*m+m-1 of group g.
+ *   bg       [C]        fp32 or NULL; added to the clean score x.W_g
+ *   eps      [T, C]     fp32; required (with Wn) when shape.noisy == 1, ignored
+ *                        (may be NULL) when shape.noisy == 0
+ *   idx      [T, k]     int32, the chosen experts in descending H order
+ *                        (hierarchical: group rank major, inner rank minor)
+ *   G        [T, k]     fp32, their gate weights (sum to 1 per token)
+ *   W1       [n, h, d]  dtype; expert e's first layer, out x in (a = W1[e] x + b1[e])
+ *   b1       [n, h]     fp32 or NULL (= zeros)
+ *   W2       [n, d, h]  dtype; expert e's second layer, out x in
+ *   b2       [n, d]     fp32 or NULL (= zeros)
+ *   counts   [n]        int32, slots routed to each expert
+ *   offsets  [n+1]      int32, exclusive prefix sum of counts
+ *   perm     [S]        int32, expert-ordered row r -> slot (stable: rows of
+ *                        one expert are in increasing slot order)
+ *   inv_perm [S]        int32, slot -> row
+ *   importance [n]      fp32, sum of the gate weights routed to each expert
+ *   cv2      [1]        fp32, population variance(importance) / mean^2
+ *   Y_slot   [S, d]     dtype, expert output of row r (expert-row order)
+ *   y        [T, d]     dtype, the layer output
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t moe_status;
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1) /* bad shape, NULL or misaligned pointer */
+#define MOE_ERR_UNSUPPORTED (-2) /* valid but outside this build's limits */
+#define MOE_ERR_WORKSPACE (-3)   /* workspace NULL, misaligned or too small */
+#define MOE_ERR_CUDA (-4)        /* a CUDA runtime/driver call failed */
+#define MOE_ERR_TIMEOUT (-5)     /* a bounded device wait ran out (device-side) */
+#define MOE_ERR_DEVICE (-6)      /* bad data found on the device, e.g. idx >= n */
+
+#define MOE_F32 0
+#define MOE_BF16 1
+
+/* Limits of this build (MOE_ERR_UNSUPPORTED beyond them). */
+#define MOE_MAX_K 16          /* experts per token; also k_groups and k/k_groups */
+#define MOE_MAX_COLS 16384    /* gate columns C */
+#define MOE_MAX_SLOTS 0x7FFFFFFF
+
+typedef struct moe_shape {
+    int64_t T;        /* tokens (0 allowed: outputs are zero-filled, nothing else runs) */
+    int32_t d;        /* model width; multiple of 64, <= 8192 */
+    int32_t h;        /* expert hidden width; multiple of 64, <= 16384 */
+    int32_t n;        /* experts, >= 1 */
+    int32_t k;        /* experts per token in total, 1 <= k <= min(n, MOE_MAX_K) */
+    int32_t groups;   /* 0: flat gating.  G > 0: hierarchical, n % G == 0 */
+    int32_t k_groups; /* hierarchical only: groups kept per token, k % k_groups == 0,
+                         k_groups <= G and k / k_groups <= n / G */
+    int32_t dtype;    /* MOE_BF16 or MOE_F32: the type of x, W1, W2, Y_slot and y */
+    int32_t noisy;    /* 1: add eps * softplus(x.W_noise) to the score; 0: clean score */
+} moe_shape;
+
+/* Library version, major*10000 + minor*100 + patch. */
+MOE_API int32_t moe_version(void);
+
+/* Static text for a status code. */
+MOE_API const char *moe_status_string(moe_status s);
+
+/* Host-only check of a shape against the rules above.  No device work. */
+MOE_API moe_status moe_validate(const moe_shape *shape);
+
+/* Workspace bytes every call below needs for this shape (0 if the shape is
+ * invalid).  One workspace serves all calls of one shape; its first 256 bytes
+ * hold the device error word.  The workspace must be 256-byte aligned. */
+MOE_API size_t moe_workspace_bytes(const moe_shape *shape);
+
+/* Clears the device error word of a workspace (enqueued on `stream`).  Call it
+ * once on a fresh workspace before its first use. */
+MOE_API moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Gate ("MoE:稀疏门控混合专家", sections 三 and 四): for every token the
+ * noisy score H = x.W_g (+ bg) + eps * softplus(x.W_noise), KeepTopK and
+ * softmax over the k survivors (flat), or the two-level choice (hierarchical:
+ * k_groups groups by their noisy group score, then k/k_groups experts in each
+ * kept group by that group's own columns; weight = group weight x inner weight).
+ * Scores are computed with fp32-faithful accuracy; ties go to the lower index.
+ * Writes idx [T,k] and G [T,k].
+ */
+MOE_API moe_status moe_gate(const moe_shape *shape, const void *x, const float *Wg, const float *Wn,
+                    const float *bg, const float *eps, int32_t *idx, float *G, void *ws,
+                    size_t ws_bytes, void *stream);
+
+/*
+ * Dispatch (routing): per-expert counts, their exclusive scan, the stable
+ * permutation of the slots into expert-contiguous rows and its inverse, the
+ * importance vector (gate weight summed per expert in row order, fp64
+ * accumulation) and its CV^2.  An idx entry outside [0, n) sets
+ * MOE_ERR_DEVICE in the error word; that slot is left out of every output
+ * (inv_perm[s] = -1) and the rest stays consistent.
+ */
+MOE_API moe_status moe_dispatch(const moe_shape *shape, const int32_t *idx, const float *G,
+                        int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                        float *importance, float *cv2, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Expert FFNs on expert-contiguous rows ("MoE:稀疏门控混合专家", section 二):
+ * for every expert e and row r in [offsets[e], offsets[e+1]), with token
+ * t = perm[r] / k,  Y_slot[r] = W2[e] . ReLU(W1[e] . x[t] + b1[e]) + b2[e].
+ * BF16: bf16 operands, fp32 accumulation on the tensor cores, the hidden
+ * activation rounded once to bf16 between the layers, Y_slot rounded once.
+ * F32: fp32 throughout.  Unselected experts are not computed.
+ */
+MOE_API moe_status moe_expert_ffn(const moe_shape *shape, const void *x, const int32_t *perm,
+                          const int32_t *offsets, const void *W1, const float *b1, const void *W2,
+                          const float *b2, void *Y_slot, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Combine: y[t] = sum_{j=0..k-1} G[t,j] * Y_slot[inv_perm[t*k+j]], summed in
+ * fp32 in that fixed j order and rounded once to the output type.  A slot
+ * with inv_perm = -1 contributes nothing; an entry >= S sets MOE_ERR_DEVICE.
+ */
+MOE_API moe_status moe_combine(const moe_shape *shape, const void *Y_slot, const int32_t *inv_perm,
+                       const float *G, void *y, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * The whole forward pass on one stream: gate, dispatch, expert FFNs and
+ * combine.  Outputs y [T,d], G [T,k], idx [T,k], importance [n], cv2 [1],
+ * counts [n]; the permutation and the expert outputs live in the workspace.
+ */
+MOE_API moe_status moe_forward(const moe_shape *shape, const void *x, const float *Wg, const float *Wn,
+                       const float *bg, const float *eps, const void *W1, const float *b1,
+                       const void *W2, const float *b2, void *y, float *G, int32_t *idx,
+                       float *importance, float *cv2, int32_t *counts, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, reads the workspace's device error word, clears it
+ * and returns it (MOE_OK when no device error was recorded).  Returns
+ * MOE_ERR_CUDA if the stream itself failed.
+ */
+MOE_API moe_status moe_check(void *ws, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -50,6 +50,8 @@ def _lib_():
         lib.oracle_experts_combine.restype = i32
         lib.oracle_forward.argtypes = [i64, i32, i32, i32, i32, i32, i32] + [vp] * 18
         lib.oracle_forward.restype = i32
+        lib.oracle_combine_rows.argtypes = [i64, i32, i32, i64] + [vp] * 4
+        lib.oracle_combine_rows.restype = i32
         _lib = lib
     return _lib
 
@@ -157,6 +159,50 @@ def experts_combine(x, idx, G, W1, b1, W2, b2):
     if rc:
         raise ValueError("oracle_experts_combine: bad arguments")
     return y
+
+
+def combine_rows(Y, inv_perm, G):
+    """y[t] = sum_j G[t,j] * Y[inv_perm[t*k+j]] from expert-order rows Y [S, d]."""
+    Y, G = _f64(Y), _f64(G)
+    inv_perm = _i32(inv_perm)
+    T, k = G.shape
+    S, d = Y.shape
+    y = np.zeros((T, d))
+    rc = _lib_().oracle_combine_rows(T, d, k, S, _p(Y), _p(inv_perm), _p(G), _p(y))
+    if rc:
+        raise ValueError("oracle_combine_rows: bad arguments")
+    return y
+
+
+def expert_rows(x_rows, experts, W1, b1, W2, b2):
+    """E_{experts[i]}(x_rows[i]) for each i.  W1/W2 may be callables e -> that expert's
+    matrix (to avoid converting every expert); rows are grouped per expert."""
+    experts = np.asarray(experts)
+    x_rows = _f64(x_rows)
+    d = x_rows.shape[1]
+    out = np.zeros((len(experts), d))
+    get = lambda W, e: W(e) if callable(W) else W[e]
+    for e in np.unique(experts):
+        sel = np.nonzero(experts == e)[0]
+        W1e, W2e = _f64(get(W1, e)), _f64(get(W2, e))
+        b1e = None if b1 is None else _f64(get(b1, e))
+        b2e = None if b2 is None else _f64(get(b2, e))
+        h = W1e.shape[0]
+        m = len(sel)
+        # Keep every array alive across the call (ctypes holds raw addresses only).
+        xs = np.ascontiguousarray(x_rows[sel])
+        ids = np.zeros((m, 1), np.int32)
+        ones = np.ones((m, 1))
+        W1b, W2b = np.ascontiguousarray(W1e[None]), np.ascontiguousarray(W2e[None])
+        b1b = None if b1e is None else np.ascontiguousarray(b1e[None])
+        b2b = None if b2e is None else np.ascontiguousarray(b2e[None])
+        y = np.zeros((m, d))
+        rc = _lib_().oracle_experts_combine(m, d, h, 1, 1, _p(xs), _p(ids), _p(ones), _p(W1b),
+                                            _p(b1b), _p(W2b), _p(b2b), _p(y))
+        if rc:
+            raise ValueError("oracle expert evaluation failed")
+        out[sel] = y
+    return out
 
 
 def forward(x, Wg, Wn, bg, eps, W1, b1, W2, b2, k: int, groups: int = 0, k_groups: int = 0):

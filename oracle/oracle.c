@@ -412,3 +412,22 @@ int oracle_forward(int64_t T, int d, int h, int n, int k, int groups, int k_grou
     if (rc) return rc;
     return oracle_experts_combine(T, d, h, n, k, x, idx, G, W1, b1, W2, b2, y);
 }
+
+/*
+ * Combine alone, from expert outputs already in expert-row order:
+ * y[t] = sum_{j<k} G[t,j] * Y[inv_perm[t*k+j]]  (rows with inv_perm < 0 skipped).
+ */
+int oracle_combine_rows(int64_t T, int d, int k, int64_t S, const double *Y,
+                        const int32_t *inv_perm, const double *G, double *y) {
+    if (T < 0 || d <= 0 || k <= 0) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int o = 0; o < d; ++o) y[t * d + o] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const int32_t r = inv_perm[t * k + j];
+            if (r < 0) continue;
+            if (r >= S) return -1;
+            for (int o = 0; o < d; ++o) y[t * d + o] += G[t * k + j] * Y[(int64_t)r * d + o];
+        }
+    }
+    return 0;
+}

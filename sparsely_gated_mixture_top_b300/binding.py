@@ -1,0 +1,186 @@
+"""Python binding of the C ABI in include/moe.h (ctypes; argument marshalling only).
+
+Every function here passes torch CUDA tensors' device pointers and sizes to
+the shared library `libmoe_b300.so` built in-tree by
+`python -m sparsely_gated_mixture_top_b300.build`; every step of the layer
+runs in that library's CUDA kernels.  PyTorch supplies device memory and
+streams only.  There is no fallback: if the library is missing, importing
+this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_WORKSPACE = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_TIMEOUT = -5
+MOE_ERR_DEVICE = -6
+MOE_F32 = 0
+MOE_BF16 = 1
+
+EXPORTS = ("moe_version", "moe_status_string", "moe_validate", "moe_workspace_bytes",
+           "moe_workspace_init", "moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine",
+           "moe_forward", "moe_check")
+
+
+class MoEShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("h", ctypes.c_int32),
+                ("n", ctypes.c_int32), ("k", ctypes.c_int32), ("groups", ctypes.c_int32),
+                ("k_groups", ctypes.c_int32), ("dtype", ctypes.c_int32), ("noisy", ctypes.c_int32)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} ({status})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run "
+                          "`python -m sparsely_gated_mixture_top_b300.build` first")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32, shp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.POINTER(MoEShape)
+    lib.moe_version.argtypes, lib.moe_version.restype = [], i32
+    lib.moe_status_string.argtypes, lib.moe_status_string.restype = [i32], ctypes.c_char_p
+    lib.moe_validate.argtypes, lib.moe_validate.restype = [shp], i32
+    lib.moe_workspace_bytes.argtypes, lib.moe_workspace_bytes.restype = [shp], sz
+    lib.moe_workspace_init.argtypes, lib.moe_workspace_init.restype = [vp, sz, vp], i32
+    lib.moe_gate.argtypes = [shp] + [vp] * 8 + [sz, vp]
+    lib.moe_dispatch.argtypes = [shp] + [vp] * 9 + [sz, vp]
+    lib.moe_expert_ffn.argtypes = [shp] + [vp] * 9 + [sz, vp]
+    lib.moe_combine.argtypes = [shp] + [vp] * 5 + [sz, vp]
+    lib.moe_forward.argtypes = [shp] + [vp] * 16 + [sz, vp]
+    lib.moe_check.argtypes = [vp, vp]
+    for f in ("moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
+              "moe_check"):
+        getattr(lib, f).restype = i32
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.moe_status_string(status).decode()
+
+
+def _p(t):
+    """Device pointer of a tensor (None -> NULL)."""
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ok(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoEError(fn, status)
+
+
+def make_shape(T, d, h, n, k, groups=0, k_groups=0, dtype="bf16", noisy=True) -> MoEShape:
+    dt = {"bf16": MOE_BF16, "f32": MOE_F32}[dtype] if isinstance(dtype, str) else int(dtype)
+    return MoEShape(int(T), int(d), int(h), int(n), int(k), int(groups), int(k_groups), dt,
+                    1 if noisy else 0)
+
+
+def shape_of(w) -> MoEShape:
+    """The ABI shape of a workload description (anything with the same fields)."""
+    return make_shape(w.T, w.d, w.h, w.n, w.k, w.groups, w.k_groups, w.dtype, w.noisy)
+
+
+def validate(shape: MoEShape) -> int:
+    return lib.moe_validate(ctypes.byref(shape))
+
+
+def workspace_bytes(shape: MoEShape) -> int:
+    return lib.moe_workspace_bytes(ctypes.byref(shape))
+
+
+def workspace(shape: MoEShape, device="cuda", stream=None) -> torch.Tensor:
+    """A fresh workspace (uint8 device tensor) with its error word cleared."""
+    nbytes = workspace_bytes(shape)
+    if nbytes == 0:
+        raise MoEError("moe_workspace_bytes", validate(shape))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    _ok("moe_workspace_init", lib.moe_workspace_init(_p(ws), nbytes, _stream(stream)))
+    return ws
+
+
+def moe_gate(shape, x, Wg, Wn, bg, eps, idx, G, ws, stream=None):
+    _ok("moe_gate", lib.moe_gate(ctypes.byref(shape), _p(x), _p(Wg), _p(Wn), _p(bg), _p(eps),
+                                 _p(idx), _p(G), _p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_dispatch(shape, idx, G, counts, offsets, perm, inv_perm, importance, cv2, ws,
+                 stream=None):
+    _ok("moe_dispatch", lib.moe_dispatch(ctypes.byref(shape), _p(idx), _p(G), _p(counts),
+                                         _p(offsets), _p(perm), _p(inv_perm), _p(importance),
+                                         _p(cv2), _p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_expert_ffn(shape, x, perm, offsets, W1, b1, W2, b2, Y_slot, ws, stream=None):
+    _ok("moe_expert_ffn", lib.moe_expert_ffn(ctypes.byref(shape), _p(x), _p(perm), _p(offsets),
+                                             _p(W1), _p(b1), _p(W2), _p(b2), _p(Y_slot), _p(ws),
+                                             ws.numel(), _stream(stream)))
+
+
+def moe_combine(shape, Y_slot, inv_perm, G, y, ws, stream=None):
+    _ok("moe_combine", lib.moe_combine(ctypes.byref(shape), _p(Y_slot), _p(inv_perm), _p(G),
+                                       _p(y), _p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_forward(shape, x, Wg, Wn, bg, eps, W1, b1, W2, b2, y, G, idx, importance, cv2, counts,
+                ws, stream=None):
+    _ok("moe_forward", lib.moe_forward(ctypes.byref(shape), _p(x), _p(Wg), _p(Wn), _p(bg),
+                                       _p(eps), _p(W1), _p(b1), _p(W2), _p(b2), _p(y), _p(G),
+                                       _p(idx), _p(importance), _p(cv2), _p(counts), _p(ws),
+                                       ws.numel(), _stream(stream)))
+
+
+def moe_check(ws, stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the workspace's device error code."""
+    return lib.moe_check(_p(ws), _stream(stream))
+
+
+def error_detail(ws) -> tuple[int, int, int]:
+    """(code, site, aux) of the workspace's error word, without clearing it."""
+    h = ws[:16].view(torch.int32).cpu().tolist()
+    return h[0], h[1], h[2]
+
+
+# --------------------------------------------------------------------------
+# Convenience: allocate outputs and run the layer.
+# --------------------------------------------------------------------------
+def outputs(shape: MoEShape, device="cuda") -> dict:
+    dt = torch.bfloat16 if shape.dtype == MOE_BF16 else torch.float32
+    T, k, n = shape.T, shape.k, shape.n
+    return dict(y=torch.empty((T, shape.d), dtype=dt, device=device),
+                G=torch.empty((T, k), dtype=torch.float32, device=device),
+                idx=torch.empty((T, k), dtype=torch.int32, device=device),
+                importance=torch.empty(n, dtype=torch.float32, device=device),
+                cv2=torch.empty(1, dtype=torch.float32, device=device),
+                counts=torch.empty(n, dtype=torch.int32, device=device))
+
+
+def forward(shape: MoEShape, inp: dict, ws=None, out=None, stream=None) -> dict:
+    """moe_forward on device tensors inp = {x, Wg, Wn, bg, eps, W1, b1, W2, b2}."""
+    dev = inp["x"].device
+    ws = workspace(shape, dev, stream) if ws is None else ws
+    out = outputs(shape, dev) if out is None else out
+    moe_forward(shape, inp["x"], inp["Wg"], inp.get("Wn"), inp.get("bg"), inp.get("eps"),
+                inp["W1"], inp.get("b1"), inp["W2"], inp.get("b2"), out["y"], out["G"],
+                out["idx"], out["importance"], out["cv2"], out["counts"], ws, stream)
+    return out

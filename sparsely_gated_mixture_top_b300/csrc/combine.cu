@@ -1,0 +1,100 @@
+// combine.cu -- y[t] = sum_j G[t,j] * Y_slot[inv_perm[t*k+j]]
+// ("MoE:稀疏门控混合专家", section 二: y = sum_i G(x)_i E_i(x), only the selected
+// experts contributing).  One warp per token, 16-byte vector loads of the
+// expert rows, fp32 accumulation in the fixed slot order j = 0..k-1 and one
+// rounding to the output type.
+#include "moe_device.cuh"
+#include "moe_launch.h"
+
+namespace moe {
+
+namespace {
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ static void load(const __nv_bfloat16 *p, float (&v)[8]) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(b[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    __device__ static void store(__nv_bfloat16 *p, const float (&v)[8]) {
+        uint4 u;
+        u.x = pack_bf16x2(v[0], v[1]);
+        u.y = pack_bf16x2(v[2], v[3]);
+        u.z = pack_bf16x2(v[4], v[5]);
+        u.w = pack_bf16x2(v[6], v[7]);
+        *reinterpret_cast<uint4 *>(p) = u;
+    }
+};
+template <>
+struct Vec<float> {
+    static constexpr int N = 4;
+    __device__ static void load(const float *p, float (&v)[4]) {
+        const float4 u = *reinterpret_cast<const float4 *>(p);
+        v[0] = u.x;
+        v[1] = u.y;
+        v[2] = u.z;
+        v[3] = u.w;
+    }
+    __device__ static void store(float *p, const float (&v)[4]) {
+        *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(const T *__restrict__ Y,
+                                                      const int32_t *__restrict__ inv_perm,
+                                                      const float *__restrict__ G, int64_t T_,
+                                                      int d, int k, int64_t S,
+                                                      T *__restrict__ y, int32_t *err) {
+    constexpr int V = Vec<T>::N;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+    if (t >= T_) return;
+    const int lane = threadIdx.x & 31;
+    for (int c = lane * V; c < d; c += 32 * V) {
+        float acc[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int32_t row = inv_perm[t * k + j];
+            if (row < 0) continue;
+            if (row >= S) {
+                report(err, MOE_ERR_DEVICE, kSiteCombineRow, static_cast<int32_t>(t));
+                continue;
+            }
+            const float w = G[t * k + j];
+            float v[V];
+            Vec<T>::load(Y + static_cast<int64_t>(row) * d + c, v);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] = fmaf(w, v[i], acc[i]);
+        }
+        Vec<T>::store(y + t * d + c, acc);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const moe_shape &s, const void *Y_slot, const int32_t *inv_perm,
+                           const float *G, void *y, int32_t *err, cudaStream_t st) {
+    if (s.T == 0) return cudaSuccess;
+    const unsigned blocks = static_cast<unsigned>((s.T + 7) / 8);
+    if (s.dtype == MOE_BF16)
+        combine_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(Y_slot), inv_perm, G, s.T, s.d, s.k, slots(s),
+            static_cast<__nv_bfloat16 *>(y), err);
+    else
+        combine_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float *>(Y_slot), inv_perm,
+                                                      G, s.T, s.d, s.k, slots(s),
+                                                      static_cast<float *>(y), err);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

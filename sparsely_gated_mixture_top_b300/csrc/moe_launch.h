@@ -1,0 +1,100 @@
+// moe_launch.h -- host-side internals shared by the library's .cu files: the
+// workspace layout and the launchers of each stage.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kRouteChunk = 1024;  // slots ranked per block by the routing kernels
+constexpr int kTcRows = 128;       // rows per tensor-core FFN tile (MMA M)
+constexpr int kSimtRows = 64;      // rows per fp32 SIMT FFN tile
+
+inline int gate_cols(const moe_shape &s) { return s.groups == 0 ? s.n : s.groups + s.n; }
+inline int64_t slots(const moe_shape &s) { return s.T * static_cast<int64_t>(s.k); }
+inline size_t dtype_bytes(const moe_shape &s) { return s.dtype == MOE_BF16 ? 2 : 4; }
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Byte offsets of every region of a workspace (all 256-byte aligned).
+struct WsLayout {
+    size_t header = 0;
+    size_t scores = 0;      // gate scores H [T, C] fp32
+    size_t local_rank = 0;  // [S] int32, rank of a slot among same-expert slots of its chunk
+    size_t chunk = 0;       // [chunks, n] int32, per-chunk expert counts, then bases
+    size_t imp64 = 0;       // [n] double, importance accumulated in fp64
+    size_t counts = 0;      // [n] int32 (used when the caller does not pass counts)
+    size_t offsets = 0;     // [n + 1] int32
+    size_t perm = 0;        // [S] int32
+    size_t inv_perm = 0;    // [S] int32
+    size_t importance = 0;  // [n] fp32
+    size_t cv2 = 0;         // [1] fp32
+    size_t tiles = 0;       // [n + 1] int32 row-tile starts of the FFN schedule
+    size_t xperm = 0;       // [S, d] dtype, x rows in expert order
+    size_t hidden = 0;      // [S, h] dtype, hidden activations in expert order
+    size_t yslot = 0;       // [S, d] dtype, expert outputs in expert order
+    size_t total = 0;
+};
+
+inline WsLayout ws_layout(const moe_shape &s) {
+    WsLayout L;
+    const size_t S = static_cast<size_t>(slots(s));
+    const size_t n = static_cast<size_t>(s.n);
+    const size_t C = static_cast<size_t>(gate_cols(s));
+    const size_t chunks = (S + kRouteChunk - 1) / kRouteChunk;
+    const size_t eb = dtype_bytes(s);
+    size_t o = 256;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.scores = take(static_cast<size_t>(s.T) * C * 4);
+    L.local_rank = take(S * 4);
+    L.chunk = take(chunks * n * 4);
+    L.imp64 = take(n * 8);
+    L.counts = take(n * 4);
+    L.offsets = take((n + 1) * 4);
+    L.perm = take(S * 4);
+    L.inv_perm = take(S * 4);
+    L.importance = take(n * 4);
+    L.cv2 = take(4);
+    L.tiles = take((n + 1) * 4);
+    L.xperm = take(S * static_cast<size_t>(s.d) * eb);
+    L.hidden = take(S * static_cast<size_t>(s.h) * eb);
+    L.yslot = take(S * static_cast<size_t>(s.d) * eb);
+    L.total = o;
+    return L;
+}
+
+template <typename T>
+inline T *ws_ptr(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+// Stage launchers (each returns the launch error, if any).
+cudaError_t launch_gate(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
+                        const float *bg, const float *eps, int32_t *idx, float *G, float *Hbuf,
+                        cudaStream_t st);
+
+cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float *G,
+                            int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                            float *importance, float *cv2, void *ws, const WsLayout &L,
+                            cudaStream_t st);
+
+cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *perm,
+                              const int32_t *offsets, const void *W1, const float *b1,
+                              const void *W2, const float *b2, void *Y_slot, void *ws,
+                              const WsLayout &L, cudaStream_t st);
+
+cudaError_t launch_combine(const moe_shape &s, const void *Y_slot, const int32_t *inv_perm,
+                           const float *G, void *y, int32_t *err, cudaStream_t st);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace moe

@@ -1,0 +1,214 @@
+// route.cu -- dispatch of the S = T*k slots to expert-contiguous rows.
+//
+// The pages' conditional computation ("MoE:稀疏门控混合专家", section 二: experts
+// with weight 0 are not computed) needs each expert's rows gathered together;
+// each expert then sees about k*b/n rows ("Outrageously Large Neural Networks -
+// 中文验证版", section 瓶颈).  This is a deterministic counting sort:
+//
+//   route_rank      per chunk of 1024 slots: the rank of each slot among the
+//                   earlier slots of its chunk with the same expert (warp
+//                   __match_any + warps taken in order), and the chunk's
+//                   per-expert counts
+//   route_colscan   per expert, an exclusive scan down the chunks (chunk bases)
+//                   and the expert's total count
+//   route_offsets   exclusive scan of the counts over the experts
+//   route_scatter   row = offsets[e] + chunk base + local rank: perm, inv_perm
+//   route_importance  per expert, sum of G over its rows in row order (fp64)
+//   route_cv2       population variance / mean^2 of the importance vector
+//
+// Integer work only until the importance; the permutation is stable, so the
+// same idx always gives the same perm bit for bit.
+#include "moe_device.cuh"
+#include "moe_launch.h"
+
+namespace moe {
+
+namespace {
+
+__global__ void __launch_bounds__(1024) route_rank(const int32_t *__restrict__ idx, int64_t S,
+                                                   int n, int32_t *__restrict__ local_rank,
+                                                   int32_t *__restrict__ chunk, int32_t *err) {
+    extern __shared__ int32_t cnt[];  // [n]
+    __shared__ int32_t base_sh[32][32];
+    for (int e = threadIdx.x; e < n; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t s = static_cast<int64_t>(blockIdx.x) * kRouteChunk + threadIdx.x;
+    int e = -1;
+    if (s < S) {
+        e = idx[s];
+        if (e < 0 || e >= n) {
+            report(err, MOE_ERR_DEVICE, kSiteRouteIdx, static_cast<int32_t>(s));
+            e = -1;
+        }
+    }
+    const unsigned mask = __match_any_sync(0xffffffffu, e);
+    const int leader = __ffs(mask) - 1;
+    const int rank_in_warp = __popc(mask & ((1u << lane) - 1u));
+    // Warps take their turn in slot order, so ranks follow slot order.
+    for (int w = 0; w < 32; ++w) {
+        if (warp == w && lane == leader && e >= 0) {
+            base_sh[w][lane] = cnt[e];
+            cnt[e] += __popc(mask);
+        }
+        __syncthreads();
+    }
+    if (e >= 0) local_rank[s] = base_sh[warp][leader] + rank_in_warp;
+    int32_t *row = chunk + static_cast<int64_t>(blockIdx.x) * n;
+    for (int ee = threadIdx.x; ee < n; ee += blockDim.x) row[ee] = cnt[ee];
+}
+
+// Block (32 x 32): 32 experts (x) by 32 chunk segments (y).
+__global__ void __launch_bounds__(1024) route_colscan(int32_t *__restrict__ chunk, int chunks,
+                                                      int n, int32_t *__restrict__ counts) {
+    __shared__ int32_t part[32][33];
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int e = blockIdx.x * 32 + tx;
+    const int seg = (chunks + 31) / 32;
+    const int b0 = ty * seg, b1 = min(chunks, b0 + seg);
+    int32_t sum = 0;
+    if (e < n)
+        for (int b = b0; b < b1; ++b) sum += chunk[static_cast<int64_t>(b) * n + e];
+    part[ty][tx] = sum;
+    __syncthreads();
+    if (ty == 0) {
+        int32_t run = 0;
+        for (int y = 0; y < 32; ++y) {
+            const int32_t v = part[y][tx];
+            part[y][tx] = run;
+            run += v;
+        }
+        if (e < n) counts[e] = run;
+    }
+    __syncthreads();
+    if (e < n) {
+        int32_t run = part[ty][tx];
+        for (int b = b0; b < b1; ++b) {
+            const int64_t at = static_cast<int64_t>(b) * n + e;
+            const int32_t v = chunk[at];
+            chunk[at] = run;
+            run += v;
+        }
+    }
+}
+
+// One block of 1024 threads: offsets = exclusive scan of counts, offsets[n] = total.
+__global__ void __launch_bounds__(1024) route_offsets(const int32_t *__restrict__ counts, int n,
+                                                      int32_t *__restrict__ offsets) {
+    __shared__ int32_t part[1024];
+    const int per = (n + 1023) / 1024;
+    const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
+    int32_t sum = 0;
+    for (int i = i0; i < i1; ++i) sum += counts[i];
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
+        const int32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
+    for (int i = i0; i < i1; ++i) {
+        offsets[i] = run;
+        run += counts[i];
+    }
+    if (threadIdx.x == 1023) offsets[n] = part[1023];
+}
+
+__global__ void route_scatter(const int32_t *__restrict__ idx, int64_t S, int n,
+                              const int32_t *__restrict__ offsets,
+                              const int32_t *__restrict__ chunk,
+                              const int32_t *__restrict__ local_rank, int32_t *__restrict__ perm,
+                              int32_t *__restrict__ inv_perm) {
+    const int64_t s = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (s >= S) return;
+    const int e = idx[s];
+    if (e < 0 || e >= n) {
+        inv_perm[s] = -1;
+    } else {
+        const int32_t row = offsets[e] + chunk[(s / kRouteChunk) * n + e] + local_rank[s];
+        perm[row] = static_cast<int32_t>(s);
+        inv_perm[s] = row;
+    }
+    if (s >= offsets[n]) perm[s] = -1;  // rows left empty by invalid slots
+}
+
+// One warp per expert; fp64 lane sums in row order, then a fixed shuffle tree.
+__global__ void route_importance(const float *__restrict__ G, const int32_t *__restrict__ perm,
+                                 const int32_t *__restrict__ offsets, int n,
+                                 float *__restrict__ importance, double *__restrict__ imp64) {
+    const int e = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (e >= n) return;
+    const int lane = threadIdx.x & 31;
+    double acc = 0.0;
+    for (int r = offsets[e] + lane; r < offsets[e + 1]; r += 32) acc += static_cast<double>(G[perm[r]]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+        importance[e] = static_cast<float>(acc);
+        imp64[e] = acc;
+    }
+}
+
+__device__ double block_sum_1024(double v, double *sh) {
+    sh[threadIdx.x] = v;
+    __syncthreads();
+    for (int o = 512; o > 0; o >>= 1) {
+        if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+        __syncthreads();
+    }
+    const double r = sh[0];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(1024) route_cv2(const double *__restrict__ imp64, int n,
+                                                  float *__restrict__ cv2) {
+    __shared__ double sh[1024];
+    double s = 0.0;
+    for (int e = threadIdx.x; e < n; e += 1024) s += imp64[e];
+    const double mean = block_sum_1024(s, sh) / n;
+    double q = 0.0;
+    for (int e = threadIdx.x; e < n; e += 1024) q += (imp64[e] - mean) * (imp64[e] - mean);
+    const double var = block_sum_1024(q, sh) / n;
+    if (threadIdx.x == 0) cv2[0] = mean != 0.0 ? static_cast<float>(var / (mean * mean)) : 0.0f;
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float *G,
+                            int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                            float *importance, float *cv2, void *ws, const WsLayout &L,
+                            cudaStream_t st) {
+    const int64_t S = slots(s);
+    const int n = s.n;
+    int32_t *err = ws_ptr<int32_t>(ws, 0);
+    if (S == 0) {
+        cudaMemsetAsync(counts, 0, sizeof(int32_t) * n, st);
+        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (n + 1), st);
+        cudaMemsetAsync(importance, 0, sizeof(float) * n, st);
+        cudaMemsetAsync(cv2, 0, sizeof(float), st);
+        return cudaGetLastError();
+    }
+    const int chunks = static_cast<int>((S + kRouteChunk - 1) / kRouteChunk);
+    int32_t *local_rank = ws_ptr<int32_t>(ws, L.local_rank);
+    int32_t *chunk = ws_ptr<int32_t>(ws, L.chunk);
+    double *imp64 = ws_ptr<double>(ws, L.imp64);
+    const size_t smem = sizeof(int32_t) * n;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(route_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    route_rank<<<chunks, 1024, smem, st>>>(idx, S, n, local_rank, chunk, err);
+    route_colscan<<<(n + 31) / 32, dim3(32, 32), 0, st>>>(chunk, chunks, n, counts);
+    route_offsets<<<1, 1024, 0, st>>>(counts, n, offsets);
+    route_scatter<<<static_cast<unsigned>((S + 255) / 256), 256, 0, st>>>(
+        idx, S, n, offsets, chunk, local_rank, perm, inv_perm);
+    route_importance<<<(n + 7) / 8, 256, 0, st>>>(G, perm, offsets, n, importance, imp64);
+    route_cv2<<<1, 1024, 0, st>>>(imp64, n, cv2);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
