@@ -153,6 +153,33 @@ MOE_API moe_status moe_dispatch(const moe_shape *shape, const int32_t *idx, cons
                         float *importance, float *cv2, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_dispatch without a workspace.  The pages have no counterpart to this
+ * call: it exists for callers that cannot allocate device memory (code
+ * running inside another framework's fixed memory pool, plug-ins whose host
+ * owns every allocation, latency-critical paths where an allocation may block
+ * or fail).  It computes exactly what moe_dispatch computes, with the same
+ * kernels, but keeps their scratch in one array of static device storage
+ * inside this library (8 MiB, resident on every device that loads the
+ * library until the process exits).  It calls no allocation routine.
+ *   - Limit: the scratch needed is 256 B + 4*S + 4*ceil(S/1024)*n + 8*n
+ *     bytes (each term rounded up to 256 B); a shape that needs more than
+ *     8 MiB returns MOE_ERR_UNSUPPORTED and enqueues nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents (each call clears the part that must start at zero).
+ *     Calls whose work overlaps on the GPU (different streams, or different
+ *     host threads) race on it: serialise them.
+ *   - An idx entry outside [0, n) is skipped as in moe_dispatch (inv_perm = -1),
+ *     but there is no workspace to carry the error word, so it is not reported.
+ */
+MOE_API moe_status moe_dispatch_noalloc(const moe_shape *shape, const int32_t *idx,
+                                        const float *G, int32_t *counts, int32_t *offsets,
+                                        int32_t *perm, int32_t *inv_perm, float *importance,
+                                        float *cv2, void *stream);
+
+/*
  * Expert FFNs on expert-contiguous rows ("MoE:稀疏门控混合专家", section 二):
  * for every expert e and row r in [offsets[e], offsets[e+1]), with token
  * t = perm[r] / k,  Y_slot[r] = W2[e] . ReLU(W1[e] . x[t] + b1[e]) + b2[e].

@@ -29,7 +29,7 @@ MOE_BF16 = 1
 
 EXPORTS = ("moe_version", "moe_status_string", "moe_validate", "moe_workspace_bytes",
            "moe_workspace_init", "moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine",
-           "moe_forward", "moe_check")
+           "moe_forward", "moe_check", "moe_dispatch_noalloc")
 
 
 class MoEShape(ctypes.Structure):
@@ -61,8 +61,9 @@ def _load():
     lib.moe_combine.argtypes = [shp] + [vp] * 5 + [sz, vp]
     lib.moe_forward.argtypes = [shp] + [vp] * 16 + [sz, vp]
     lib.moe_check.argtypes = [vp, vp]
+    lib.moe_dispatch_noalloc.argtypes = [shp] + [vp] * 9
     for f in ("moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
-              "moe_check"):
+              "moe_check", "moe_dispatch_noalloc"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -129,6 +130,16 @@ def moe_dispatch(shape, idx, G, counts, offsets, perm, inv_perm, importance, cv2
     _ok("moe_dispatch", lib.moe_dispatch(ctypes.byref(shape), _p(idx), _p(G), _p(counts),
                                          _p(offsets), _p(perm), _p(inv_perm), _p(importance),
                                          _p(cv2), _p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_dispatch_noalloc(shape, idx, G, counts, offsets, perm, inv_perm, importance, cv2,
+                         stream=None):
+    """moe_dispatch for callers that cannot allocate: the routing scratch lives in a
+    fixed 8 MiB static device array inside the library (no workspace argument).
+    Calls that overlap on the GPU share that array and must be serialised."""
+    _ok("moe_dispatch_noalloc", lib.moe_dispatch_noalloc(
+        ctypes.byref(shape), _p(idx), _p(G), _p(counts), _p(offsets), _p(perm), _p(inv_perm),
+        _p(importance), _p(cv2), _stream(stream)))
 
 
 def moe_expert_ffn(shape, x, perm, offsets, W1, b1, W2, b2, Y_slot, ws, stream=None):
