@@ -106,8 +106,7 @@ moe_status moe_gate(const moe_shape *s, const void *x, const float *Wg, const fl
     if (s->T == 0) return MOE_OK;
     const WsLayout L = ws_layout(*s);
     return cuda_status(launch_gate(*s, x, Wg, s->noisy ? Wn : nullptr, bg, s->noisy ? eps : nullptr,
-                                   idx, G, ws_ptr<float>(ws, L.scores),
-                                   static_cast<cudaStream_t>(stream)));
+                                   idx, G, ws, L, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_dispatch(const moe_shape *s, const int32_t *idx, const float *G, int32_t *counts,
@@ -178,7 +177,7 @@ moe_status moe_forward(const moe_shape *s, const void *x, const float *Wg, const
     cudaError_t e = cudaSuccess;
     if (s->T > 0)
         e = launch_gate(*s, x, Wg, s->noisy ? Wn : nullptr, bg, s->noisy ? eps : nullptr, idx, G,
-                        ws_ptr<float>(ws, L.scores), st);
+                        ws, L, st);
     if (e == cudaSuccess) e = launch_dispatch(*s, idx, G, cnt, off, perm, inv, imp, c2, ws, L, st);
     if (e == cudaSuccess) e = launch_expert_ffn(*s, x, perm, off, W1, b1, W2, b2, yslot, ws, L, st);
     if (e == cudaSuccess) e = launch_combine(*s, yslot, inv, G, y, ws_ptr<int32_t>(ws, 0), st);

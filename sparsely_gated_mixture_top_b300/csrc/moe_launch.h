@@ -20,10 +20,16 @@ inline size_t dtype_bytes(const moe_shape &s) { return s.dtype == MOE_BF16 ? 2 :
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Tensor-core gate (gate_tc.cu): whether it handles a shape, and the bytes of
+// its packed split-bf16 gate matrices.
+bool gate_tc_supported(const moe_shape &s);
+size_t gate_tc_pack_bytes(const moe_shape &s);
+
 // Byte offsets of every region of a workspace (all 256-byte aligned).
 struct WsLayout {
     size_t header = 0;
-    size_t scores = 0;      // gate scores H [T, C] fp32
+    size_t scores = 0;      // gate scores H [T, C] fp32 (SIMT gate only)
+    size_t gpack = 0;       // packed bf16 hi/lo gate matrices (tensor-core gate only)
     size_t local_rank = 0;  // [S] int32, rank of a slot among same-expert slots of its chunk
     size_t chunk = 0;       // [chunks, n] int32, per-chunk expert counts, then bases
     size_t imp64 = 0;       // [n] double, importance accumulated in fp64
@@ -53,7 +59,9 @@ inline WsLayout ws_layout(const moe_shape &s) {
         o = align_up(o + bytes, 256);
         return at;
     };
-    L.scores = take(static_cast<size_t>(s.T) * C * 4);
+    const bool tc_gate = gate_tc_supported(s);
+    L.scores = take(tc_gate ? 0 : static_cast<size_t>(s.T) * C * 4);
+    L.gpack = take(tc_gate ? gate_tc_pack_bytes(s) : 0);
     L.local_rank = take(S * 4);
     L.chunk = take(chunks * n * 4);
     L.imp64 = take(n * 8);
@@ -78,8 +86,11 @@ inline T *ws_ptr(void *ws, size_t off) {
 
 // Stage launchers (each returns the launch error, if any).
 cudaError_t launch_gate(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
-                        const float *bg, const float *eps, int32_t *idx, float *G, float *Hbuf,
-                        cudaStream_t st);
+                        const float *bg, const float *eps, int32_t *idx, float *G, void *ws,
+                        const WsLayout &L, cudaStream_t st);
+cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
+                           const float *bg, const float *eps, int32_t *idx, float *G, void *pack,
+                           int32_t *err, cudaStream_t st);
 
 cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float *G,
                             int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,

@@ -35,6 +35,10 @@ SMALL = [
     W("hier_one_group", T=64, d=64, h=128, n=12, k=3, groups=1, k_groups=1, seed=21),
     W("wide_k16", T=128, d=64, h=128, n=40, k=16, seed=22),
     W("bn256_two_tiles", T=700, d=512, h=1024, n=3, k=1, bias_std=0.1, seed=23),
+    W("hier_wide_inner_cuda_core_gate", T=50, d=64, h=64, n=32, k=8, groups=2, k_groups=1,
+      seed=24),
+    W("hier_stream_x", T=130, d=576, h=128, n=12, k=2, groups=3, k_groups=1, seed=25),
+    W("flat_stream_x_k1", T=300, d=640, h=64, n=70, k=1, bias_std=0.1, seed=26),
 ]
 
 
