@@ -16,14 +16,20 @@
 //   gate_tc         persistent over 128-token tiles.  Warp 0 issues TMA loads,
 //                   warp 1 issues tcgen05.mma (M=128 tokens, N=128 = 64 clean +
 //                   64 noise columns, hi then lo pass into one fp32 accumulator,
-//                   double-buffered in tensor memory), warps 2..5 are the
-//                   epilogue: thread r owns token r of the tile (tensor-memory
-//                   lane r), adds b_g, eps * softplus(noise score), keeps its
-//                   running top-k in registers (KeepTopK, ties to the lower
-//                   index) and finishes with the softmax over the k survivors.
+//                   double-buffered in tensor memory), warps 2..9 are the
+//                   epilogue: two warps per tensor-memory lane quarter, each
+//                   owning one half of every chunk's columns for its 32 tokens
+//                   (thread r = token r = tensor-memory lane r).  A first pass
+//                   over 16 columns at a time bounds each noisy score from
+//                   above without evaluating softplus and flags only the
+//                   columns that can still enter the running top-k; a second
+//                   pass computes H = clean (+ b_g) + eps * softplus(noise) for
+//                   the flagged ones and inserts them (KeepTopK, ties to the
+//                   lower index).  The halves merge their lists through shared
+//                   memory and the softmax runs over the k survivors.
 //                   Hierarchical gating picks the groups from the first chunks
-//                   and only then looks at (and reads eps for) the inner
-//                   columns of its chosen groups.
+//                   (both halves merge them) and only then looks at (and reads
+//                   eps for) the inner columns of its chosen groups.
 // x stays resident in shared memory for the whole tile when d <= 512;
 // otherwise each stage carries its x block with the W blocks.
 #include "moe_device.cuh"
@@ -102,12 +108,17 @@ struct TopK {
             i[q] = INT_MAX;
         }
     }
-    // Entry kk-1 (kk <= KM) is the current k-th best.
+    // Entry kk-1 (kk <= KM) is the current k-th best.  The empty asm keeps each
+    // entry an opaque register value, so that the compiler does not turn this
+    // select into an indexed load (which would move the list to local memory).
     __device__ __forceinline__ float kth(int kk) const {
         float r = v[0];
 #pragma unroll
-        for (int q = 0; q < KM; ++q)
-            if (q == kk - 1) r = v[q];
+        for (int q = 0; q < KM; ++q) {
+            float c = v[q];
+            asm("" : "+f"(c));
+            if (q == kk - 1) r = c;
+        }
         return r;
     }
     __device__ __forceinline__ void insert(float cv, int ci) {
@@ -145,13 +156,21 @@ __device__ __forceinline__ void softmax_top(const TopK<KM> &t, int kk, float (&w
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <bool kResident>
+constexpr int kGateEpiWarps = 8;                 // two per tensor-memory lane quarter
+constexpr int kGateThreads = 32 * (2 + kGateEpiWarps);
+
+template <bool kResident, bool kHier, int KM>
 struct GateCfg {
-    static constexpr int kStages = kResident ? 5 : 4;
+    static constexpr int kStages = 4;
     static constexpr int kStageBytes = kResident ? kKBytes : 3 * kKBytes;
     static constexpr int kXBytes = kResident ? 8 * kKBytes : 0;  // d <= 512
+    // Exchange between the two column halves: the group lists of both halves
+    // (hierarchical only) and the final lists of half 1, [slot][token] order.
+    static constexpr int kPrimSlots = kHier ? 2 * KM : 0;
+    static constexpr int kFinalSlots = kHier ? KM * KM : KM;
+    static constexpr int kXchBytes = (kPrimSlots + kFinalSlots) * kGateRows * 8;
     static constexpr int kBarBytes = 8 * (2 * kStages + 7) + 16;
-    static constexpr int kSmem = kXBytes + kStages * kStageBytes + 1024 + kBarBytes;
+    static constexpr int kSmem = kXBytes + kStages * kStageBytes + kXchBytes + 1024 + kBarBytes;
     static constexpr uint32_t kTmemCols = 256;  // 2 accumulators x 128 columns
 };
 
@@ -169,18 +188,49 @@ struct GateArgs {
     int32_t *err;
 };
 
+// Named barrier of the eight epilogue warps.
+__device__ __forceinline__ void epi_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kGateEpiWarps) : "memory");
+}
+
+// eps[row][col0 + j] for the 32 columns j of one chunk half whose bit is set
+// in `live` (0 elsewhere).  Vector loads when the row stride and col0 allow
+// 16-byte alignment (then every live group of 4 is all live).
+__device__ __forceinline__ void load_eps32(const float *__restrict__ row, int col0, int C,
+                                           bool vec, uint32_t live, float (&ev)[32]) {
+    if (vec) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (col0 + 4 * q < C && ((live >> (4 * q)) & 1u))
+                v = __ldg(reinterpret_cast<const float4 *>(row + col0 + 4 * q));
+            ev[4 * q] = v.x;
+            ev[4 * q + 1] = v.y;
+            ev[4 * q + 2] = v.z;
+            ev[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            ev[j] = (col0 + j < C && ((live >> j) & 1u)) ? __ldg(row + col0 + j) : 0.0f;
+    }
+}
+
 // KM: list size for flat (>= k) or for each hierarchical level (>= k_groups, k_inner).
 template <bool kResident, bool kHier, int KM>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGateThreads, 1)
     gate_tc(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapHi,
             const __grid_constant__ CUtensorMap mapLo, const GateArgs a) {
-    using Cfg = GateCfg<kResident>;
+    using Cfg = GateCfg<kResident, kHier, KM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sX = smem;                        // resident x tile (kResident)
     uint8_t *sS = smem + Cfg::kXBytes;         // stage ring
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sS + Cfg::kStages * Cfg::kStageBytes);
+    uint8_t *sXch = sS + Cfg::kStages * Cfg::kStageBytes;
+    float *xch_v = reinterpret_cast<float *>(sXch);
+    int *xch_i = reinterpret_cast<int *>(sXch + (Cfg::kPrimSlots + Cfg::kFinalSlots) * kGateRows * 4);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sXch + Cfg::kXchBytes);
     // full[S], empty[S], tfull[2], tempty[2], xfull, xempty, drain
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Cfg::kStages + 7);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
@@ -201,7 +251,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull(b), 1);
-            mbar_init(tempty(b), 128);
+            mbar_init(tempty(b), 32 * kGateEpiWarps);
         }
         mbar_init(xfull, 1);
         mbar_init(xempty, 1);
@@ -365,76 +415,150 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ------------------------------ epilogue ------------------------------
+        // Warp w (2..9) reads tensor-memory lanes 32*(w%4).. (token r of the
+        // tile) and column half `half` of every chunk: clean columns
+        // half*32 .. +32 and the matching noise columns 64 + half*32 .. +32.
+        // Each thread keeps the running top-k of its half; the halves merge
+        // through shared memory at the end of the tile (hierarchical: also
+        // after the group columns, since both halves need the chosen groups).
+        const int half = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         const int k_inner = kHier ? a.k / a.k_groups : a.k;
+        const int kk_prim = kHier ? a.k_groups : a.k;
+        const bool vec_eps = (a.C & 3) == 0;
+        constexpr int kFinalOff = Cfg::kPrimSlots * kGateRows;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
             const int64_t t = static_cast<int64_t>(tile) * kGateRows + r;
             const bool valid = t < a.T;
-            const float *eps_row = (valid && a.noisy) ? a.eps + t * a.C : nullptr;
-            TopK<KM> prim;      // flat: the only list; hierarchical: the groups
+            const bool noisy = valid && a.noisy;
+            const float *eps_row = noisy ? a.eps + t * a.C : nullptr;
+            TopK<KM> prim;  // flat: the only list; hierarchical: the groups
             TopK<KM> inner[kHier ? KM : 1];
             prim.reset();
 #pragma unroll
             for (int q = 0; q < (kHier ? KM : 1); ++q) inner[q].reset();
             float gw[KM];
-            int kk_prim = kHier ? a.k_groups : a.k;
+            int glo[KM];  // hierarchical: first inner column of each chosen group
+#pragma unroll
+            for (int q = 0; q < KM; ++q) {
+                gw[q] = 0.0f;
+                glo[q] = -0x40000000;
+            }
             for (int c = 0; c < a.chunks; ++c) {
-                if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, a.err, kSiteTcEpilogue)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (kHier && c == a.prim_chunks) softmax_top<KM>(prim, kk_prim, gw);
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t cv[32], nv[32];
-                    const uint32_t col = static_cast<uint32_t>(acc * 128 + half * 32);
-                    tmem_ld_32x32b_x32(tmem_base + lane_addr + col, cv);
-                    tmem_ld_32x32b_x32(tmem_base + lane_addr + col + 64, nv);
-                    tmem_ld_wait();
-                    if (half == 1) {
-                        tc_fence_before();
-                        mbar_arrive(tempty(acc));  // accumulator fully read
+                const bool inner_chunk = kHier && c >= a.prim_chunks;
+                if (kHier && c == a.prim_chunks) {
+                    // both halves publish their group lists and merge the other's
+#pragma unroll
+                    for (int q = 0; q < KM; ++q) {
+                        xch_v[(half * KM + q) * kGateRows + r] = prim.v[q];
+                        xch_i[(half * KM + q) * kGateRows + r] = prim.i[q];
                     }
-                    if (!valid) continue;
-                    const int lc0 = c * kGateChunk + half * 32;
+                    epi_bar();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int lc = lc0 + j;
-                        int col_src;
-                        int rank = 0;
-                        if (!kHier) {
-                            if (lc >= a.C) break;
-                            col_src = lc;
-                        } else if (c < a.prim_chunks) {
-                            if (lc >= a.groups) break;
-                            col_src = lc;
-                        } else {
-                            const int ic = lc - a.prim_pad;
-                            if (ic >= a.n) break;
-                            const int g = ic / a.m;
-                            rank = -1;
+                    for (int q = 0; q < KM; ++q)
+                        prim.insert(xch_v[((1 - half) * KM + q) * kGateRows + r],
+                                    xch_i[((1 - half) * KM + q) * kGateRows + r]);
+                    softmax_top<KM>(prim, kk_prim, gw);
 #pragma unroll
-                            for (int q = 0; q < KM; ++q)
-                                if (q < a.k_groups && prim.i[q] == g) rank = q;
-                            if (rank < 0) continue;
-                            col_src = a.groups + ic;
+                    for (int q = 0; q < KM; ++q)
+                        if (q < a.k_groups) glo[q] = prim.i[q] * a.m;
+                }
+                // columns of this chunk half (score index space of the list)
+                const int col0 = inner_chunk ? (c - a.prim_chunks) * kGateChunk + half * 32
+                                             : c * kGateChunk + half * 32;
+                const int ncols = inner_chunk ? a.n : (kHier ? a.groups : a.C);
+                const int ecol0 = inner_chunk ? a.groups + col0 : col0;  // eps / bg column
+                float ev[32];
+                if (eps_row && col0 < ncols) {
+                    uint32_t live = 0xffffffffu;
+                    bool vec = vec_eps;
+                    if (inner_chunk) {
+                        live = 0;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            #pragma unroll
+                            for (int qq = 0; qq < KM; ++qq)
+                                if (qq < a.k_groups && static_cast<unsigned>(col0 + j - glo[qq]) <
+                                                           static_cast<unsigned>(a.m))
+                                    live |= 1u << j;
+                        vec = vec && (ecol0 & 3) == 0 && (a.m & 3) == 0;
+                    }
+                    load_eps32(eps_row, ecol0, a.C, vec, live, ev);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ev[j] = 0.0f;
+                }
+                if (ok && !mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, a.err,
+                                             kSiteTcEpilogue))
+                    ok = false;
+                if (ok) {
+                    tc_fence_after();
+                    // Pass 1 thresholds: the k-th entry of each list, fixed for the span.
+                    const float thr_p = prim.kth(kk_prim);
+                    float thr_i[kHier ? KM : 1];
+#pragma unroll
+                    for (int qq = 0; qq < (kHier ? KM : 1); ++qq) thr_i[qq] = inner[qq].kth(k_inner);
+#pragma unroll
+                    for (int piece = 0; piece < 2; ++piece) {
+                        uint32_t cv[16], nv[16];
+                        const uint32_t col = static_cast<uint32_t>(acc * 128 + half * 32 + piece * 16);
+                        tmem_ld_32x32b_x16(tmem_base + lane_addr + col, cv);
+                        tmem_ld_32x32b_x16(tmem_base + lane_addr + col + 64, nv);
+                        tmem_ld_wait();
+                        if (piece == 1) {
+                            tc_fence_before();
+                            mbar_arrive(tempty(acc));  // this half of the accumulator is read
                         }
-                        float hv = __uint_as_float(cv[j]);
-                        if (a.bg) hv += a.bg[col_src];
-                        if (eps_row) hv += eps_row[col_src] * softplus_f(__uint_as_float(nv[j]));
-                        const int id = kHier && c >= a.prim_chunks ? (lc - a.prim_pad) % a.m : col_src;
-                        if (!kHier || c < a.prim_chunks) {
-                            prim.insert(hv, id);
-                        } else {
+                        if (!valid) continue;
+                        // Pass 1: which columns' upper bound beats their list's k-th entry.
+                        uint32_t pass = 0;
 #pragma unroll
-                            for (int q = 0; q < (kHier ? KM : 1); ++q)
-                                if (q == rank) inner[q].insert(hv, id);
+                        for (int j = 0; j < 16; ++j) {
+                            const int sc = col0 + piece * 16 + j;
+                            float clean = __uint_as_float(cv[j]);
+                            if (a.bg && sc < ncols) clean += __ldg(a.bg + ecol0 + piece * 16 + j);
+                            cv[j] = __float_as_uint(clean);
+                            const float e = ev[piece * 16 + j];
+                            // softplus(z) is in [0, max(z, 0) + ln 2]: with eps <= 0 the
+                            // noise term can only lower the score, else it adds at most
+                            // eps * (max(z, 0) + 0.75) (an upper bound after fp32 rounding too).
+                            const float ub =
+                                noisy ? fmaf(fmaxf(e, 0.0f), fmaxf(__uint_as_float(nv[j]), 0.0f) + 0.75f, clean)
+                                      : clean;
+                            float thr = thr_p;
+                            if (inner_chunk) {
+                                thr = INFINITY;  // outside the chosen groups
+#pragma unroll
+                                for (int qq = 0; qq < (kHier ? KM : 1); ++qq)
+                                    if (qq < a.k_groups &&
+                                        static_cast<unsigned>(sc - glo[qq]) < static_cast<unsigned>(a.m))
+                                        thr = thr_i[qq];
+                            }
+                            if (sc < ncols && ub > thr) pass |= 1u << j;
+                        }
+                        // Pass 2 (rare): the exact noisy score and the insertion.
+                        if (pass) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                if (!((pass >> j) & 1u)) continue;
+                                const int sc = col0 + piece * 16 + j;
+                                float h = __uint_as_float(cv[j]);
+                                if (noisy) h += ev[piece * 16 + j] * softplus_f(__uint_as_float(nv[j]));
+                                if (!inner_chunk) {
+                                    prim.insert(h, sc);
+                                } else {
+#pragma unroll
+                                    for (int qq = 0; qq < (kHier ? KM : 1); ++qq)
+                                        if (qq < a.k_groups && static_cast<unsigned>(sc - glo[qq]) <
+                                                                   static_cast<unsigned>(a.m))
+                                            inner[qq].insert(h, sc - glo[qq]);
+                                }
+                            }
                         }
                     }
                 }
@@ -443,30 +567,58 @@ __global__ void __launch_bounds__(192, 1)
                     acc_phase ^= 1u;
                 }
             }
-            if (!ok || !valid) continue;
-            if (!kHier) {
-                float w[KM];
-                softmax_top<KM>(prim, a.k, w);
+            // half 1 hands its lists to half 0, which merges and writes the token
+            epi_bar();  // half 0 is done with the previous tile's exchange
+            if (half == 1) {
+                if (!kHier) {
 #pragma unroll
-                for (int q = 0; q < KM; ++q)
-                    if (q < a.k) {
-                        a.idx[t * a.k + q] = prim.i[q];
-                        a.G[t * a.k + q] = w[q];
+                    for (int q = 0; q < KM; ++q) {
+                        xch_v[kFinalOff + q * kGateRows + r] = prim.v[q];
+                        xch_i[kFinalOff + q * kGateRows + r] = prim.i[q];
                     }
-            } else {
-                if (a.prim_chunks == a.chunks) softmax_top<KM>(prim, kk_prim, gw);
+                } else {
 #pragma unroll
-                for (int q = 0; q < KM; ++q) {
-                    if (q >= a.k_groups) break;
-                    float wi[KM];
-                    softmax_top<KM>(inner[q], k_inner, wi);
-                    const int g = prim.i[q];
+                    for (int g = 0; g < (kHier ? KM : 1); ++g)
 #pragma unroll
-                    for (int e = 0; e < KM; ++e)
-                        if (e < k_inner) {
-                            a.idx[t * a.k + q * k_inner + e] = g * a.m + inner[q].i[e];
-                            a.G[t * a.k + q * k_inner + e] = gw[q] * wi[e];
+                        for (int q = 0; q < KM; ++q) {
+                            xch_v[kFinalOff + (g * KM + q) * kGateRows + r] = inner[g].v[q];
+                            xch_i[kFinalOff + (g * KM + q) * kGateRows + r] = inner[g].i[q];
                         }
+                }
+            }
+            epi_bar();
+            if (half == 0 && ok && valid) {
+                if (!kHier) {
+#pragma unroll
+                    for (int q = 0; q < KM; ++q)
+                        prim.insert(xch_v[kFinalOff + q * kGateRows + r],
+                                    xch_i[kFinalOff + q * kGateRows + r]);
+                    float w[KM];
+                    softmax_top<KM>(prim, a.k, w);
+#pragma unroll
+                    for (int q = 0; q < KM; ++q)
+                        if (q < a.k) {
+                            a.idx[t * a.k + q] = prim.i[q];
+                            a.G[t * a.k + q] = w[q];
+                        }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < (kHier ? KM : 1); ++g) {
+                        if (g >= a.k_groups) break;
+#pragma unroll
+                        for (int q = 0; q < KM; ++q)
+                            inner[g].insert(xch_v[kFinalOff + (g * KM + q) * kGateRows + r],
+                                            xch_i[kFinalOff + (g * KM + q) * kGateRows + r]);
+                        float wi[KM];
+                        softmax_top<KM>(inner[g], k_inner, wi);
+                        const int grp = prim.i[g];
+#pragma unroll
+                        for (int e = 0; e < KM; ++e)
+                            if (e < k_inner) {
+                                a.idx[t * a.k + g * k_inner + e] = grp * a.m + inner[g].i[e];
+                                a.G[t * a.k + g * k_inner + e] = gw[g] * wi[e];
+                            }
+                    }
                 }
             }
         }
@@ -512,7 +664,7 @@ bool gate_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows) {
 template <bool kResident, bool kHier, int KM>
 cudaError_t launch_gate_tc_t(const CUtensorMap &mx, const CUtensorMap &mh, const CUtensorMap &ml,
                              const GateArgs &ga, int grid, cudaStream_t st) {
-    using Cfg = GateCfg<kResident>;
+    using Cfg = GateCfg<kResident, kHier, KM>;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
@@ -520,7 +672,7 @@ cudaError_t launch_gate_tc_t(const CUtensorMap &mx, const CUtensorMap &mh, const
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     });
     if (attr != cudaSuccess) return attr;
-    gate_tc<kResident, kHier, KM><<<grid, 192, Cfg::kSmem, st>>>(mx, mh, ml, ga);
+    gate_tc<kResident, kHier, KM><<<grid, kGateThreads, Cfg::kSmem, st>>>(mx, mh, ml, ga);
     return cudaGetLastError();
 }
 
