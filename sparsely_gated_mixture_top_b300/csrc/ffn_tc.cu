@@ -13,13 +13,17 @@
 // networks ("MoE:稀疏门控混合专家", section 二).
 //
 // Structure (one CTA per SM, persistent over a static tile sequence):
-//   warp 0       TMA producer: A and B tiles (128 x 64 and BN x 64, 128-byte
-//                swizzle) into a STAGES-deep shared-memory ring
+//   warp 0       TMA producer: per stage one 3-D copy each of A (128 rows) and
+//                B (BN rows), two 64-wide k-blocks, 128-byte swizzle, into a
+//                STAGES-deep shared-memory ring (few large copies: a copy
+//                costs a fixed issue time whatever its size)
 //   warp 1       allocates tensor memory; one lane issues tcgen05.mma
 //                (M = 128, N = BN, K = 16) and commits each stage back to the
 //                producer and each finished accumulator to the epilogue
-//   warps 2..5   epilogue: tcgen05.ld of the accumulator (each warp its 32
-//                lanes), bias, activation, bf16 rounding, stores
+//   warps 2..9   epilogue: tcgen05.ld of the accumulator (two warps per
+//                32-lane quarter, each one half of the columns, the next 32
+//                columns in flight while the current ones are converted),
+//                bias, activation, bf16 rounding, 16-byte stores
 // The accumulator is double-buffered in tensor memory (2 x BN columns) so
 // the epilogue of one tile overlaps the main loop of the next.  Every wait is
 // bounded; on a timeout the kernel records MOE_ERR_TIMEOUT, drains its own
@@ -36,9 +40,10 @@ namespace {
 template <int BN, int STAGES>
 struct TcCfg {
     static constexpr int kBM = kTcRows;
-    static constexpr int kBK = 64;
-    static constexpr int kABytes = kBM * kBK * 2;
-    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kBK = 64;       // K per swizzle atom row (128 bytes)
+    static constexpr int kKB = 2;        // k-blocks per stage (one 3-D TMA box each)
+    static constexpr int kABytes = kBM * kBK * 2 * kKB;
+    static constexpr int kBBytes = BN * kBK * 2 * kKB;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kBarBytes = 8 * (2 * STAGES + 5) + 16;
     static constexpr int kSmem = STAGES * kStageBytes + 1024 + kBarBytes;
@@ -81,12 +86,15 @@ __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, int32_
     return true;
 }
 
+constexpr int kFfnEpiWarps = 8;  // two per tensor-memory lane quarter
+constexpr int kFfnThreads = 32 * (2 + kFfnEpiWarps);
+
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kFfnThreads, 1)
     ffn_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const int32_t *__restrict__ offsets, const int32_t *__restrict__ tiles, int n,
                 int K, int N, const float *__restrict__ bias, int relu,
-                __nv_bfloat16 *__restrict__ out, int32_t *err) {
+                __nv_bfloat16 *__restrict__ out, int out_v8, int32_t *err) {
     using Cfg = TcCfg<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -111,7 +119,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull(b), 1);
-            mbar_init(tempty(b), 128);
+            mbar_init(tempty(b), 32 * kFfnEpiWarps);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -133,6 +141,7 @@ __global__ void __launch_bounds__(192, 1)
     const int ncb = N / BN;
     const int total = tiles[n] * ncb;
     const int kblocks = K / Cfg::kBK;
+    const int kstages = (kblocks + Cfg::kKB - 1) / Cfg::kKB;  // a missing last k-block reads as zeros
 
     if (warp == 0) {
         if (lane == 0) {
@@ -143,17 +152,17 @@ __global__ void __launch_bounds__(192, 1)
             for (int q = blockIdx.x; q < total && ok; q += gridDim.x) {
                 const TileInfo ti = decode_tile(q, ncb, tiles, n, offsets);
                 const int brow = ti.e * N + ti.cb * BN;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, err,
                                            kSiteTcProducer)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(full(stage), Cfg::kStageBytes);
-                    tma_load_2d(smem_u32(sA + stage * Cfg::kABytes), &mapA, full(stage),
-                                kb * Cfg::kBK, ti.row0);
-                    tma_load_2d(smem_u32(sB + stage * Cfg::kBBytes), &mapB, full(stage),
-                                kb * Cfg::kBK, brow);
+                    tma_load_3d(smem_u32(sA + stage * Cfg::kABytes), &mapA, full(stage), 0, ti.row0,
+                                ks * Cfg::kKB);
+                    tma_load_3d(smem_u32(sB + stage * Cfg::kBBytes), &mapB, full(stage), 0, brow,
+                                ks * Cfg::kKB);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -188,7 +197,7 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait_bounded(full(stage), phase, abort_flag, err, kSiteTcMma)) {
                         ok = false;
                         break;
@@ -196,11 +205,16 @@ __global__ void __launch_bounds__(192, 1)
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(sA + stage * Cfg::kABytes);
                     const uint32_t b0 = smem_u32(sB + stage * Cfg::kBBytes);
+                    const int nkb = min(Cfg::kKB, kblocks - ks * Cfg::kKB);
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        const uint32_t ak = a0 + kb * (Cfg::kBM * 128);
+                        const uint32_t bk = b0 + kb * (BN * 128);
 #pragma unroll
-                    for (int kk = 0; kk < Cfg::kBK / 16; ++kk)
-                        tc_mma_f16(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32),
-                                   sdesc_kmajor_sw128(b0 + kk * 32), idesc,
-                                   (kb | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < Cfg::kBK / 16; ++kk)
+                            tc_mma_f16(d_tmem, sdesc_kmajor_sw128(ak + kk * 32),
+                                       sdesc_kmajor_sw128(bk + kk * 32), idesc,
+                                       (ks | kb | kk) != 0 ? 1u : 0u);
+                    }
                     tc_commit(empty(stage));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -219,8 +233,15 @@ __global__ void __launch_bounds__(192, 1)
             mbar_drain(drain_bar, 0, err);
         }
     } else {
-        const int quad = warp & 3;  // tensor-memory lanes 32*quad .. 32*quad+31
+        // Epilogue: warp w (2..9) reads tensor-memory lanes 32*(w%4).. (rows
+        // of the tile) and one half of the tile's columns, 32 at a time; the
+        // next 32 columns are already being read while these are converted.
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        constexpr int kHalf = BN / 2;
+        constexpr int kChunks = kHalf / 32;
         const int r = quad * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int q = blockIdx.x; q < total; q += gridDim.x) {
@@ -228,40 +249,57 @@ __global__ void __launch_bounds__(192, 1)
             if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, err, kSiteTcEpilogue)) break;
             tc_fence_after();
             const bool valid = r < ti.rows;
-            const int64_t grow = static_cast<int64_t>(ti.row0) + r;
-            const float *bp = bias ? bias + static_cast<int64_t>(ti.e) * N + ti.cb * BN : nullptr;
-            __nv_bfloat16 *orow = out + grow * N + ti.cb * BN;
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                       static_cast<uint32_t>(acc * BN + c),
-                                   v);
+            const int col0 = ti.cb * BN + half * kHalf;
+            const float *bp = bias ? bias + static_cast<int64_t>(ti.e) * N + col0 : nullptr;
+            __nv_bfloat16 *orow = out + (static_cast<int64_t>(ti.row0) + r) * N + col0;
+            const uint32_t tbase = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + half * kHalf);
+            uint32_t v[2][32];
+            tmem_ld_32x32b_x32(tbase, v[0]);
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch) {
                 tmem_ld_wait();
+                if (ch + 1 < kChunks) tmem_ld_32x32b_x32(tbase + (ch + 1) * 32, v[(ch + 1) & 1]);
+                if (ch + 1 == kChunks) {
+                    tc_fence_before();
+                    mbar_arrive(tempty(acc));  // this half of the accumulator is read
+                }
                 if (valid) {
+                    float b[32];
+                    if (bp) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 t = __ldg(reinterpret_cast<const float4 *>(bp + ch * 32) + j);
+                            b[4 * j] = t.x;
+                            b[4 * j + 1] = t.y;
+                            b[4 * j + 2] = t.z;
+                            b[4 * j + 3] = t.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) b[j] = 0.0f;
+                    }
                     uint32_t pk[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        float f0 = __uint_as_float(v[2 * j]);
-                        float f1 = __uint_as_float(v[2 * j + 1]);
-                        if (bp) {
-                            f0 += bp[c + 2 * j];
-                            f1 += bp[c + 2 * j + 1];
-                        }
+                        float f0 = __uint_as_float(v[ch & 1][2 * j]) + b[2 * j];
+                        float f1 = __uint_as_float(v[ch & 1][2 * j + 1]) + b[2 * j + 1];
                         if (relu) {
                             f0 = fmaxf(f0, 0.0f);
                             f1 = fmaxf(f1, 0.0f);
                         }
                         pk[j] = pack_bf16x2(f0, f1);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+                    if (out_v8) {
+                        st_global_v8(orow + ch * 32, pk);
+                        st_global_v8(orow + ch * 32 + 16, pk + 8);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(tempty(acc));
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -294,15 +332,18 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor [rows, inner] (inner contiguous), box [box_rows, 64], 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+// bf16 matrix [rows, K] (K contiguous) seen as a 3-D tensor {64, rows, K/64}
+// (strides K*2 and 128 bytes), box {64, box_rows, 2}: one copy brings two
+// 64-wide k-blocks of box_rows rows, each landing as a 128-byte-swizzled
+// K-major tile; a k-block past K/64 reads as zeros.
+bool make_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+    cuuint64_t dims[3] = {64, rows, K / 64};
+    cuuint64_t strides[2] = {K * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -311,6 +352,7 @@ template <int BN, int STAGES>
 cudaError_t launch_bn(const CUtensorMap &mA, const CUtensorMap &mB, const int32_t *offsets,
                       const int32_t *tiles, int n, int K, int N, const float *bias, int relu,
                       __nv_bfloat16 *out, int32_t *err, int grid, cudaStream_t st) {
+    const int out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
     using Cfg = TcCfg<BN, STAGES>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -319,8 +361,8 @@ cudaError_t launch_bn(const CUtensorMap &mA, const CUtensorMap &mB, const int32_
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    ffn_gemm_tc<BN, STAGES><<<grid, 192, Cfg::kSmem, st>>>(mA, mB, offsets, tiles, n, K, N, bias,
-                                                           relu, out, err);
+    ffn_gemm_tc<BN, STAGES><<<grid, kFfnThreads, Cfg::kSmem, st>>>(mA, mB, offsets, tiles, n, K, N, bias,
+                                                           relu, out, out_v8, err);
     return cudaGetLastError();
 }
 
@@ -346,10 +388,10 @@ cudaError_t launch_grouped_gemm_tc(const moe_shape &s, const __nv_bfloat16 *A, i
     const int64_t max_tiles = ((S + kTcRows - 1) / kTcRows + s.n) * (N / BN);
     const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
     if (BN == 256)
-        return launch_bn<256, 4>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
+        return launch_bn<256, 2>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
     if (BN == 128)
-        return launch_bn<128, 6>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
-    return launch_bn<64, 8>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
+        return launch_bn<128, 3>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
+    return launch_bn<64, 4>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
 }
 
 }  // namespace moe
