@@ -8,11 +8,13 @@
 // tcgen05.mma: every product is exact and the sum carries fp32 rounding only,
 // like an fp32 dot product.
 //
-//   gate_pack       W_g, W_noise [d, C] fp32 -> Bhi, Blo [chunks*128, d] bf16,
-//                   K-major: chunk c holds 64 clean-score columns (rows 0..63)
-//                   and the same 64 noise-score columns (rows 64..127).
-//                   Hierarchical: the G group columns come first (padded to a
-//                   chunk boundary), then the n inner columns.
+//   gate_pack       W_g, W_noise [d, C] fp32 -> hi/lo bf16 units, one 32 KB
+//                   unit per (chunk, 64-wide k-block), stored pre-swizzled so
+//                   that one bulk copy fills a pipeline stage: chunk c holds 64
+//                   clean-score columns (rows 0..63) and the same 64
+//                   noise-score columns (rows 64..127).  Hierarchical: the G
+//                   group columns come first (padded to a chunk boundary),
+//                   then the n inner columns.
 //   gate_tc         persistent over 128-token tiles.  Warp 0 issues TMA loads,
 //                   warp 1 issues tcgen05.mma (M=128 tokens, N=128 = 64 clean +
 //                   64 noise columns, hi then lo pass into one fp32 accumulator,
@@ -60,12 +62,15 @@ __host__ __device__ __forceinline__ int gate_source_col(int lc, int C, int group
     return ic < C - groups ? groups + ic : -1;
 }
 
-// Block: 64 d-rows x 64 logical columns of one matrix (clean or noise).
+// Block: 64 d-rows (k-block kb) x 64 logical columns of one matrix (clean or
+// noise).  Output: for every (chunk, k-block) a 32 KB unit [hi | lo], each a
+// 128-row x 64-element bf16 tile already in the 128-byte-swizzled K-major
+// order a TMA copy would produce (16-byte group g of row r stored at group
+// g ^ (r % 8)), so that one bulk copy moves it into shared memory.
 __global__ void __launch_bounds__(256) gate_pack(const float *__restrict__ Wg,
                                                  const float *__restrict__ Wn, int d, int C,
                                                  int groups, int prim_pad, int noisy,
-                                                 __nv_bfloat16 *__restrict__ Bhi,
-                                                 __nv_bfloat16 *__restrict__ Blo) {
+                                                 uint8_t *__restrict__ pack) {
     __shared__ float tile[64][65];
     const int chunk = blockIdx.x;
     const int which = blockIdx.y;  // 0 clean, 1 noise
@@ -84,9 +89,11 @@ __global__ void __launch_bounds__(256) gate_pack(const float *__restrict__ Wg,
         const float v = tile[tx][cc];
         const __nv_bfloat16 hi = __float2bfloat16_rn(v);
         const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-        const int64_t row = static_cast<int64_t>(chunk) * 128 + which * 64 + cc;
-        Bhi[row * d + d0 + tx] = hi;
-        Blo[row * d + d0 + tx] = lo;
+        const int rr = which * 64 + cc;
+        const int64_t unit = (static_cast<int64_t>(chunk) * (d / 64) + blockIdx.z) * 2 * kKBytes;
+        const int off = rr * 128 + (((tx >> 3) ^ (rr & 7)) << 4) + (tx & 7) * 2;
+        *reinterpret_cast<__nv_bfloat16 *>(pack + unit + off) = hi;
+        *reinterpret_cast<__nv_bfloat16 *>(pack + unit + kKBytes + off) = lo;
     }
 }
 
@@ -161,8 +168,10 @@ constexpr int kGateThreads = 32 * (2 + kGateEpiWarps);
 
 template <bool kResident, bool kHier, int KM>
 struct GateCfg {
-    static constexpr int kStages = 4;
-    static constexpr int kStageBytes = kResident ? kKBytes : 3 * kKBytes;
+    // Stage: the hi and lo W tiles of one (chunk, k-block) unit (plus, when x
+    // is not resident, that k-block of x).
+    static constexpr int kStages = kResident ? 2 : 3;
+    static constexpr int kStageBytes = kResident ? 2 * kKBytes : 3 * kKBytes;
     static constexpr int kXBytes = kResident ? 8 * kKBytes : 0;  // d <= 512
     // Exchange between the two column halves: the group lists of both halves
     // (hierarchical only) and the final lists of half 1, [slot][token] order.
@@ -219,8 +228,8 @@ __device__ __forceinline__ void load_eps32(const float *__restrict__ row, int co
 // KM: list size for flat (>= k) or for each hierarchical level (>= k_groups, k_inner).
 template <bool kResident, bool kHier, int KM>
 __global__ void __launch_bounds__(kGateThreads, 1)
-    gate_tc(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapHi,
-            const __grid_constant__ CUtensorMap mapLo, const GateArgs a) {
+    gate_tc(const __grid_constant__ CUtensorMap mapX, const uint8_t *__restrict__ wpack,
+            const GateArgs a) {
     using Cfg = GateCfg<kResident, kHier, KM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -261,8 +270,6 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&mapX);
-        tma_prefetch_map(&mapHi);
-        tma_prefetch_map(&mapLo);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -290,36 +297,32 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                         break;
                     }
                     xphase ^= 1u;
+                    // the whole x tile (all k-blocks) in one 3-D copy
                     mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(kblocks * kKBytes));
-                    for (int kb = 0; kb < kblocks; ++kb)
-                        tma_load_2d(smem_u32(sX + kb * kKBytes), &mapX, xfull, kb * kGateBK, row0);
+                    tma_load_3d(smem_u32(sX), &mapX, xfull, 0, row0, 0);
                 }
                 for (int c = 0; c < a.chunks && ok; ++c) {
                     for (int kb = 0; kb < kblocks && ok; ++kb) {
-                        for (int split = 0; split < (kResident ? 2 : 1); ++split) {
-                            if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, a.err,
-                                                   kSiteTcProducer)) {
-                                ok = false;
-                                break;
-                            }
-                            uint8_t *st = sS + stage * Cfg::kStageBytes;
-                            if (kResident) {
-                                mbar_arrive_expect_tx(full(stage), kKBytes);
-                                tma_load_2d(smem_u32(st), split ? &mapLo : &mapHi, full(stage),
-                                            kb * kGateBK, c * 128);
-                            } else {
-                                mbar_arrive_expect_tx(full(stage), 3 * kKBytes);
-                                tma_load_2d(smem_u32(st), &mapX, full(stage), kb * kGateBK, row0);
-                                tma_load_2d(smem_u32(st + kKBytes), &mapHi, full(stage),
-                                            kb * kGateBK, c * 128);
-                                tma_load_2d(smem_u32(st + 2 * kKBytes), &mapLo, full(stage),
-                                            kb * kGateBK, c * 128);
-                            }
-                            ++issued;
-                            if (++stage == S) {
-                                stage = 0;
-                                phase ^= 1u;
-                            }
+                        if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, a.err,
+                                               kSiteTcProducer)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *st = sS + stage * Cfg::kStageBytes;
+                        const uint8_t *unit =
+                            wpack + (static_cast<int64_t>(c) * kblocks + kb) * (2 * kKBytes);
+                        if (kResident) {
+                            mbar_arrive_expect_tx(full(stage), 2 * kKBytes);
+                            bulk_load(smem_u32(st), unit, 2 * kKBytes, full(stage));
+                        } else {
+                            mbar_arrive_expect_tx(full(stage), 3 * kKBytes);
+                            tma_load_3d(smem_u32(st), &mapX, full(stage), 0, row0, kb);
+                            bulk_load(smem_u32(st + kKBytes), unit, 2 * kKBytes, full(stage));
+                        }
+                        ++issued;
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1u;
                         }
                     }
                 }
@@ -367,35 +370,27 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 128);
                     for (int kb = 0; kb < kblocks && ok; ++kb) {
-                        for (int split = 0; split < (kResident ? 2 : 1); ++split) {
-                            if (!mbar_wait_bounded(full(stage), phase, abort_flag, a.err,
-                                                   kSiteTcMma)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint32_t st = smem_u32(sS + stage * Cfg::kStageBytes);
-                            const uint32_t xa = kResident ? smem_u32(sX + kb * kKBytes) : st;
+                        if (!mbar_wait_bounded(full(stage), phase, abort_flag, a.err, kSiteTcMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t st = smem_u32(sS + stage * Cfg::kStageBytes);
+                        const uint32_t xa = kResident ? smem_u32(sX + kb * kKBytes) : st;
+                        const uint32_t wb = kResident ? st : st + kKBytes;
 #pragma unroll
-                            for (int kk = 0; kk < kGateBK / 16; ++kk) {
-                                const uint64_t ad = sdesc_kmajor_sw128(xa + kk * 32);
-                                if (kResident) {
-                                    tc_mma_f16(d_tmem, ad, sdesc_kmajor_sw128(st + kk * 32), idesc,
-                                               (kb | split | kk) != 0 ? 1u : 0u);
-                                } else {
-                                    tc_mma_f16(d_tmem, ad,
-                                               sdesc_kmajor_sw128(st + kKBytes + kk * 32), idesc,
-                                               (kb | kk) != 0 ? 1u : 0u);
-                                    tc_mma_f16(d_tmem, ad,
-                                               sdesc_kmajor_sw128(st + 2 * kKBytes + kk * 32),
-                                               idesc, 1u);
-                                }
-                            }
-                            tc_commit(empty(stage));
-                            if (++stage == S) {
-                                stage = 0;
-                                phase ^= 1u;
-                            }
+                        for (int kk = 0; kk < kGateBK / 16; ++kk)  // x . W_hi
+                            tc_mma_f16(d_tmem, sdesc_kmajor_sw128(xa + kk * 32),
+                                       sdesc_kmajor_sw128(wb + kk * 32), idesc,
+                                       (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+                        for (int kk = 0; kk < kGateBK / 16; ++kk)  // + x . W_lo
+                            tc_mma_f16(d_tmem, sdesc_kmajor_sw128(xa + kk * 32),
+                                       sdesc_kmajor_sw128(wb + kKBytes + kk * 32), idesc, 1u);
+                        tc_commit(empty(stage));
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1u;
                         }
                     }
                     if (!ok) break;
@@ -473,6 +468,8 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                                              : c * kGateChunk + half * 32;
                 const int ncols = inner_chunk ? a.n : (kHier ? a.groups : a.C);
                 const int ecol0 = inner_chunk ? a.groups + col0 : col0;  // eps / bg column
+                if (eps_row && !kHier && c + 2 < a.chunks && (c + 2) * kGateChunk + half * 32 < a.C)
+                    prefetch_l2(eps_row + (c + 2) * kGateChunk + half * 32);
                 float ev[32];
                 if (eps_row && col0 < ncols) {
                     uint32_t live = 0xffffffffu;
@@ -496,6 +493,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                 if (ok && !mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, a.err,
                                              kSiteTcEpilogue))
                     ok = false;
+                ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the votes below need every lane
                 if (ok) {
                     tc_fence_after();
                     // Pass 1 thresholds: the k-th entry of each list, fixed for the span.
@@ -514,8 +512,8 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                             tc_fence_before();
                             mbar_arrive(tempty(acc));  // this half of the accumulator is read
                         }
-                        if (!valid) continue;
-                        // Pass 1: which columns' upper bound beats their list's k-th entry.
+                        // Pass 1: which columns' upper bound beats their list's k-th entry
+                        // (tokens past T flag nothing but still take part in the votes).
                         uint32_t pass = 0;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -539,16 +537,19 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                                         static_cast<unsigned>(sc - glo[qq]) < static_cast<unsigned>(a.m))
                                         thr = thr_i[qq];
                             }
-                            if (sc < ncols && ub > thr) pass |= 1u << j;
+                            if (valid && sc < ncols && ub > thr) pass |= 1u << j;
                         }
-                        // Pass 2 (rare): the exact noisy score and the insertion.
-                        if (pass) {
+                        // Pass 2 (rare): the exact noisy score and the insertion.  The
+                        // warp vote keeps a column's body a real branch, taken only
+                        // when some lane flagged that column.
+                        if (__any_sync(0xffffffffu, pass != 0)) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
+                                if (!__any_sync(0xffffffffu, (pass >> j) & 1u)) continue;
                                 if (!((pass >> j) & 1u)) continue;
                                 const int sc = col0 + piece * 16 + j;
                                 float h = __uint_as_float(cv[j]);
-                                if (noisy) h += ev[piece * 16 + j] * softplus_f(__uint_as_float(nv[j]));
+                                if (noisy) h += ev[piece * 16 + j] * softplus_fast(__uint_as_float(nv[j]));
                                 if (!inner_chunk) {
                                     prim.insert(h, sc);
                                 } else {
@@ -649,21 +650,23 @@ EncodeTiledFn gate_encode_fn() {
     return fn;
 }
 
-bool gate_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows) {
+// x [T, d] bf16 seen as {64, T, d/64} (strides d*2 and 128 bytes); a box of
+// 128 tokens x kb_box k-blocks lands as kb_box 128-byte-swizzled K-major tiles.
+bool gate_map(CUtensorMap *m, const void *base, uint64_t d, uint64_t rows, uint32_t kb_box) {
     EncodeTiledFn enc = gate_encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {64, 128};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+    cuuint64_t dims[3] = {64, rows, d / 64};
+    cuuint64_t strides[2] = {d * 2, 128};
+    cuuint32_t box[3] = {64, 128, kb_box};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool kResident, bool kHier, int KM>
-cudaError_t launch_gate_tc_t(const CUtensorMap &mx, const CUtensorMap &mh, const CUtensorMap &ml,
-                             const GateArgs &ga, int grid, cudaStream_t st) {
+cudaError_t launch_gate_tc_t(const CUtensorMap &mx, const uint8_t *wpack, const GateArgs &ga,
+                             int grid, cudaStream_t st) {
     using Cfg = GateCfg<kResident, kHier, KM>;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
@@ -672,21 +675,20 @@ cudaError_t launch_gate_tc_t(const CUtensorMap &mx, const CUtensorMap &mh, const
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     });
     if (attr != cudaSuccess) return attr;
-    gate_tc<kResident, kHier, KM><<<grid, kGateThreads, Cfg::kSmem, st>>>(mx, mh, ml, ga);
+    gate_tc<kResident, kHier, KM><<<grid, kGateThreads, Cfg::kSmem, st>>>(mx, wpack, ga);
     return cudaGetLastError();
 }
 
 template <bool kResident, bool kHier>
-cudaError_t launch_gate_tc_km(int km, const CUtensorMap &mx, const CUtensorMap &mh,
-                              const CUtensorMap &ml, const GateArgs &ga, int grid,
-                              cudaStream_t st) {
-    if (km <= 2) return launch_gate_tc_t<kResident, kHier, 2>(mx, mh, ml, ga, grid, st);
-    if (km <= 4) return launch_gate_tc_t<kResident, kHier, 4>(mx, mh, ml, ga, grid, st);
+cudaError_t launch_gate_tc_km(int km, const CUtensorMap &mx, const uint8_t *wpack,
+                              const GateArgs &ga, int grid, cudaStream_t st) {
+    if (km <= 2) return launch_gate_tc_t<kResident, kHier, 2>(mx, wpack, ga, grid, st);
+    if (km <= 4) return launch_gate_tc_t<kResident, kHier, 4>(mx, wpack, ga, grid, st);
     if constexpr (kHier) {
         return cudaErrorInvalidValue;  // hierarchical lists are limited to 4
     } else {
-        if (km <= 8) return launch_gate_tc_t<kResident, kHier, 8>(mx, mh, ml, ga, grid, st);
-        return launch_gate_tc_t<kResident, kHier, 16>(mx, mh, ml, ga, grid, st);
+        if (km <= 8) return launch_gate_tc_t<kResident, kHier, 8>(mx, wpack, ga, grid, st);
+        return launch_gate_tc_t<kResident, kHier, 16>(mx, wpack, ga, grid, st);
     }
 }
 
@@ -739,24 +741,21 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
         ga.prim_pad = ga.prim_chunks * kGateChunk;
         ga.chunks = ga.prim_chunks + (s.n + kGateChunk - 1) / kGateChunk;
     }
-    __nv_bfloat16 *Bhi = static_cast<__nv_bfloat16 *>(pack);
-    __nv_bfloat16 *Blo = Bhi + static_cast<size_t>(ga.chunks) * 128 * s.d;
+    uint8_t *wpack = static_cast<uint8_t *>(pack);
     gate_pack<<<dim3(ga.chunks, 2, s.d / 64), 256, 0, st>>>(Wg, noisy ? Wn : Wg, s.d, C, s.groups,
-                                                          ga.prim_pad, noisy, Bhi, Blo);
-    CUtensorMap mx, mh, ml;
-    if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T)) ||
-        !gate_map(&mh, Bhi, s.d, static_cast<uint64_t>(ga.chunks) * 128) ||
-        !gate_map(&ml, Blo, s.d, static_cast<uint64_t>(ga.chunks) * 128))
+                                                          ga.prim_pad, noisy, wpack);
+    const bool resident = s.d <= 512;
+    CUtensorMap mx;
+    if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? s.d / 64 : 1))
         return cudaErrorInvalidValue;
     const int tiles = static_cast<int>((s.T + kGateRows - 1) / kGateRows);
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    const bool resident = s.d <= 512;
     const int km = s.groups ? (s.k_groups > s.k / s.k_groups ? s.k_groups : s.k / s.k_groups) : s.k;
     if (resident)
-        return s.groups ? launch_gate_tc_km<true, true>(km, mx, mh, ml, ga, grid, st)
-                        : launch_gate_tc_km<true, false>(km, mx, mh, ml, ga, grid, st);
-    return s.groups ? launch_gate_tc_km<false, true>(km, mx, mh, ml, ga, grid, st)
-                    : launch_gate_tc_km<false, false>(km, mx, mh, ml, ga, grid, st);
+        return s.groups ? launch_gate_tc_km<true, true>(km, mx, wpack, ga, grid, st)
+                        : launch_gate_tc_km<true, false>(km, mx, wpack, ga, grid, st);
+    return s.groups ? launch_gate_tc_km<false, true>(km, mx, wpack, ga, grid, st)
+                    : launch_gate_tc_km<false, false>(km, mx, wpack, ga, grid, st);
 }
 
 }  // namespace moe

@@ -141,6 +141,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Contiguous global -> shared copy of `bytes` (multiple of 16; both addresses
+// 16-byte aligned), completion counted on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // 32-byte global store of 8 words; p must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *w) {
     asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
@@ -248,6 +259,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float softplus_f(float z) {
     return fmaxf(z, 0.0f) + log1pf(expf(-fabsf(z)));
+}
+
+// softplus with the hardware exp/log approximations: max(z, 0) + log(1 + e^-|z|).
+// Absolute error below 1e-6 (the log of a value in [1, 2] and an exp of a
+// value <= 0), against a score that needs about 1e-5.
+__device__ __forceinline__ float softplus_fast(float z) {
+    return fmaxf(z, 0.0f) + __logf(1.0f + __expf(-fabsf(z)));
+}
+
+// Hint that a global line will be read soon (into L2).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
