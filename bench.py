@@ -41,7 +41,7 @@ UNIT = "tokens/s"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="flat_n256_k4", choices=sorted(wl.WORKLOADS))
@@ -225,7 +225,10 @@ def config_of(w: wl.Workload) -> dict:
 # GPU arm
 # ---------------------------------------------------------------------------
 def launches_per_step(w: wl.Workload) -> int:
-    gate, dispatch, combine = 2, 6, 1
+    """Kernels moe_forward launches per step: gate (pack + scores/top-k),
+    dispatch (rank, column scan, finish, scatter), expert FFN (tile table,
+    gather + two grouped GEMMs in bf16; two SIMT GEMMs in fp32), combine."""
+    gate, dispatch, combine = 2, 4, 1
     ffn = 4 if w.dtype == "bf16" else 3
     return gate + dispatch + ffn + combine
 

@@ -161,7 +161,7 @@ MOE_API moe_status moe_dispatch(const moe_shape *shape, const int32_t *idx, cons
  * kernels, but keeps their scratch in one array of static device storage
  * inside this library (8 MiB, resident on every device that loads the
  * library until the process exits).  It calls no allocation routine.
- *   - Limit: the scratch needed is 256 B + 4*S + 4*ceil(S/1024)*n + 8*n
+ *   - Limit: the scratch needed is 256 B + 4*S + 12*ceil(S/1024)*n + 8*n
  *     bytes (each term rounded up to 256 B); a shape that needs more than
  *     8 MiB returns MOE_ERR_UNSUPPORTED and enqueues nothing.
  *   - The first call on a device looks up the array's device address

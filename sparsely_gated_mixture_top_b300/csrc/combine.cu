@@ -1,8 +1,8 @@
 // combine.cu -- y[t] = sum_j G[t,j] * Y_slot[inv_perm[t*k+j]]
 // ("MoE:稀疏门控混合专家", section 二: y = sum_i G(x)_i E_i(x), only the selected
 // experts contributing).  One warp per token, 16-byte vector loads of the
-// expert rows, fp32 accumulation in the fixed slot order j = 0..k-1 and one
-// rounding to the output type.
+// expert rows (four in flight), fp32 accumulation in the fixed slot order
+// j = 0..k-1 and one rounding to the output type.
 #include "moe_device.cuh"
 #include "moe_launch.h"
 
@@ -49,8 +49,11 @@ struct Vec<float> {
     }
 };
 
-template <typename T>
-__global__ void __launch_bounds__(256) combine_kernel(const T *__restrict__ Y,
+// One warp per token.  The token's k rows and weights are read once; for each
+// 32*V-wide column span, four expert rows are loaded before any is summed,
+// then the sum runs in the fixed slot order j = 0..k-1.
+template <typename T, int KM>
+__global__ void __launch_bounds__(256, KM <= 4 ? 3 : 2) combine_kernel(const T *__restrict__ Y,
                                                       const int32_t *__restrict__ inv_perm,
                                                       const float *__restrict__ G, int64_t T_,
                                                       int d, int k, int64_t S,
@@ -59,22 +62,44 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *__restrict__ Y,
     const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
     if (t >= T_) return;
     const int lane = threadIdx.x & 31;
+    int32_t rows[KM];
+    float w[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        rows[j] = -1;
+        w[j] = 0.0f;
+        if (j < k) {
+            int32_t row = inv_perm[t * k + j];
+            if (row >= S) {
+                if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteCombineRow, static_cast<int32_t>(t));
+                row = -1;
+            }
+            rows[j] = row;
+            w[j] = G[t * k + j];
+        }
+    }
     for (int c = lane * V; c < d; c += 32 * V) {
         float acc[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) acc[i] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const int32_t row = inv_perm[t * k + j];
-            if (row < 0) continue;
-            if (row >= S) {
-                report(err, MOE_ERR_DEVICE, kSiteCombineRow, static_cast<int32_t>(t));
-                continue;
-            }
-            const float w = G[t * k + j];
-            float v[V];
-            Vec<T>::load(Y + static_cast<int64_t>(row) * d + c, v);
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc[i] = fmaf(w, v[i], acc[i]);
+        for (int j0 = 0; j0 < KM; j0 += 4) {
+            if (j0 >= k) break;
+            float v[4][V];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = j0 + jj;
+                if (j < k && rows[j] >= 0)
+                    Vec<T>::load(Y + static_cast<int64_t>(rows[j]) * d + c, v[jj]);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = j0 + jj;
+                if (j < k && rows[j] >= 0) {
+#pragma unroll
+                    for (int i = 0; i < V; ++i) acc[i] = fmaf(w[j], v[jj][i], acc[i]);
+                }
+            }
         }
         Vec<T>::store(y + t * d + c, acc);
     }
@@ -86,14 +111,22 @@ cudaError_t launch_combine(const moe_shape &s, const void *Y_slot, const int32_t
                            const float *G, void *y, int32_t *err, cudaStream_t st) {
     if (s.T == 0) return cudaSuccess;
     const unsigned blocks = static_cast<unsigned>((s.T + 7) / 8);
-    if (s.dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
-            static_cast<const __nv_bfloat16 *>(Y_slot), inv_perm, G, s.T, s.d, s.k, slots(s),
-            static_cast<__nv_bfloat16 *>(y), err);
-    else
-        combine_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float *>(Y_slot), inv_perm,
-                                                      G, s.T, s.d, s.k, slots(s),
-                                                      static_cast<float *>(y), err);
+    const int64_t S = slots(s);
+    if (s.dtype == MOE_BF16) {
+        const auto *Yb = static_cast<const __nv_bfloat16 *>(Y_slot);
+        auto *yb = static_cast<__nv_bfloat16 *>(y);
+        if (s.k <= 4)
+            combine_kernel<__nv_bfloat16, 4><<<blocks, 256, 0, st>>>(Yb, inv_perm, G, s.T, s.d, s.k, S, yb, err);
+        else
+            combine_kernel<__nv_bfloat16, MOE_MAX_K><<<blocks, 256, 0, st>>>(Yb, inv_perm, G, s.T, s.d, s.k, S, yb, err);
+    } else {
+        const auto *Yf = static_cast<const float *>(Y_slot);
+        auto *yf = static_cast<float *>(y);
+        if (s.k <= 4)
+            combine_kernel<float, 4><<<blocks, 256, 0, st>>>(Yf, inv_perm, G, s.T, s.d, s.k, S, yf, err);
+        else
+            combine_kernel<float, MOE_MAX_K><<<blocks, 256, 0, st>>>(Yf, inv_perm, G, s.T, s.d, s.k, S, yf, err);
+    }
     return cudaGetLastError();
 }
 

@@ -36,6 +36,8 @@ WsLayout noalloc_layout(const moe_shape &s) {
     o = align_up(o + S * 4, 256);
     L.chunk = o;
     o = align_up(o + chunks * n * 4, 256);
+    L.chunk_imp = o;
+    o = align_up(o + chunks * n * 8, 256);
     L.imp64 = o;
     o = align_up(o + n * 8, 256);
     L.total = o;

@@ -21,14 +21,14 @@
 //                   double-buffered in tensor memory), warps 2..9 are the
 //                   epilogue: two warps per tensor-memory lane quarter, each
 //                   owning one half of every chunk's columns for its 32 tokens
-//                   (thread r = token r = tensor-memory lane r).  A first pass
-//                   over 16 columns at a time bounds each noisy score from
-//                   above without evaluating softplus and flags only the
-//                   columns that can still enter the running top-k; a second
-//                   pass computes H = clean (+ b_g) + eps * softplus(noise) for
-//                   the flagged ones and inserts them (KeepTopK, ties to the
-//                   lower index).  The halves merge their lists through shared
-//                   memory and the softmax runs over the k survivors.
+//                   (thread r = token r = tensor-memory lane r).  A first,
+//                   branch-free pass over 16 columns at a time computes
+//                   H = clean (+ b_g) + eps * softplus(noise) (softplus from
+//                   the hardware exp/log) and flags the columns that beat the
+//                   k-th entry of the running top-k; a second pass inserts the
+//                   flagged ones (KeepTopK, ties to the lower index).  The
+//                   halves merge their lists through shared memory and the
+//                   softmax runs over the k survivors.
 //                   Hierarchical gating picks the groups from the first chunks
 //                   (both halves merge them) and only then looks at (and reads
 //                   eps for) the inner columns of its chosen groups.
@@ -512,22 +512,19 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                             tc_fence_before();
                             mbar_arrive(tempty(acc));  // this half of the accumulator is read
                         }
-                        // Pass 1: which columns' upper bound beats their list's k-th entry
-                        // (tokens past T flag nothing but still take part in the votes).
+                        // Pass 1 (branch-free): the noisy score of every column and
+                        // which ones beat the k-th entry of their list.  Within a
+                        // thread's list the columns arrive in increasing index order,
+                        // so an equal score never displaces an entry: '>' is exact.
+                        // Tokens past T flag nothing but still take part in the votes.
                         uint32_t pass = 0;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int sc = col0 + piece * 16 + j;
-                            float clean = __uint_as_float(cv[j]);
-                            if (a.bg && sc < ncols) clean += __ldg(a.bg + ecol0 + piece * 16 + j);
-                            cv[j] = __float_as_uint(clean);
-                            const float e = ev[piece * 16 + j];
-                            // softplus(z) is in [0, max(z, 0) + ln 2]: with eps <= 0 the
-                            // noise term can only lower the score, else it adds at most
-                            // eps * (max(z, 0) + 0.75) (an upper bound after fp32 rounding too).
-                            const float ub =
-                                noisy ? fmaf(fmaxf(e, 0.0f), fmaxf(__uint_as_float(nv[j]), 0.0f) + 0.75f, clean)
-                                      : clean;
+                            float h = __uint_as_float(cv[j]);
+                            if (a.bg && sc < ncols) h += __ldg(a.bg + ecol0 + piece * 16 + j);
+                            if (noisy) h += ev[piece * 16 + j] * softplus_fast(__uint_as_float(nv[j]));
+                            cv[j] = __float_as_uint(h);
                             float thr = thr_p;
                             if (inner_chunk) {
                                 thr = INFINITY;  // outside the chosen groups
@@ -537,19 +534,17 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                                         static_cast<unsigned>(sc - glo[qq]) < static_cast<unsigned>(a.m))
                                         thr = thr_i[qq];
                             }
-                            if (valid && sc < ncols && ub > thr) pass |= 1u << j;
+                            if (valid && sc < ncols && h > thr) pass |= 1u << j;
                         }
-                        // Pass 2 (rare): the exact noisy score and the insertion.  The
-                        // warp vote keeps a column's body a real branch, taken only
-                        // when some lane flagged that column.
+                        // Pass 2 (rare): insert the flagged columns.  The warp vote
+                        // keeps each column's insertion a real branch.
                         if (__any_sync(0xffffffffu, pass != 0)) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 if (!__any_sync(0xffffffffu, (pass >> j) & 1u)) continue;
                                 if (!((pass >> j) & 1u)) continue;
                                 const int sc = col0 + piece * 16 + j;
-                                float h = __uint_as_float(cv[j]);
-                                if (noisy) h += ev[piece * 16 + j] * softplus_fast(__uint_as_float(nv[j]));
+                                const float h = __uint_as_float(cv[j]);
                                 if (!inner_chunk) {
                                     prim.insert(h, sc);
                                 } else {

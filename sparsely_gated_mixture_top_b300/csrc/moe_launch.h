@@ -32,6 +32,7 @@ struct WsLayout {
     size_t gpack = 0;       // packed bf16 hi/lo gate matrices (tensor-core gate only)
     size_t local_rank = 0;  // [S] int32, rank of a slot among same-expert slots of its chunk
     size_t chunk = 0;       // [chunks, n] int32, per-chunk expert counts, then bases
+    size_t chunk_imp = 0;   // [chunks, n] double, per-chunk gate-weight sums
     size_t imp64 = 0;       // [n] double, importance accumulated in fp64
     size_t counts = 0;      // [n] int32 (used when the caller does not pass counts)
     size_t offsets = 0;     // [n + 1] int32
@@ -64,6 +65,7 @@ inline WsLayout ws_layout(const moe_shape &s) {
     L.gpack = take(tc_gate ? gate_tc_pack_bytes(s) : 0);
     L.local_rank = take(S * 4);
     L.chunk = take(chunks * n * 4);
+    L.chunk_imp = take(chunks * n * 8);
     L.imp64 = take(n * 8);
     L.counts = take(n * 4);
     L.offsets = take((n + 1) * 4);

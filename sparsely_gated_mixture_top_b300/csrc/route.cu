@@ -7,78 +7,121 @@
 //
 //   route_rank      per chunk of 1024 slots: the rank of each slot among the
 //                   earlier slots of its chunk with the same expert (warp
-//                   __match_any + warps taken in order), and the chunk's
-//                   per-expert counts
-//   route_colscan   per expert, an exclusive scan down the chunks (chunk bases)
-//                   and the expert's total count
-//   route_offsets   exclusive scan of the counts over the experts
+//                   __match_any + warps taken in order), the chunk's
+//                   per-expert counts and gate-weight sums (each warp's group
+//                   of <= 32 slots in fp32, the groups in fp64, slot order)
+//   route_colscan   per expert, an exclusive scan of the counts down the
+//                   chunks (chunk bases), the expert's count and its
+//                   importance (chunk partials summed in chunk order)
+//   route_finish    one block: exclusive scan of the counts over the experts
+//                   (offsets), importance in fp32, population variance /
+//                   mean^2 of the importance vector (CV^2)
 //   route_scatter   row = offsets[e] + chunk base + local rank: perm, inv_perm
-//   route_importance  per expert, sum of G over its rows in row order (fp64)
-//   route_cv2       population variance / mean^2 of the importance vector
 //
-// Integer work only until the importance; the permutation is stable, so the
-// same idx always gives the same perm bit for bit.
+// The permutation is stable and every sum has a fixed order, so the same idx
+// and G always give the same outputs bit for bit.
 #include "moe_device.cuh"
 #include "moe_launch.h"
+
+#include <mutex>
 
 namespace moe {
 
 namespace {
 
-__global__ void __launch_bounds__(1024) route_rank(const int32_t *__restrict__ idx, int64_t S,
-                                                   int n, int32_t *__restrict__ local_rank,
-                                                   int32_t *__restrict__ chunk, int32_t *err) {
-    extern __shared__ int32_t cnt[];  // [n]
+__global__ void __launch_bounds__(1024) route_rank(const int32_t *__restrict__ idx,
+                                                   const float *__restrict__ G, int64_t S, int n,
+                                                   int32_t *__restrict__ local_rank,
+                                                   int32_t *__restrict__ chunk,
+                                                   double *__restrict__ chunk_imp, int32_t *err) {
+    extern __shared__ __align__(8) unsigned char route_sh[];
+    double *imp = reinterpret_cast<double *>(route_sh);              // [n]
+    int32_t *cnt = reinterpret_cast<int32_t *>(route_sh + 8 * n);     // [n]
     __shared__ int32_t base_sh[32][32];
-    for (int e = threadIdx.x; e < n; e += blockDim.x) cnt[e] = 0;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+        cnt[e] = 0;
+        imp[e] = 0.0;
+    }
     __syncthreads();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t s = static_cast<int64_t>(blockIdx.x) * kRouteChunk + threadIdx.x;
     int e = -1;
+    float g = 0.0f;
     if (s < S) {
         e = idx[s];
         if (e < 0 || e >= n) {
             report(err, MOE_ERR_DEVICE, kSiteRouteIdx, static_cast<int32_t>(s));
             e = -1;
+        } else {
+            g = G[s];
         }
     }
     const unsigned mask = __match_any_sync(0xffffffffu, e);
     const int leader = __ffs(mask) - 1;
     const int rank_in_warp = __popc(mask & ((1u << lane) - 1u));
-    // Warps take their turn in slot order, so ranks follow slot order.
+    // Gate weight of this lane's expert group (at most 32 slots) summed in
+    // lane order in fp32; the groups are then accumulated in fp64.
+    float seg = 0.0f;
+#pragma unroll
+    for (int src = 0; src < 32; ++src) {
+        const float v = __shfl_sync(0xffffffffu, g, src);
+        if ((mask >> src) & 1u) seg += v;
+    }
+    // Warps take their turn in slot order, so ranks and importance sums
+    // follow slot order.
     for (int w = 0; w < 32; ++w) {
         if (warp == w && lane == leader && e >= 0) {
             base_sh[w][lane] = cnt[e];
             cnt[e] += __popc(mask);
+            imp[e] += static_cast<double>(seg);
         }
         __syncthreads();
     }
     if (e >= 0) local_rank[s] = base_sh[warp][leader] + rank_in_warp;
     int32_t *row = chunk + static_cast<int64_t>(blockIdx.x) * n;
-    for (int ee = threadIdx.x; ee < n; ee += blockDim.x) row[ee] = cnt[ee];
+    double *irow = chunk_imp + static_cast<int64_t>(blockIdx.x) * n;
+    for (int ee = threadIdx.x; ee < n; ee += blockDim.x) {
+        row[ee] = cnt[ee];
+        irow[ee] = imp[ee];
+    }
 }
 
-// Block (32 x 32): 32 experts (x) by 32 chunk segments (y).
-__global__ void __launch_bounds__(1024) route_colscan(int32_t *__restrict__ chunk, int chunks,
-                                                      int n, int32_t *__restrict__ counts) {
+// Block (32 x 32): 32 experts (x) by 32 chunk segments (y).  Chunk counts
+// become chunk bases (exclusive scan down the chunks); the expert's count
+// and importance (fp64, chunk order) are the column totals.
+__global__ void __launch_bounds__(1024) route_colscan(int32_t *__restrict__ chunk,
+                                                      const double *__restrict__ chunk_imp,
+                                                      int chunks, int n, int32_t *__restrict__ counts,
+                                                      double *__restrict__ imp64) {
     __shared__ int32_t part[32][33];
+    __shared__ double ipart[32][33];
     const int tx = threadIdx.x, ty = threadIdx.y;
     const int e = blockIdx.x * 32 + tx;
     const int seg = (chunks + 31) / 32;
     const int b0 = ty * seg, b1 = min(chunks, b0 + seg);
     int32_t sum = 0;
+    double isum = 0.0;
     if (e < n)
-        for (int b = b0; b < b1; ++b) sum += chunk[static_cast<int64_t>(b) * n + e];
+        for (int b = b0; b < b1; ++b) {
+            sum += chunk[static_cast<int64_t>(b) * n + e];
+            isum += chunk_imp[static_cast<int64_t>(b) * n + e];
+        }
     part[ty][tx] = sum;
+    ipart[ty][tx] = isum;
     __syncthreads();
     if (ty == 0) {
         int32_t run = 0;
+        double irun = 0.0;
         for (int y = 0; y < 32; ++y) {
             const int32_t v = part[y][tx];
             part[y][tx] = run;
             run += v;
+            irun += ipart[y][tx];
         }
-        if (e < n) counts[e] = run;
+        if (e < n) {
+            counts[e] = run;
+            imp64[e] = irun;
+        }
     }
     __syncthreads();
     if (e < n) {
@@ -92,10 +135,27 @@ __global__ void __launch_bounds__(1024) route_colscan(int32_t *__restrict__ chun
     }
 }
 
-// One block of 1024 threads: offsets = exclusive scan of counts, offsets[n] = total.
-__global__ void __launch_bounds__(1024) route_offsets(const int32_t *__restrict__ counts, int n,
-                                                      int32_t *__restrict__ offsets) {
+__device__ double block_sum_1024(double v, double *sh) {
+    sh[threadIdx.x] = v;
+    __syncthreads();
+    for (int o = 512; o > 0; o >>= 1) {
+        if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+        __syncthreads();
+    }
+    const double r = sh[0];
+    __syncthreads();
+    return r;
+}
+
+// One block of 1024 threads: offsets = exclusive scan of counts (offsets[n] =
+// total), importance in fp32, and CV^2 = population variance / mean^2.
+__global__ void __launch_bounds__(1024) route_finish(const int32_t *__restrict__ counts,
+                                                     const double *__restrict__ imp64, int n,
+                                                     int32_t *__restrict__ offsets,
+                                                     float *__restrict__ importance,
+                                                     float *__restrict__ cv2) {
     __shared__ int32_t part[1024];
+    __shared__ double sh[1024];
     const int per = (n + 1023) / 1024;
     const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
     int32_t sum = 0;
@@ -114,6 +174,16 @@ __global__ void __launch_bounds__(1024) route_offsets(const int32_t *__restrict_
         run += counts[i];
     }
     if (threadIdx.x == 1023) offsets[n] = part[1023];
+    double s = 0.0;
+    for (int e = threadIdx.x; e < n; e += 1024) {
+        s += imp64[e];
+        importance[e] = static_cast<float>(imp64[e]);
+    }
+    const double mean = block_sum_1024(s, sh) / n;
+    double q = 0.0;
+    for (int e = threadIdx.x; e < n; e += 1024) q += (imp64[e] - mean) * (imp64[e] - mean);
+    const double var = block_sum_1024(q, sh) / n;
+    if (threadIdx.x == 0) cv2[0] = mean != 0.0 ? static_cast<float>(var / (mean * mean)) : 0.0f;
 }
 
 __global__ void route_scatter(const int32_t *__restrict__ idx, int64_t S, int n,
@@ -132,47 +202,6 @@ __global__ void route_scatter(const int32_t *__restrict__ idx, int64_t S, int n,
         inv_perm[s] = row;
     }
     if (s >= offsets[n]) perm[s] = -1;  // rows left empty by invalid slots
-}
-
-// One warp per expert; fp64 lane sums in row order, then a fixed shuffle tree.
-__global__ void route_importance(const float *__restrict__ G, const int32_t *__restrict__ perm,
-                                 const int32_t *__restrict__ offsets, int n,
-                                 float *__restrict__ importance, double *__restrict__ imp64) {
-    const int e = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    if (e >= n) return;
-    const int lane = threadIdx.x & 31;
-    double acc = 0.0;
-    for (int r = offsets[e] + lane; r < offsets[e + 1]; r += 32) acc += static_cast<double>(G[perm[r]]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-        importance[e] = static_cast<float>(acc);
-        imp64[e] = acc;
-    }
-}
-
-__device__ double block_sum_1024(double v, double *sh) {
-    sh[threadIdx.x] = v;
-    __syncthreads();
-    for (int o = 512; o > 0; o >>= 1) {
-        if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
-        __syncthreads();
-    }
-    const double r = sh[0];
-    __syncthreads();
-    return r;
-}
-
-__global__ void __launch_bounds__(1024) route_cv2(const double *__restrict__ imp64, int n,
-                                                  float *__restrict__ cv2) {
-    __shared__ double sh[1024];
-    double s = 0.0;
-    for (int e = threadIdx.x; e < n; e += 1024) s += imp64[e];
-    const double mean = block_sum_1024(s, sh) / n;
-    double q = 0.0;
-    for (int e = threadIdx.x; e < n; e += 1024) q += (imp64[e] - mean) * (imp64[e] - mean);
-    const double var = block_sum_1024(q, sh) / n;
-    if (threadIdx.x == 0) cv2[0] = mean != 0.0 ? static_cast<float>(var / (mean * mean)) : 0.0f;
 }
 
 }  // namespace
@@ -194,20 +223,27 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
     const int chunks = static_cast<int>((S + kRouteChunk - 1) / kRouteChunk);
     int32_t *local_rank = ws_ptr<int32_t>(ws, L.local_rank);
     int32_t *chunk = ws_ptr<int32_t>(ws, L.chunk);
+    double *chunk_imp = ws_ptr<double>(ws, L.chunk_imp);
     double *imp64 = ws_ptr<double>(ws, L.imp64);
-    const size_t smem = sizeof(int32_t) * n;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(route_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
+    // Dynamic shared memory: n doubles and n ints (plus 4 KB static); the
+    // opt-in above the default 48 KB is raised once to the largest size seen.
+    const size_t smem = 12 * static_cast<size_t>(n);
+    static size_t opted_in = 0;
+    static std::mutex opt_mu;
+    if (smem + 4096 > 48 * 1024) {
+        std::lock_guard<std::mutex> lock(opt_mu);
+        if (smem > opted_in) {
+            cudaError_t e = cudaFuncSetAttribute(
+                route_rank, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+            opted_in = smem;
+        }
     }
-    route_rank<<<chunks, 1024, smem, st>>>(idx, S, n, local_rank, chunk, err);
-    route_colscan<<<(n + 31) / 32, dim3(32, 32), 0, st>>>(chunk, chunks, n, counts);
-    route_offsets<<<1, 1024, 0, st>>>(counts, n, offsets);
+    route_rank<<<chunks, 1024, smem, st>>>(idx, G, S, n, local_rank, chunk, chunk_imp, err);
+    route_colscan<<<(n + 31) / 32, dim3(32, 32), 0, st>>>(chunk, chunk_imp, chunks, n, counts, imp64);
+    route_finish<<<1, 1024, 0, st>>>(counts, imp64, n, offsets, importance, cv2);
     route_scatter<<<static_cast<unsigned>((S + 255) / 256), 256, 0, st>>>(
         idx, S, n, offsets, chunk, local_rank, perm, inv_perm);
-    route_importance<<<(n + 7) / 8, 256, 0, st>>>(G, perm, offsets, n, importance, imp64);
-    route_cv2<<<1, 1024, 0, st>>>(imp64, n, cv2);
     return cudaGetLastError();
 }
 
