@@ -13,10 +13,10 @@
 // networks ("MoE:稀疏门控混合专家", section 二).
 //
 // Structure (one CTA per SM, persistent over a static tile sequence):
-//   warp 0       TMA producer: per stage one 3-D copy each of A (128 rows) and
-//                B (BN rows), two 64-wide k-blocks, 128-byte swizzle, into a
-//                STAGES-deep shared-memory ring (few large copies: a copy
-//                costs a fixed issue time whatever its size)
+//   warp 0       TMA producer: per stage one copy each of A (128 rows) and B
+//                (BN rows) of one 64-wide k-block, 128-byte swizzle, into a
+//                STAGES-deep shared-memory ring (192 KB in all: the weights
+//                come from HBM and the ring must cover that latency)
 //   warp 1       allocates tensor memory; one lane issues tcgen05.mma
 //                (M = 128, N = BN, K = 16) and commits each stage back to the
 //                producer and each finished accumulator to the epilogue
@@ -41,7 +41,7 @@ template <int BN, int STAGES>
 struct TcCfg {
     static constexpr int kBM = kTcRows;
     static constexpr int kBK = 64;       // K per swizzle atom row (128 bytes)
-    static constexpr int kKB = 2;        // k-blocks per stage (one 3-D TMA box each)
+    static constexpr int kKB = 1;        // k-blocks per stage (one 3-D TMA box each)
     static constexpr int kABytes = kBM * kBK * 2 * kKB;
     static constexpr int kBBytes = BN * kBK * 2 * kKB;
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -333,7 +333,7 @@ EncodeTiledFn encode_fn() {
 }
 
 // bf16 matrix [rows, K] (K contiguous) seen as a 3-D tensor {64, rows, K/64}
-// (strides K*2 and 128 bytes), box {64, box_rows, 2}: one copy brings two
+// (strides K*2 and 128 bytes), box {64, box_rows, kKB}: one copy brings kKB
 // 64-wide k-blocks of box_rows rows, each landing as a 128-byte-swizzled
 // K-major tile; a k-block past K/64 reads as zeros.
 bool make_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows) {
@@ -341,7 +341,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint3
     if (!enc) return false;
     cuuint64_t dims[3] = {64, rows, K / 64};
     cuuint64_t strides[2] = {K * 2, 128};
-    cuuint32_t box[3] = {64, box_rows, 2};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -388,10 +388,10 @@ cudaError_t launch_grouped_gemm_tc(const moe_shape &s, const __nv_bfloat16 *A, i
     const int64_t max_tiles = ((S + kTcRows - 1) / kTcRows + s.n) * (N / BN);
     const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
     if (BN == 256)
-        return launch_bn<256, 2>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
+        return launch_bn<256, 4>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
     if (BN == 128)
-        return launch_bn<128, 3>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
-    return launch_bn<64, 4>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
+        return launch_bn<128, 6>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
+    return launch_bn<64, 8>(mA, mB, offsets, tiles, s.n, K, N, bias, relu, out, err, grid, st);
 }
 
 }  // namespace moe

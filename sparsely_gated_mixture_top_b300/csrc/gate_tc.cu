@@ -18,7 +18,7 @@
 //   gate_tc         persistent over 128-token tiles.  Warp 0 issues TMA loads,
 //                   warp 1 issues tcgen05.mma (M=128 tokens, N=128 = 64 clean +
 //                   64 noise columns, hi then lo pass into one fp32 accumulator,
-//                   double-buffered in tensor memory), warps 2..9 are the
+//                   four accumulators in tensor memory), warps 2..9 are the
 //                   epilogue: two warps per tensor-memory lane quarter, each
 //                   owning one half of every chunk's columns for its 32 tokens
 //                   (thread r = token r = tensor-memory lane r).  A first,
@@ -128,17 +128,18 @@ struct TopK {
         }
         return r;
     }
+    // Branch-free: every position takes the better of (its entry, the
+    // carried candidate) and passes the other one down.
     __device__ __forceinline__ void insert(float cv, int ci) {
 #pragma unroll
         for (int p = 0; p < KM; ++p) {
-            if (better(cv, ci, v[p], i[p])) {
-                const float tv = v[p];
-                const int ti = i[p];
-                v[p] = cv;
-                i[p] = ci;
-                cv = tv;
-                ci = ti;
-            }
+            const bool b = (cv > v[p]) | ((cv == v[p]) & (ci < i[p]));
+            const float tv = v[p];
+            const int ti = i[p];
+            v[p] = b ? cv : tv;
+            i[p] = b ? ci : ti;
+            cv = b ? tv : cv;
+            ci = b ? ti : ci;
         }
     }
 };
@@ -178,9 +179,10 @@ struct GateCfg {
     static constexpr int kPrimSlots = kHier ? 2 * KM : 0;
     static constexpr int kFinalSlots = kHier ? KM * KM : KM;
     static constexpr int kXchBytes = (kPrimSlots + kFinalSlots) * kGateRows * 8;
-    static constexpr int kBarBytes = 8 * (2 * kStages + 7) + 16;
+    static constexpr int kBarBytes = 8 * (2 * kStages + 11) + 16;
     static constexpr int kSmem = kXBytes + kStages * kStageBytes + kXchBytes + 1024 + kBarBytes;
-    static constexpr uint32_t kTmemCols = 256;  // 2 accumulators x 128 columns
+    static constexpr int kAcc = 4;               // accumulators (128 columns each)
+    static constexpr uint32_t kTmemCols = 128 * kAcc;
 };
 
 struct GateArgs {
@@ -240,17 +242,18 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     float *xch_v = reinterpret_cast<float *>(sXch);
     int *xch_i = reinterpret_cast<int *>(sXch + (Cfg::kPrimSlots + Cfg::kFinalSlots) * kGateRows * 4);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sXch + Cfg::kXchBytes);
-    // full[S], empty[S], tfull[2], tempty[2], xfull, xempty, drain
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Cfg::kStages + 7);
+    // full[S], empty[S], tfull[4], tempty[4], xfull, xempty, drain
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Cfg::kStages + 11);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
     constexpr int S = Cfg::kStages;
     auto full = [&](int s) { return smem_u32(bars + s); };
     auto empty = [&](int s) { return smem_u32(bars + S + s); };
+    constexpr int NA = Cfg::kAcc;
     auto tfull = [&](int b) { return smem_u32(bars + 2 * S + b); };
-    auto tempty = [&](int b) { return smem_u32(bars + 2 * S + 2 + b); };
-    const uint32_t xfull = smem_u32(bars + 2 * S + 4);
-    const uint32_t xempty = smem_u32(bars + 2 * S + 5);
-    const uint32_t drain_bar = smem_u32(bars + 2 * S + 6);
+    auto tempty = [&](int b) { return smem_u32(bars + 2 * S + NA + b); };
+    const uint32_t xfull = smem_u32(bars + 2 * S + 2 * NA);
+    const uint32_t xempty = smem_u32(bars + 2 * S + 2 * NA + 1);
+    const uint32_t drain_bar = smem_u32(bars + 2 * S + 2 * NA + 2);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NA; ++b) {
             mbar_init(tfull(b), 1);
             mbar_init(tempty(b), 32 * kGateEpiWarps);
         }
@@ -395,7 +398,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                     }
                     if (!ok) break;
                     tc_commit(tfull(acc));
-                    if (++acc == 2) {
+                    if (++acc == NA) {
                         acc = 0;
                         acc_phase ^= 1u;
                     }
@@ -558,7 +561,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                         }
                     }
                 }
-                if (++acc == 2) {
+                if (++acc == NA) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
