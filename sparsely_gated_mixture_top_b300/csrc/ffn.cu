@@ -150,6 +150,21 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt(
 
 }  // namespace
 
+cudaError_t launch_row_tiles(const int32_t *offsets, int n, int bm, int32_t *tiles,
+                             cudaStream_t st) {
+    ffn_tiles<<<1, 1024, 0, st>>>(offsets, n, bm, tiles);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, const int32_t *offsets,
+                               int n, int64_t S, int d, int k, __nv_bfloat16 *out, int32_t *err,
+                               cudaStream_t st) {
+    if (S == 0) return cudaSuccess;
+    ffn_gather<<<static_cast<unsigned>((S + 7) / 8), 256, 0, st>>>(x, perm, offsets, n, S, d, k, out,
+                                                                 err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *perm,
                               const int32_t *offsets, const void *W1, const float *b1,
                               const void *W2, const float *b2, void *Y_slot, void *ws,

@@ -1,6 +1,5 @@
 // gate.cu -- noisy top-k gating ("MoE:稀疏门控混合专家", sections 三 and 四),
-// CUDA-core path: fp32 inputs, and hierarchical shapes with more than 4 kept
-// groups or experts per group (bf16 shapes otherwise take gate_tc.cu).
+// CUDA-core path for fp32 inputs (bf16 shapes take gate_tc.cu).
 //
 // Two kernels:
 //   gate_scores_simt  H[t,c] = x[t].Wg[:,c] (+ bg[c]) + eps[t,c] * softplus(x[t].Wn[:,c])
@@ -232,9 +231,7 @@ void launch_select(const float *H, const moe_shape &s, int C, int32_t *idx, floa
 cudaError_t launch_gate(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
                         const float *bg, const float *eps, int32_t *idx, float *G, void *ws,
                         const WsLayout &L, cudaStream_t st) {
-    if (gate_tc_supported(s))
-        return launch_gate_tc(s, x, Wg, Wn, bg, eps, idx, G, ws_ptr<void>(ws, L.gpack),
-                              ws_ptr<int32_t>(ws, 0), st);
+    if (gate_tc_supported(s)) return launch_gate_tc(s, x, Wg, Wn, bg, eps, idx, G, ws, L, st);
     float *Hbuf = ws_ptr<float>(ws, L.scores);
     const int C = gate_cols(s);
     const int noisy = (s.noisy && eps != nullptr) ? 1 : 0;

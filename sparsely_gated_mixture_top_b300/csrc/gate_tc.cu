@@ -8,20 +8,19 @@
 // tcgen05.mma: every product is exact and the sum carries fp32 rounding only,
 // like an fp32 dot product.
 //
-//   gate_pack       W_g, W_noise [d, C] fp32 -> hi/lo bf16 units, one 32 KB
+//   gate_pack       W_g, W_noise [d, ldw] fp32 -> hi/lo bf16 units, one 32 KB
 //                   unit per (chunk, 64-wide k-block), stored pre-swizzled so
 //                   that one bulk copy fills a pipeline stage: chunk c holds 64
 //                   clean-score columns (rows 0..63) and the same 64
-//                   noise-score columns (rows 64..127).  Hierarchical: the G
-//                   group columns come first (padded to a chunk boundary),
-//                   then the n inner columns.
-//   gate_tc         persistent over 128-token tiles.  Warp 0 issues TMA loads,
-//                   warp 1 issues tcgen05.mma (M=128 tokens, N=128 = 64 clean +
+//                   noise-score columns (rows 64..127).  In grouped packing
+//                   every group's m columns start on a chunk boundary.
+//   gate_tc         persistent over 128-row tiles.  Warp 0 issues the copies,
+//                   warp 1 issues tcgen05.mma (M=128 rows, N=128 = 64 clean +
 //                   64 noise columns, hi then lo pass into one fp32 accumulator,
 //                   four accumulators in tensor memory), warps 2..9 are the
 //                   epilogue: two warps per tensor-memory lane quarter, each
-//                   owning one half of every chunk's columns for its 32 tokens
-//                   (thread r = token r = tensor-memory lane r).  A first,
+//                   owning one half of every chunk's columns for its 32 rows
+//                   (thread r = row r = tensor-memory lane r).  A first,
 //                   branch-free pass over 16 columns at a time computes
 //                   H = clean (+ b_g) + eps * softplus(noise) (softplus from
 //                   the hardware exp/log) and flags the columns that beat the
@@ -29,11 +28,20 @@
 //                   flagged ones (KeepTopK, ties to the lower index).  The
 //                   halves merge their lists through shared memory and the
 //                   softmax runs over the k survivors.
-//                   Hierarchical gating picks the groups from the first chunks
-//                   (both halves merge them) and only then looks at (and reads
-//                   eps for) the inner columns of its chosen groups.
-// x stays resident in shared memory for the whole tile when d <= 512;
-// otherwise each stage carries its x block with the W blocks.
+//
+// Flat gating runs gate_tc once over the tokens and all n columns.
+// Hierarchical gating (MoE-N-h, section 三: pick the groups, then the experts
+// inside each chosen group) runs it twice:
+//   1. flat over the G group columns -> the k_g chosen groups of every token
+//      and their softmax weights Gp;
+//   2. the (token, rank) pairs are routed by group with the dispatch kernels,
+//      their x rows gathered into group order, and gate_tc in grouped mode
+//      scores each 128-row tile of one group against that group's m columns
+//      only; a row's k_i survivors get the weights Gp * softmax.
+// So the inner scores cost T * k_g * m columns instead of T * n.
+// x (or the gathered rows) stays resident in shared memory for the whole
+// tile when d <= 512; otherwise each stage carries its x block with the W
+// blocks.
 #include "moe_device.cuh"
 #include "moe_launch.h"
 
@@ -46,30 +54,27 @@ namespace moe {
 
 namespace {
 
-constexpr int kGateChunk = 64;       // score columns (clean and noise each) per chunk
-constexpr int kGateRows = 128;       // tokens per tile
-constexpr int kGateBK = 64;          // d per k-block
+constexpr int kGateChunk = 64;         // score columns (clean and noise each) per chunk
+constexpr int kGateRows = 128;         // rows per tile
+constexpr int kGateBK = 64;            // d per k-block
 constexpr int kKBytes = 128 * 64 * 2;  // one 128 x 64 bf16 block: 16 KB
 
 // ---------------------------------------------------------------------------
 // Packing
 // ---------------------------------------------------------------------------
-// Logical chunk column lc -> source column of W (or -1 for padding).
-__host__ __device__ __forceinline__ int gate_source_col(int lc, int C, int groups, int prim_pad) {
-    if (groups == 0) return lc < C ? lc : -1;
-    if (lc < prim_pad) return lc < groups ? lc : -1;
-    const int ic = lc - prim_pad;
-    return ic < C - groups ? groups + ic : -1;
-}
-
-// Block: 64 d-rows (k-block kb) x 64 logical columns of one matrix (clean or
-// noise).  Output: for every (chunk, k-block) a 32 KB unit [hi | lo], each a
-// 128-row x 64-element bf16 tile already in the 128-byte-swizzled K-major
-// order a TMA copy would produce (16-byte group g of row r stored at group
-// g ^ (r % 8)), so that one bulk copy moves it into shared memory.
+// Block: 64 d-rows (k-block kb = blockIdx.z) x 64 chunk columns of one matrix
+// (clean or noise).  Chunk column lc of chunk `chunk` takes W column
+//   group_m == 0: col_base + chunk*64 + lc            (if < ncols columns)
+//   group_m  > 0: col_base + g*group_m + cl, with g = chunk / mchunks and
+//                 cl = (chunk % mchunks)*64 + lc      (if cl < group_m)
+// and zero elsewhere.  Output: for every (chunk, k-block) a 32 KB unit
+// [hi | lo], each a 128-row x 64-element bf16 tile already in the
+// 128-byte-swizzled K-major order a TMA copy would produce (16-byte group g
+// of row r stored at group g ^ (r % 8)), so that one bulk copy moves it.
 __global__ void __launch_bounds__(256) gate_pack(const float *__restrict__ Wg,
-                                                 const float *__restrict__ Wn, int d, int C,
-                                                 int groups, int prim_pad, int noisy,
+                                                 const float *__restrict__ Wn, int d, int ldw,
+                                                 int col_base, int ncols, int group_m,
+                                                 int mchunks, int noisy,
                                                  uint8_t *__restrict__ pack) {
     __shared__ float tile[64][65];
     const int chunk = blockIdx.x;
@@ -77,14 +82,21 @@ __global__ void __launch_bounds__(256) gate_pack(const float *__restrict__ Wg,
     const int d0 = blockIdx.z * 64;
     const float *W = which ? Wn : Wg;
     const int tx = threadIdx.x % 64, ty = threadIdx.x / 64;
-    const int src = gate_source_col(chunk * kGateChunk + tx, C, groups, prim_pad);
+    int src;
+    if (group_m == 0) {
+        const int col = chunk * kGateChunk + tx;
+        src = col < ncols ? col_base + col : -1;
+    } else {
+        const int g = chunk / mchunks;
+        const int cl = (chunk - g * mchunks) * kGateChunk + tx;
+        src = cl < group_m ? col_base + g * group_m + cl : -1;
+    }
     for (int r = ty; r < 64; r += 4) {
         float v = 0.0f;
-        if (src >= 0 && (which == 0 || noisy)) v = W[static_cast<int64_t>(d0 + r) * C + src];
+        if (src >= 0 && (which == 0 || noisy)) v = W[static_cast<int64_t>(d0 + r) * ldw + src];
         tile[r][tx] = v;  // tile[d][col]
     }
     __syncthreads();
-    // Write rows (one per column) of 64 d-values: thread (col = ty.., dd = tx).
     for (int cc = ty; cc < 64; cc += 4) {
         const float v = tile[tx][cc];
         const __nv_bfloat16 hi = __float2bfloat16_rn(v);
@@ -98,12 +110,8 @@ __global__ void __launch_bounds__(256) gate_pack(const float *__restrict__ Wg,
 }
 
 // ---------------------------------------------------------------------------
-// Per-token running top-k (registers only; all indices compile-time)
+// Per-row running top-k (registers only; all indices compile-time)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
-    return a > b || (a == b && ia < ib);
-}
-
 template <int KM>
 struct TopK {
     float v[KM];
@@ -129,7 +137,8 @@ struct TopK {
         return r;
     }
     // Branch-free: every position takes the better of (its entry, the
-    // carried candidate) and passes the other one down.
+    // carried candidate) and passes the other one down.  Better = larger
+    // value, equal values by lower index.
     __device__ __forceinline__ void insert(float cv, int ci) {
 #pragma unroll
         for (int p = 0; p < KM; ++p) {
@@ -164,39 +173,44 @@ __device__ __forceinline__ void softmax_top(const TopK<KM> &t, int kk, float (&w
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-constexpr int kGateEpiWarps = 8;                 // two per tensor-memory lane quarter
+constexpr int kGateEpiWarps = 8;  // two per tensor-memory lane quarter
 constexpr int kGateThreads = 32 * (2 + kGateEpiWarps);
 
-template <bool kResident, bool kHier, int KM>
+template <bool kResident, int KM>
 struct GateCfg {
     // Stage: the hi and lo W tiles of one (chunk, k-block) unit (plus, when x
     // is not resident, that k-block of x).
     static constexpr int kStages = kResident ? 2 : 3;
     static constexpr int kStageBytes = kResident ? 2 * kKBytes : 3 * kKBytes;
     static constexpr int kXBytes = kResident ? 8 * kKBytes : 0;  // d <= 512
-    // Exchange between the two column halves: the group lists of both halves
-    // (hierarchical only) and the final lists of half 1, [slot][token] order.
-    static constexpr int kPrimSlots = kHier ? 2 * KM : 0;
-    static constexpr int kFinalSlots = kHier ? KM * KM : KM;
-    static constexpr int kXchBytes = (kPrimSlots + kFinalSlots) * kGateRows * 8;
-    static constexpr int kBarBytes = 8 * (2 * kStages + 11) + 16;
+    // Exchange of the final lists of half 1, [slot][row] order.
+    static constexpr int kXchBytes = KM * kGateRows * 8;
+    static constexpr int kAcc = 4;  // accumulators (128 columns each)
+    static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kAcc + 3) + 16;
     static constexpr int kSmem = kXBytes + kStages * kStageBytes + kXchBytes + 1024 + kBarBytes;
-    static constexpr int kAcc = 4;               // accumulators (128 columns each)
     static constexpr uint32_t kTmemCols = 128 * kAcc;
 };
 
 struct GateArgs {
-    const __nv_bfloat16 *x;
-    const float *bg;
-    const float *eps;
-    int32_t *idx;
-    float *G;
-    int64_t T;
-    int d, C, n, k;
-    int groups, k_groups, m, prim_pad;
-    int chunks, prim_chunks;
+    const float *bg;   // [C] or NULL
+    const float *eps;  // rows of ldE floats, or NULL (clean scores)
+    int32_t *idx;      // [T, k]
+    float *G;          // [T, k]
+    int64_t T;         // tokens (flat: rows)
+    int d;
+    int k;             // outputs per token
+    int kk;            // list length used: flat k; grouped k_inner
+    int ncols;         // score columns of one row's list (flat: C; grouped: m)
+    int chunks;        // chunks per tile
+    int ldE;           // eps row stride (floats)
     int noisy;
     int32_t *err;
+    // grouped mode (pairs = (token, rank) rows, ordered by group)
+    const int32_t *perm_g;     // [T*kg] row -> pair = t*kg + q
+    const int32_t *offsets_g;  // [G+1]
+    const int32_t *tiles_g;    // [G+1] row-tile starts
+    const float *gw;           // [T*kg] group weights
+    int groups, kg, m;
 };
 
 // Named barrier of the eight epilogue warps.
@@ -204,17 +218,15 @@ __device__ __forceinline__ void epi_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kGateEpiWarps) : "memory");
 }
 
-// eps[row][col0 + j] for the 32 columns j of one chunk half whose bit is set
-// in `live` (0 elsewhere).  Vector loads when the row stride and col0 allow
-// 16-byte alignment (then every live group of 4 is all live).
+// eps[row][col0 + j] for the 32 columns j of one chunk half (0 past C).
+// Vector loads when the row stride and col0 allow 16-byte alignment.
 __device__ __forceinline__ void load_eps32(const float *__restrict__ row, int col0, int C,
-                                           bool vec, uint32_t live, float (&ev)[32]) {
+                                           bool vec, float (&ev)[32]) {
     if (vec) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (col0 + 4 * q < C && ((live >> (4 * q)) & 1u))
-                v = __ldg(reinterpret_cast<const float4 *>(row + col0 + 4 * q));
+            if (col0 + 4 * q < C) v = __ldg(reinterpret_cast<const float4 *>(row + col0 + 4 * q));
             ev[4 * q] = v.x;
             ev[4 * q + 1] = v.y;
             ev[4 * q + 2] = v.z;
@@ -222,33 +234,61 @@ __device__ __forceinline__ void load_eps32(const float *__restrict__ row, int co
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            ev[j] = (col0 + j < C && ((live >> j) & 1u)) ? __ldg(row + col0 + j) : 0.0f;
+        for (int j = 0; j < 32; ++j) ev[j] = (col0 + j < C) ? __ldg(row + col0 + j) : 0.0f;
     }
 }
 
-// KM: list size for flat (>= k) or for each hierarchical level (>= k_groups, k_inner).
-template <bool kResident, bool kHier, int KM>
+struct GateTile {
+    int g, row0, rows;
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ GateTile gate_tile(int tile, const GateArgs &a) {
+    GateTile ti;
+    if (!kGrouped) {
+        ti.g = 0;
+        ti.row0 = tile * kGateRows;
+        const int64_t left = a.T - ti.row0;
+        ti.rows = left < kGateRows ? static_cast<int>(left) : kGateRows;
+    } else {
+        int lo = 0, hi = a.groups - 1;  // largest g with tiles_g[g] <= tile
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.tiles_g[mid] <= tile)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        ti.g = lo;
+        ti.row0 = a.offsets_g[lo] + (tile - a.tiles_g[lo]) * kGateRows;
+        ti.rows = min(kGateRows, a.offsets_g[lo + 1] - ti.row0);
+    }
+    return ti;
+}
+
+// KM: list size (>= kk).  kGrouped: rows are (token, rank) pairs of one group
+// per tile, scored against that group's columns.
+template <bool kResident, bool kGrouped, int KM>
 __global__ void __launch_bounds__(kGateThreads, 1)
     gate_tc(const __grid_constant__ CUtensorMap mapX, const uint8_t *__restrict__ wpack,
             const GateArgs a) {
-    using Cfg = GateCfg<kResident, kHier, KM>;
+    using Cfg = GateCfg<kResident, KM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *sX = smem;                        // resident x tile (kResident)
-    uint8_t *sS = smem + Cfg::kXBytes;         // stage ring
+    uint8_t *sX = smem;                 // resident x tile (kResident)
+    uint8_t *sS = smem + Cfg::kXBytes;  // stage ring
     uint8_t *sXch = sS + Cfg::kStages * Cfg::kStageBytes;
     float *xch_v = reinterpret_cast<float *>(sXch);
-    int *xch_i = reinterpret_cast<int *>(sXch + (Cfg::kPrimSlots + Cfg::kFinalSlots) * kGateRows * 4);
+    int *xch_i = reinterpret_cast<int *>(sXch + KM * kGateRows * 4);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sXch + Cfg::kXchBytes);
-    // full[S], empty[S], tfull[4], tempty[4], xfull, xempty, drain
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Cfg::kStages + 11);
-    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
     constexpr int S = Cfg::kStages;
+    constexpr int NA = Cfg::kAcc;
+    // full[S], empty[S], tfull[NA], tempty[NA], xfull, xempty, drain
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 2 * NA + 3);
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
     auto full = [&](int s) { return smem_u32(bars + s); };
     auto empty = [&](int s) { return smem_u32(bars + S + s); };
-    constexpr int NA = Cfg::kAcc;
     auto tfull = [&](int b) { return smem_u32(bars + 2 * S + b); };
     auto tempty = [&](int b) { return smem_u32(bars + 2 * S + NA + b); };
     const uint32_t xfull = smem_u32(bars + 2 * S + 2 * NA);
@@ -271,9 +311,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&mapX);
-    }
+    if (warp == 0 && lane == 0) tma_prefetch_map(&mapX);
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
         tmem_relinquish();
@@ -282,7 +320,8 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int tiles = static_cast<int>((a.T + kGateRows - 1) / kGateRows);
+    const int tiles = kGrouped ? a.tiles_g[a.groups]
+                               : static_cast<int>((a.T + kGateRows - 1) / kGateRows);
     const int kblocks = a.d / kGateBK;
 
     if (warp == 0) {
@@ -293,7 +332,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
             bool ok = true;
             int64_t issued = 0;
             for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-                const int row0 = tile * kGateRows;
+                const GateTile ti = gate_tile<kGrouped>(tile, a);
                 if (kResident) {
                     if (!mbar_wait_bounded(xempty, xphase ^ 1u, abort_flag, a.err, kSiteTcProducer)) {
                         ok = false;
@@ -302,8 +341,9 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                     xphase ^= 1u;
                     // the whole x tile (all k-blocks) in one 3-D copy
                     mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(kblocks * kKBytes));
-                    tma_load_3d(smem_u32(sX), &mapX, xfull, 0, row0, 0);
+                    tma_load_3d(smem_u32(sX), &mapX, xfull, 0, ti.row0, 0);
                 }
+                const int64_t unit0 = static_cast<int64_t>(ti.g) * a.chunks;
                 for (int c = 0; c < a.chunks && ok; ++c) {
                     for (int kb = 0; kb < kblocks && ok; ++kb) {
                         if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, a.err,
@@ -312,14 +352,13 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                             break;
                         }
                         uint8_t *st = sS + stage * Cfg::kStageBytes;
-                        const uint8_t *unit =
-                            wpack + (static_cast<int64_t>(c) * kblocks + kb) * (2 * kKBytes);
+                        const uint8_t *unit = wpack + ((unit0 + c) * kblocks + kb) * (2 * kKBytes);
                         if (kResident) {
                             mbar_arrive_expect_tx(full(stage), 2 * kKBytes);
                             bulk_load(smem_u32(st), unit, 2 * kKBytes, full(stage));
                         } else {
                             mbar_arrive_expect_tx(full(stage), 3 * kKBytes);
-                            tma_load_3d(smem_u32(st), &mapX, full(stage), 0, row0, kb);
+                            tma_load_3d(smem_u32(st), &mapX, full(stage), 0, ti.row0, kb);
                             bulk_load(smem_u32(st + kKBytes), unit, 2 * kKBytes, full(stage));
                         }
                         ++issued;
@@ -413,82 +452,52 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         }
     } else {
         // ------------------------------ epilogue ------------------------------
-        // Warp w (2..9) reads tensor-memory lanes 32*(w%4).. (token r of the
+        // Warp w (2..9) reads tensor-memory lanes 32*(w%4).. (row r of the
         // tile) and column half `half` of every chunk: clean columns
         // half*32 .. +32 and the matching noise columns 64 + half*32 .. +32.
         // Each thread keeps the running top-k of its half; the halves merge
-        // through shared memory at the end of the tile (hierarchical: also
-        // after the group columns, since both halves need the chosen groups).
+        // through shared memory at the end of the tile.
         const int half = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-        const int k_inner = kHier ? a.k / a.k_groups : a.k;
-        const int kk_prim = kHier ? a.k_groups : a.k;
-        const bool vec_eps = (a.C & 3) == 0;
-        constexpr int kFinalOff = Cfg::kPrimSlots * kGateRows;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-            const int64_t t = static_cast<int64_t>(tile) * kGateRows + r;
-            const bool valid = t < a.T;
-            const bool noisy = valid && a.noisy;
-            const float *eps_row = noisy ? a.eps + t * a.C : nullptr;
-            TopK<KM> prim;  // flat: the only list; hierarchical: the groups
-            TopK<KM> inner[kHier ? KM : 1];
-            prim.reset();
-#pragma unroll
-            for (int q = 0; q < (kHier ? KM : 1); ++q) inner[q].reset();
-            float gw[KM];
-            int glo[KM];  // hierarchical: first inner column of each chosen group
-#pragma unroll
-            for (int q = 0; q < KM; ++q) {
-                gw[q] = 0.0f;
-                glo[q] = -0x40000000;
-            }
-            for (int c = 0; c < a.chunks; ++c) {
-                const bool inner_chunk = kHier && c >= a.prim_chunks;
-                if (kHier && c == a.prim_chunks) {
-                    // both halves publish their group lists and merge the other's
-#pragma unroll
-                    for (int q = 0; q < KM; ++q) {
-                        xch_v[(half * KM + q) * kGateRows + r] = prim.v[q];
-                        xch_i[(half * KM + q) * kGateRows + r] = prim.i[q];
-                    }
-                    epi_bar();
-#pragma unroll
-                    for (int q = 0; q < KM; ++q)
-                        prim.insert(xch_v[((1 - half) * KM + q) * kGateRows + r],
-                                    xch_i[((1 - half) * KM + q) * kGateRows + r]);
-                    softmax_top<KM>(prim, kk_prim, gw);
-#pragma unroll
-                    for (int q = 0; q < KM; ++q)
-                        if (q < a.k_groups) glo[q] = prim.i[q] * a.m;
+            const GateTile ti = gate_tile<kGrouped>(tile, a);
+            const bool valid = r < ti.rows;
+            // The row's token, its output slots and the score columns it reads.
+            int64_t t = ti.row0 + r;
+            int64_t out0 = t * a.k;
+            float wrow = 1.0f;
+            int col_off = 0;  // eps/bg column of list column 0
+            if (kGrouped) {
+                t = 0;
+                out0 = 0;
+                if (valid) {
+                    const int pair = a.perm_g[ti.row0 + r];
+                    t = pair / a.kg;
+                    const int q = pair - static_cast<int>(t) * a.kg;
+                    out0 = t * a.k + static_cast<int64_t>(q) * a.kk;
+                    wrow = a.gw[pair];
                 }
-                // columns of this chunk half (score index space of the list)
-                const int col0 = inner_chunk ? (c - a.prim_chunks) * kGateChunk + half * 32
-                                             : c * kGateChunk + half * 32;
-                const int ncols = inner_chunk ? a.n : (kHier ? a.groups : a.C);
-                const int ecol0 = inner_chunk ? a.groups + col0 : col0;  // eps / bg column
-                if (eps_row && !kHier && c + 2 < a.chunks && (c + 2) * kGateChunk + half * 32 < a.C)
-                    prefetch_l2(eps_row + (c + 2) * kGateChunk + half * 32);
+                col_off = a.groups + ti.g * a.m;
+            }
+            const bool noisy = valid && a.noisy;
+            const float *eps_row = noisy ? a.eps + t * a.ldE + col_off : nullptr;
+            const float *bg_row = a.bg ? a.bg + col_off : nullptr;
+            // 16-byte loads need an aligned row, column base and column count
+            const bool vec_eps = ((a.ldE | col_off | a.ncols) & 3) == 0;
+            TopK<KM> list;
+            list.reset();
+            for (int c = 0; c < a.chunks; ++c) {
+                const int col0 = c * kGateChunk + half * 32;  // list column of this half
+                if (eps_row && c + 2 < a.chunks && col0 + 2 * kGateChunk < a.ncols)
+                    prefetch_l2(eps_row + col0 + 2 * kGateChunk);
                 float ev[32];
-                if (eps_row && col0 < ncols) {
-                    uint32_t live = 0xffffffffu;
-                    bool vec = vec_eps;
-                    if (inner_chunk) {
-                        live = 0;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            #pragma unroll
-                            for (int qq = 0; qq < KM; ++qq)
-                                if (qq < a.k_groups && static_cast<unsigned>(col0 + j - glo[qq]) <
-                                                           static_cast<unsigned>(a.m))
-                                    live |= 1u << j;
-                        vec = vec && (ecol0 & 3) == 0 && (a.m & 3) == 0;
-                    }
-                    load_eps32(eps_row, ecol0, a.C, vec, live, ev);
+                if (eps_row && col0 < a.ncols) {
+                    load_eps32(eps_row, col0, a.ncols, vec_eps, ev);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) ev[j] = 0.0f;
@@ -499,11 +508,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                 ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the votes below need every lane
                 if (ok) {
                     tc_fence_after();
-                    // Pass 1 thresholds: the k-th entry of each list, fixed for the span.
-                    const float thr_p = prim.kth(kk_prim);
-                    float thr_i[kHier ? KM : 1];
-#pragma unroll
-                    for (int qq = 0; qq < (kHier ? KM : 1); ++qq) thr_i[qq] = inner[qq].kth(k_inner);
+                    const float thr = list.kth(a.kk);  // fixed for the span
 #pragma unroll
                     for (int piece = 0; piece < 2; ++piece) {
                         uint32_t cv[16], nv[16];
@@ -516,28 +521,20 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                             mbar_arrive(tempty(acc));  // this half of the accumulator is read
                         }
                         // Pass 1 (branch-free): the noisy score of every column and
-                        // which ones beat the k-th entry of their list.  Within a
+                        // which ones beat the k-th entry of the list.  Within a
                         // thread's list the columns arrive in increasing index order,
                         // so an equal score never displaces an entry: '>' is exact.
-                        // Tokens past T flag nothing but still take part in the votes.
+                        // Rows past the tile flag nothing but still take part in the
+                        // votes.
                         uint32_t pass = 0;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int sc = col0 + piece * 16 + j;
                             float h = __uint_as_float(cv[j]);
-                            if (a.bg && sc < ncols) h += __ldg(a.bg + ecol0 + piece * 16 + j);
+                            if (bg_row && sc < a.ncols) h += __ldg(bg_row + sc);
                             if (noisy) h += ev[piece * 16 + j] * softplus_fast(__uint_as_float(nv[j]));
                             cv[j] = __float_as_uint(h);
-                            float thr = thr_p;
-                            if (inner_chunk) {
-                                thr = INFINITY;  // outside the chosen groups
-#pragma unroll
-                                for (int qq = 0; qq < (kHier ? KM : 1); ++qq)
-                                    if (qq < a.k_groups &&
-                                        static_cast<unsigned>(sc - glo[qq]) < static_cast<unsigned>(a.m))
-                                        thr = thr_i[qq];
-                            }
-                            if (valid && sc < ncols && h > thr) pass |= 1u << j;
+                            if (valid && sc < a.ncols && h > thr) pass |= 1u << j;
                         }
                         // Pass 2 (rare): insert the flagged columns.  The warp vote
                         // keeps each column's insertion a real branch.
@@ -545,18 +542,8 @@ __global__ void __launch_bounds__(kGateThreads, 1)
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 if (!__any_sync(0xffffffffu, (pass >> j) & 1u)) continue;
-                                if (!((pass >> j) & 1u)) continue;
-                                const int sc = col0 + piece * 16 + j;
-                                const float h = __uint_as_float(cv[j]);
-                                if (!inner_chunk) {
-                                    prim.insert(h, sc);
-                                } else {
-#pragma unroll
-                                    for (int qq = 0; qq < (kHier ? KM : 1); ++qq)
-                                        if (qq < a.k_groups && static_cast<unsigned>(sc - glo[qq]) <
-                                                                   static_cast<unsigned>(a.m))
-                                            inner[qq].insert(h, sc - glo[qq]);
-                                }
+                                if ((pass >> j) & 1u)
+                                    list.insert(__uint_as_float(cv[j]), col0 + piece * 16 + j);
                             }
                         }
                     }
@@ -566,59 +553,29 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                     acc_phase ^= 1u;
                 }
             }
-            // half 1 hands its lists to half 0, which merges and writes the token
+            // half 1 hands its list to half 0, which merges and writes the row
             epi_bar();  // half 0 is done with the previous tile's exchange
             if (half == 1) {
-                if (!kHier) {
 #pragma unroll
-                    for (int q = 0; q < KM; ++q) {
-                        xch_v[kFinalOff + q * kGateRows + r] = prim.v[q];
-                        xch_i[kFinalOff + q * kGateRows + r] = prim.i[q];
-                    }
-                } else {
-#pragma unroll
-                    for (int g = 0; g < (kHier ? KM : 1); ++g)
-#pragma unroll
-                        for (int q = 0; q < KM; ++q) {
-                            xch_v[kFinalOff + (g * KM + q) * kGateRows + r] = inner[g].v[q];
-                            xch_i[kFinalOff + (g * KM + q) * kGateRows + r] = inner[g].i[q];
-                        }
+                for (int q = 0; q < KM; ++q) {
+                    xch_v[q * kGateRows + r] = list.v[q];
+                    xch_i[q * kGateRows + r] = list.i[q];
                 }
             }
             epi_bar();
             if (half == 0 && ok && valid) {
-                if (!kHier) {
 #pragma unroll
-                    for (int q = 0; q < KM; ++q)
-                        prim.insert(xch_v[kFinalOff + q * kGateRows + r],
-                                    xch_i[kFinalOff + q * kGateRows + r]);
-                    float w[KM];
-                    softmax_top<KM>(prim, a.k, w);
+                for (int q = 0; q < KM; ++q)
+                    list.insert(xch_v[q * kGateRows + r], xch_i[q * kGateRows + r]);
+                float w[KM];
+                softmax_top<KM>(list, a.kk, w);
+                const int id_off = kGrouped ? ti.g * a.m : 0;
 #pragma unroll
-                    for (int q = 0; q < KM; ++q)
-                        if (q < a.k) {
-                            a.idx[t * a.k + q] = prim.i[q];
-                            a.G[t * a.k + q] = w[q];
-                        }
-                } else {
-#pragma unroll
-                    for (int g = 0; g < (kHier ? KM : 1); ++g) {
-                        if (g >= a.k_groups) break;
-#pragma unroll
-                        for (int q = 0; q < KM; ++q)
-                            inner[g].insert(xch_v[kFinalOff + (g * KM + q) * kGateRows + r],
-                                            xch_i[kFinalOff + (g * KM + q) * kGateRows + r]);
-                        float wi[KM];
-                        softmax_top<KM>(inner[g], k_inner, wi);
-                        const int grp = prim.i[g];
-#pragma unroll
-                        for (int e = 0; e < KM; ++e)
-                            if (e < k_inner) {
-                                a.idx[t * a.k + g * k_inner + e] = grp * a.m + inner[g].i[e];
-                                a.G[t * a.k + g * k_inner + e] = gw[g] * wi[e];
-                            }
+                for (int q = 0; q < KM; ++q)
+                    if (q < a.kk) {
+                        a.idx[out0 + q] = id_off + list.i[q];
+                        a.G[out0 + q] = wrow * w[q];
                     }
-                }
             }
         }
     }
@@ -648,8 +605,8 @@ EncodeTiledFn gate_encode_fn() {
     return fn;
 }
 
-// x [T, d] bf16 seen as {64, T, d/64} (strides d*2 and 128 bytes); a box of
-// 128 tokens x kb_box k-blocks lands as kb_box 128-byte-swizzled K-major tiles.
+// x [rows, d] bf16 seen as {64, rows, d/64} (strides d*2 and 128 bytes); a box
+// of 128 rows x kb_box k-blocks lands as kb_box 128-byte-swizzled K-major tiles.
 bool gate_map(CUtensorMap *m, const void *base, uint64_t d, uint64_t rows, uint32_t kb_box) {
     EncodeTiledFn enc = gate_encode_fn();
     if (!enc) return false;
@@ -662,98 +619,150 @@ bool gate_map(CUtensorMap *m, const void *base, uint64_t d, uint64_t rows, uint3
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kResident, bool kHier, int KM>
+template <bool kResident, bool kGrouped, int KM>
 cudaError_t launch_gate_tc_t(const CUtensorMap &mx, const uint8_t *wpack, const GateArgs &ga,
                              int grid, cudaStream_t st) {
-    using Cfg = GateCfg<kResident, kHier, KM>;
+    using Cfg = GateCfg<kResident, KM>;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(gate_tc<kResident, kHier, KM>,
+        attr = cudaFuncSetAttribute(gate_tc<kResident, kGrouped, KM>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     });
     if (attr != cudaSuccess) return attr;
-    gate_tc<kResident, kHier, KM><<<grid, kGateThreads, Cfg::kSmem, st>>>(mx, wpack, ga);
+    gate_tc<kResident, kGrouped, KM><<<grid, kGateThreads, Cfg::kSmem, st>>>(mx, wpack, ga);
     return cudaGetLastError();
 }
 
-template <bool kResident, bool kHier>
-cudaError_t launch_gate_tc_km(int km, const CUtensorMap &mx, const uint8_t *wpack,
+template <bool kGrouped>
+cudaError_t launch_gate_tc_km(bool resident, int km, const CUtensorMap &mx, const uint8_t *wpack,
                               const GateArgs &ga, int grid, cudaStream_t st) {
-    if (km <= 2) return launch_gate_tc_t<kResident, kHier, 2>(mx, wpack, ga, grid, st);
-    if (km <= 4) return launch_gate_tc_t<kResident, kHier, 4>(mx, wpack, ga, grid, st);
-    if constexpr (kHier) {
-        return cudaErrorInvalidValue;  // hierarchical lists are limited to 4
-    } else {
-        if (km <= 8) return launch_gate_tc_t<kResident, kHier, 8>(mx, wpack, ga, grid, st);
-        return launch_gate_tc_t<kResident, kHier, 16>(mx, wpack, ga, grid, st);
+    if (resident) {
+        if (km <= 2) return launch_gate_tc_t<true, kGrouped, 2>(mx, wpack, ga, grid, st);
+        if (km <= 4) return launch_gate_tc_t<true, kGrouped, 4>(mx, wpack, ga, grid, st);
+        if (km <= 8) return launch_gate_tc_t<true, kGrouped, 8>(mx, wpack, ga, grid, st);
+        return launch_gate_tc_t<true, kGrouped, 16>(mx, wpack, ga, grid, st);
     }
+    if (km <= 2) return launch_gate_tc_t<false, kGrouped, 2>(mx, wpack, ga, grid, st);
+    if (km <= 4) return launch_gate_tc_t<false, kGrouped, 4>(mx, wpack, ga, grid, st);
+    if (km <= 8) return launch_gate_tc_t<false, kGrouped, 8>(mx, wpack, ga, grid, st);
+    return launch_gate_tc_t<false, kGrouped, 16>(mx, wpack, ga, grid, st);
 }
+
+int chunks_of(int cols) { return (cols + kGateChunk - 1) / kGateChunk; }
 
 }  // namespace
 
 size_t gate_tc_pack_bytes(const moe_shape &s) {
-    const int C = gate_cols(s);
     int chunks;
     if (s.groups == 0) {
-        chunks = (C + kGateChunk - 1) / kGateChunk;
+        chunks = chunks_of(s.n);
     } else {
-        chunks = (s.groups + kGateChunk - 1) / kGateChunk + (s.n + kGateChunk - 1) / kGateChunk;
+        chunks = chunks_of(s.groups) + s.groups * chunks_of(s.n / s.groups);
     }
     return static_cast<size_t>(chunks) * 128 * s.d * 2 * 2;  // hi + lo
 }
 
-bool gate_tc_supported(const moe_shape &s) {
-    if (s.dtype != MOE_BF16) return false;
-    if (s.groups == 0) return s.k <= 16;
-    return s.k_groups <= 4 && s.k / s.k_groups <= 4;
-}
+bool gate_tc_supported(const moe_shape &s) { return s.dtype == MOE_BF16; }
 
 cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
-                           const float *bg, const float *eps, int32_t *idx, float *G, void *pack,
-                           int32_t *err, cudaStream_t st) {
+                           const float *bg, const float *eps, int32_t *idx, float *G, void *ws,
+                           const WsLayout &L, cudaStream_t st) {
     const int C = gate_cols(s);
     const int noisy = (s.noisy && eps != nullptr && Wn != nullptr) ? 1 : 0;
-    GateArgs ga;
-    ga.x = static_cast<const __nv_bfloat16 *>(x);
+    const bool resident = s.d <= 512;
+    const int kblocks = s.d / 64;
+    int32_t *err = ws_ptr<int32_t>(ws, 0);
+    uint8_t *pack = ws_ptr<uint8_t>(ws, L.gpack);
+    const float *Wnp = noisy ? Wn : Wg;
+    GateArgs ga{};
     ga.bg = bg;
-    ga.eps = eps;
-    ga.idx = idx;
-    ga.G = G;
+    ga.eps = noisy ? eps : nullptr;
     ga.T = s.T;
     ga.d = s.d;
-    ga.C = C;
-    ga.n = s.n;
-    ga.k = s.k;
-    ga.groups = s.groups;
-    ga.k_groups = s.k_groups;
-    ga.m = s.groups ? s.n / s.groups : s.n;
+    ga.ldE = C;
     ga.noisy = noisy;
     ga.err = err;
+    const int sms = sm_count();
     if (s.groups == 0) {
-        ga.prim_pad = 0;
-        ga.prim_chunks = 0;
-        ga.chunks = (C + kGateChunk - 1) / kGateChunk;
-    } else {
-        ga.prim_chunks = (s.groups + kGateChunk - 1) / kGateChunk;
-        ga.prim_pad = ga.prim_chunks * kGateChunk;
-        ga.chunks = ga.prim_chunks + (s.n + kGateChunk - 1) / kGateChunk;
+        // flat: one pass over the tokens and the n columns
+        ga.idx = idx;
+        ga.G = G;
+        ga.k = ga.kk = s.k;
+        ga.ncols = s.n;
+        ga.chunks = chunks_of(s.n);
+        gate_pack<<<dim3(ga.chunks, 2, kblocks), 256, 0, st>>>(Wg, Wnp, s.d, C, 0, s.n, 0, 1,
+                                                             noisy, pack);
+        CUtensorMap mx;
+        if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
+            return cudaErrorInvalidValue;
+        const int tiles = static_cast<int>((s.T + kGateRows - 1) / kGateRows);
+        return launch_gate_tc_km<false>(resident, s.k, mx, pack, ga, tiles < sms ? tiles : sms, st);
     }
-    uint8_t *wpack = static_cast<uint8_t *>(pack);
-    gate_pack<<<dim3(ga.chunks, 2, s.d / 64), 256, 0, st>>>(Wg, noisy ? Wn : Wg, s.d, C, s.groups,
-                                                          ga.prim_pad, noisy, wpack);
-    const bool resident = s.d <= 512;
+
+    // hierarchical, pass 1: the groups (flat over the G group columns)
+    const int Gn = s.groups, kg = s.k_groups, ki = s.k / s.k_groups, m = s.n / s.groups;
+    const int64_t P = s.T * static_cast<int64_t>(kg);  // (token, rank) pairs
+    int32_t *gidx = ws_ptr<int32_t>(ws, L.gsel);
+    float *gw = reinterpret_cast<float *>(gidx + P);
+    const int pchunks = chunks_of(Gn), mchunks = chunks_of(m);
+    uint8_t *pack_i = pack + static_cast<size_t>(pchunks) * kblocks * 2 * kKBytes;
+    GateArgs gp = ga;
+    gp.idx = gidx;
+    gp.G = gw;
+    gp.k = gp.kk = kg;
+    gp.ncols = Gn;
+    gp.chunks = pchunks;
+    gate_pack<<<dim3(pchunks, 2, kblocks), 256, 0, st>>>(Wg, Wnp, s.d, C, 0, Gn, 0, 1, noisy, pack);
     CUtensorMap mx;
-    if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? s.d / 64 : 1))
+    if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
         return cudaErrorInvalidValue;
-    const int tiles = static_cast<int>((s.T + kGateRows - 1) / kGateRows);
-    const int grid = tiles < sm_count() ? tiles : sm_count();
-    const int km = s.groups ? (s.k_groups > s.k / s.k_groups ? s.k_groups : s.k / s.k_groups) : s.k;
-    if (resident)
-        return s.groups ? launch_gate_tc_km<true, true>(km, mx, wpack, ga, grid, st)
-                        : launch_gate_tc_km<true, false>(km, mx, wpack, ga, grid, st);
-    return s.groups ? launch_gate_tc_km<false, true>(km, mx, wpack, ga, grid, st)
-                    : launch_gate_tc_km<false, false>(km, mx, wpack, ga, grid, st);
+    const int ttiles = static_cast<int>((s.T + kGateRows - 1) / kGateRows);
+    cudaError_t e = launch_gate_tc_km<false>(resident, kg, mx, pack, gp, ttiles < sms ? ttiles : sms, st);
+    if (e != cudaSuccess) return e;
+
+    // pass 2: route the pairs by group, gather their x rows, score each group's columns
+    moe_shape sg = s;
+    sg.n = Gn;
+    sg.k = kg;
+    sg.groups = 0;
+    sg.k_groups = 0;
+    int32_t *counts_g = ws_ptr<int32_t>(ws, L.counts);
+    int32_t *offsets_g = ws_ptr<int32_t>(ws, L.offsets);
+    int32_t *perm_g = ws_ptr<int32_t>(ws, L.perm);
+    int32_t *inv_g = ws_ptr<int32_t>(ws, L.inv_perm);
+    int32_t *tiles_g = ws_ptr<int32_t>(ws, L.tiles);
+    __nv_bfloat16 *xg = ws_ptr<__nv_bfloat16>(ws, L.xperm);
+    e = launch_dispatch(sg, gidx, gw, counts_g, offsets_g, perm_g, inv_g,
+                        ws_ptr<float>(ws, L.importance), ws_ptr<float>(ws, L.cv2), ws, L, st);
+    if (e != cudaSuccess) return e;
+    e = launch_row_tiles(offsets_g, Gn, kGateRows, tiles_g, st);
+    if (e != cudaSuccess) return e;
+    e = launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), perm_g, offsets_g, Gn, P, s.d, kg,
+                           xg, err, st);
+    if (e != cudaSuccess) return e;
+    gate_pack<<<dim3(Gn * mchunks, 2, kblocks), 256, 0, st>>>(Wg, Wnp, s.d, C, Gn, s.n, m, mchunks,
+                                                            noisy, pack_i);
+    CUtensorMap mg;
+    if (!gate_map(&mg, xg, s.d, static_cast<uint64_t>(P), resident ? kblocks : 1))
+        return cudaErrorInvalidValue;
+    GateArgs gi = ga;
+    gi.idx = idx;
+    gi.G = G;
+    gi.k = s.k;
+    gi.kk = ki;
+    gi.ncols = m;
+    gi.chunks = mchunks;
+    gi.perm_g = perm_g;
+    gi.offsets_g = offsets_g;
+    gi.tiles_g = tiles_g;
+    gi.gw = gw;
+    gi.groups = Gn;
+    gi.kg = kg;
+    gi.m = m;
+    const int64_t max_tiles = (P + kGateRows - 1) / kGateRows + Gn;
+    const int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
+    return launch_gate_tc_km<true>(resident, ki, mg, pack_i, gi, grid, st);
 }
 
 }  // namespace moe

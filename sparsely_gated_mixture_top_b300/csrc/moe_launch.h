@@ -2,6 +2,7 @@
 // workspace layout and the launchers of each stage.  Not part of the public ABI.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -30,6 +31,8 @@ struct WsLayout {
     size_t header = 0;
     size_t scores = 0;      // gate scores H [T, C] fp32 (SIMT gate only)
     size_t gpack = 0;       // packed bf16 hi/lo gate matrices (tensor-core gate only)
+    size_t gsel = 0;        // [T*k_groups] int32 chosen groups, then [T*k_groups] fp32
+                            // their weights (hierarchical tensor-core gate only)
     size_t local_rank = 0;  // [S] int32, rank of a slot among same-expert slots of its chunk
     size_t chunk = 0;       // [chunks, n] int32, per-chunk expert counts, then bases
     size_t chunk_imp = 0;   // [chunks, n] double, per-chunk gate-weight sums
@@ -63,6 +66,7 @@ inline WsLayout ws_layout(const moe_shape &s) {
     const bool tc_gate = gate_tc_supported(s);
     L.scores = take(tc_gate ? 0 : static_cast<size_t>(s.T) * C * 4);
     L.gpack = take(tc_gate ? gate_tc_pack_bytes(s) : 0);
+    L.gsel = take(tc_gate && s.groups > 0 ? static_cast<size_t>(s.T) * s.k_groups * 8 : 0);
     L.local_rank = take(S * 4);
     L.chunk = take(chunks * n * 4);
     L.chunk_imp = take(chunks * n * 8);
@@ -90,9 +94,11 @@ inline T *ws_ptr(void *ws, size_t off) {
 cudaError_t launch_gate(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
                         const float *bg, const float *eps, int32_t *idx, float *G, void *ws,
                         const WsLayout &L, cudaStream_t st);
+// Tensor-core gate.  Hierarchical shapes also use the workspace's routing,
+// row-tile and gathered-row regions (free until the dispatch that follows).
 cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
-                           const float *bg, const float *eps, int32_t *idx, float *G, void *pack,
-                           int32_t *err, cudaStream_t st);
+                           const float *bg, const float *eps, int32_t *idx, float *G, void *ws,
+                           const WsLayout &L, cudaStream_t st);
 
 cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float *G,
                             int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
@@ -106,6 +112,15 @@ cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *
 
 cudaError_t launch_combine(const moe_shape &s, const void *Y_slot, const int32_t *inv_perm,
                            const float *G, void *y, int32_t *err, cudaStream_t st);
+
+// tiles[e] = sum over e' < e of ceil(rows of e' / bm) for offsets[0..n]; tiles[n] = total.
+cudaError_t launch_row_tiles(const int32_t *offsets, int n, int bm, int32_t *tiles,
+                             cudaStream_t st);
+
+// out[r] = x[perm[r] / k] (d bf16 values per row) for r < offsets[n].
+cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, const int32_t *offsets,
+                               int n, int64_t S, int d, int k, __nv_bfloat16 *out, int32_t *err,
+                               cudaStream_t st);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
