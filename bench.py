@@ -66,6 +66,37 @@ def peaks():
         return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
 
 
+def source_digest() -> str:
+    """sha256 of the CUDA library's sources (kernels, headers, the C ABI)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "sparsely_gated_mixture_top_b300", "csrc", "*.cu")) +
+                   glob.glob(os.path.join(ROOT, "sparsely_gated_mixture_top_b300", "csrc", "*.cuh")) +
+                   glob.glob(os.path.join(ROOT, "sparsely_gated_mixture_top_b300", "csrc", "*.h")) +
+                   glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def stage_traffic(w: wl.Workload):
+    """DRAM bytes (read + write) of one expert-FFN stage from the committed ncu
+    summary of this workload, or None if there is none or the kernels changed
+    since it was captured (its source digest no longer matches)."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != source_digest() or rec.get("workload") != w.name:
+        return None
+    return rec.get("ffn_stage_dram_bytes_per_launch")
+
+
 def algorithmic(w: wl.Workload, counts: np.ndarray) -> dict:
     """Algorithmic bytes and FLOPs of one forward pass, from the run's own counts."""
     eb = 2 if w.dtype == "bf16" else 4
@@ -339,22 +370,29 @@ def main():
         B.moe_combine(s, comp["Y"], comp["inv_perm"], comp["G"], out["y"], ws, stream)
     torch.cuda.synchronize(dev)
     ffn_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
-    ffn_bound_hbm = alg["ffn_bytes"] / (pk["hbm"] * 1e9) >= alg["flops"] / (pk["bf16"] * 1e12)
+    # A contraction timed inside a loop of more than a second runs under the
+    # power cap: its peak is the sustained one, else the burst one.
+    long_run = ms > 1000.0
+    tc_peak = pk["bf16_sustained"] if long_run else pk["bf16"]
+    tc_label = "sustained" if long_run else "burst"
+    ffn_bound_hbm = alg["ffn_bytes"] / (pk["hbm"] * 1e9) >= alg["flops"] / (tc_peak * 1e12)
     if ffn_bound_hbm:
         achieved = alg["ffn_bytes"] / (ffn_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s"}
+        roof["peak_source"] = pk["source"] + " copy bandwidth"
     else:
         achieved = alg["flops"] / (ffn_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s"}
+        roof["peak_source"] = f"{pk['source']} bf16 ({tc_label})"
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
-    roof["kernel"] = "expert FFN stage (moe_expert_ffn: gather + 2 grouped tcgen05 GEMMs)"
+    roof["traffic"] = stage_traffic(w)
+    roof["kernel"] = "expert FFN stage (moe_expert_ffn: tile table, gather, 2 grouped tcgen05 GEMMs)"
+    roof["algorithmic_per_launch"] = alg["ffn_bytes"] if ffn_bound_hbm else alg["flops"]
     roof["ms_per_launch"] = ffn_ms
-    roof["peak_source"] = pk["source"] + " (burst)"
 
-    t_roof = max(alg["layer_bytes"] / (pk["hbm"] * 1e9), alg["flops"] / (pk["bf16"] * 1e12))
+    t_roof = max(alg["layer_bytes"] / (pk["hbm"] * 1e9), alg["flops"] / (tc_peak * 1e12))
     layer_roof = {"bound": "hbm" if alg["layer_bytes"] / (pk["hbm"] * 1e9) >= alg["flops"] / (
-                      pk["bf16"] * 1e12) else "tensor",
+                      tc_peak * 1e12) else "tensor", "tensor_peak": f"{tc_label} {tc_peak} TFLOP/s",
                   "t_roof_us": t_roof * 1e6, "t_meas_us": ms_step * 1e3,
                   "frac": t_roof / (ms_step / 1e3), "algorithmic_bytes": alg["layer_bytes"],
                   "flops": alg["flops"], "experts_hit": alg["experts_hit"]}

@@ -135,54 +135,60 @@ __global__ void __launch_bounds__(1024) route_colscan(int32_t *__restrict__ chun
     }
 }
 
-__device__ double block_sum_1024(double v, double *sh) {
-    sh[threadIdx.x] = v;
+// Sum over the 256 threads of the block in a fixed order (warp shuffle tree,
+// then the 8 warp sums in warp order); every thread gets the result.
+__device__ double block_sum_256(double v, double *sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
     __syncthreads();
-    for (int o = 512; o > 0; o >>= 1) {
-        if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
-        __syncthreads();
-    }
-    const double r = sh[0];
+    double r = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) r += sh[w];
     __syncthreads();
     return r;
 }
 
-// One block of 1024 threads: offsets = exclusive scan of counts (offsets[n] =
+// One block of 256 threads: offsets = exclusive scan of counts (offsets[n] =
 // total), importance in fp32, and CV^2 = population variance / mean^2.
-__global__ void __launch_bounds__(1024) route_finish(const int32_t *__restrict__ counts,
-                                                     const double *__restrict__ imp64, int n,
-                                                     int32_t *__restrict__ offsets,
-                                                     float *__restrict__ importance,
-                                                     float *__restrict__ cv2) {
-    __shared__ int32_t part[1024];
-    __shared__ double sh[1024];
-    const int per = (n + 1023) / 1024;
+__global__ void __launch_bounds__(256) route_finish(const int32_t *__restrict__ counts,
+                                                    const double *__restrict__ imp64, int n,
+                                                    int32_t *__restrict__ offsets,
+                                                    float *__restrict__ importance,
+                                                    float *__restrict__ cv2) {
+    __shared__ int32_t wsum[8];
+    __shared__ double sh[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per = (n + 255) / 256;
     const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
     int32_t sum = 0;
     for (int i = i0; i < i1; ++i) sum += counts[i];
-    part[threadIdx.x] = sum;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
-        const int32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
+    // exclusive scan of the per-thread sums: warp shuffles, then the warps
+    int32_t inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
     }
-    int32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    int32_t base = 0;
+    for (int w = 0; w < warp; ++w) base += wsum[w];
+    int32_t run = base + inc - sum;
     for (int i = i0; i < i1; ++i) {
         offsets[i] = run;
         run += counts[i];
     }
-    if (threadIdx.x == 1023) offsets[n] = part[1023];
+    if (threadIdx.x == 255) offsets[n] = base + inc;
     double s = 0.0;
-    for (int e = threadIdx.x; e < n; e += 1024) {
+    for (int e = threadIdx.x; e < n; e += 256) {
         s += imp64[e];
         importance[e] = static_cast<float>(imp64[e]);
     }
-    const double mean = block_sum_1024(s, sh) / n;
+    const double mean = block_sum_256(s, sh) / n;
     double q = 0.0;
-    for (int e = threadIdx.x; e < n; e += 1024) q += (imp64[e] - mean) * (imp64[e] - mean);
-    const double var = block_sum_1024(q, sh) / n;
+    for (int e = threadIdx.x; e < n; e += 256) q += (imp64[e] - mean) * (imp64[e] - mean);
+    const double var = block_sum_256(q, sh) / n;
     if (threadIdx.x == 0) cv2[0] = mean != 0.0 ? static_cast<float>(var / (mean * mean)) : 0.0f;
 }
 
@@ -241,7 +247,7 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
     }
     route_rank<<<chunks, 1024, smem, st>>>(idx, G, S, n, local_rank, chunk, chunk_imp, err);
     route_colscan<<<(n + 31) / 32, dim3(32, 32), 0, st>>>(chunk, chunk_imp, chunks, n, counts, imp64);
-    route_finish<<<1, 1024, 0, st>>>(counts, imp64, n, offsets, importance, cv2);
+    route_finish<<<1, 256, 0, st>>>(counts, imp64, n, offsets, importance, cv2);
     route_scatter<<<static_cast<unsigned>((S + 255) / 256), 256, 0, st>>>(
         idx, S, n, offsets, chunk, local_rank, perm, inv_perm);
     return cudaGetLastError();
