@@ -97,6 +97,20 @@ def stage_traffic(w: wl.Workload):
     return rec.get("ffn_stage_dram_bytes_per_launch")
 
 
+def job_throughput(ms_local: float, tokens_per_rank: int, dist=None, device="cpu"):
+    """Whole-job throughput of a weak-scaling run: every rank processes
+    tokens_per_rank tokens; the job time is the slowest rank's time (MAX over
+    ranks).  Returns (job ms, tokens per second over all ranks)."""
+    ms = ms_local
+    world = 1
+    if dist is not None:
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        world = dist.get_world_size()
+    return ms, tokens_per_rank * world / (ms / 1e3)
+
+
 def algorithmic(w: wl.Workload, counts: np.ndarray) -> dict:
     """Algorithmic bytes and FLOPs of one forward pass, from the run's own counts."""
     eb = 2 if w.dtype == "bf16" else 4
@@ -335,13 +349,8 @@ def main():
     status = B.moe_check(ws, stream)
     if status != B.MOE_OK:
         raise RuntimeError(f"device error in the timed region: {B.status_string(status)}")
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, value = job_throughput(ms, w.T * args.steps, dist, dev)
     ms_step = ms / args.steps
-    tokens = w.T * args.steps * world
-    value = tokens / (ms / 1e3)
     counts = out["counts"].cpu().numpy()
     alg = algorithmic(w, counts)
     pk = peaks()
@@ -435,12 +444,8 @@ def main():
             e2e_step(i)
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = a.elapsed_time(b)
-        if dist:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": w.T * args.e2e_steps * world / (e_ms / 1e3), "unit": UNIT,
+        e_ms, e_value = job_throughput(a.elapsed_time(b), w.T * args.e2e_steps, dist, dev)
+        e2e = {"value": e_value, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps, "api": "moe_forward (pinned host x/eps in, y/G/idx/"
                                                 "importance/cv2/counts out)"}
