@@ -97,15 +97,27 @@ __global__ void __launch_bounds__(256) gate_pack(const float *__restrict__ Wg,
         tile[r][tx] = v;  // tile[d][col]
     }
     __syncthreads();
-    for (int cc = ty; cc < 64; cc += 4) {
-        const float v = tile[tx][cc];
-        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    // Output: 64 rows (one per column) x 8 groups of 8 d-values; each thread
+    // writes whole 16-byte groups of hi and of lo.
+    const int64_t unit = (static_cast<int64_t>(chunk) * (d / 64) + blockIdx.z) * 2 * kKBytes;
+    for (int o = threadIdx.x; o < 64 * 8; o += 256) {
+        const int cc = o >> 3, g = o & 7;
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float v0 = tile[g * 8 + 2 * e][cc], v1 = tile[g * 8 + 2 * e + 1][cc];
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
+            const __nv_bfloat16 l0 = __float2bfloat16_rn(v0 - __bfloat162float(h0));
+            const __nv_bfloat16 l1 = __float2bfloat16_rn(v1 - __bfloat162float(h1));
+            hi[e] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+            lo[e] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+        }
         const int rr = which * 64 + cc;
-        const int64_t unit = (static_cast<int64_t>(chunk) * (d / 64) + blockIdx.z) * 2 * kKBytes;
-        const int off = rr * 128 + (((tx >> 3) ^ (rr & 7)) << 4) + (tx & 7) * 2;
-        *reinterpret_cast<__nv_bfloat16 *>(pack + unit + off) = hi;
-        *reinterpret_cast<__nv_bfloat16 *>(pack + unit + kKBytes + off) = lo;
+        const int off = rr * 128 + ((g ^ (rr & 7)) << 4);
+        *reinterpret_cast<uint4 *>(pack + unit + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(pack + unit + kKBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
 }
 
