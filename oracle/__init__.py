@@ -50,6 +50,8 @@ def _lib_():
         lib.oracle_experts_combine.restype = i32
         lib.oracle_forward.argtypes = [i64, i32, i32, i32, i32, i32, i32] + [vp] * 18
         lib.oracle_forward.restype = i32
+        lib.oracle_load.argtypes = [i64, i32, i32, i32] + [vp] * 8
+        lib.oracle_load.restype = i32
         lib.oracle_combine_rows.argtypes = [i64, i32, i32, i64] + [vp] * 4
         lib.oracle_combine_rows.restype = i32
         _lib = lib
@@ -98,6 +100,23 @@ def gate_flat(x, Wg, Wn, bg, eps, k: int):
     if rc:
         raise ValueError("oracle_gate_flat: bad arguments")
     return idx, G, H, margin
+
+
+def load(x, Wg, Wn, bg, eps, k: int):
+    """Load estimate of the flat noisy gate: P [T,n] (probability that expert i
+    stays in the top k when its own noise is redrawn), load [n] = sum over
+    tokens, and the CV^2 of load."""
+    x, Wg, Wn, bg, eps = map(_f64, (x, Wg, Wn, bg, eps))
+    T, d = x.shape
+    n = Wg.shape[1]
+    P = np.zeros((T, n))
+    ld = np.zeros(n)
+    cv2 = np.zeros(1)
+    rc = _lib_().oracle_load(T, d, n, k, _p(x), _p(Wg), _p(Wn), _p(bg), _p(eps), _p(P), _p(ld),
+                             _p(cv2))
+    if rc:
+        raise ValueError("oracle_load: bad arguments")
+    return P, ld, float(cv2[0])
 
 
 def gate_hier(x, Wg, Wn, bg, eps, groups: int, k_groups: int, k: int):

@@ -45,6 +45,10 @@
  *     the hierarchical weight product and the CV^2 convention beyond the
  *     invariants the tests check: the pages print no value for either.
  *   - the expert has biases b1, b2; ReLU after the first layer only.
+ *   - load estimate: the paper's smooth load (probability of staying in the
+ *     top k under a redraw of the expert's own noise), summed over tokens;
+ *     flat gating with noise only.  PARITY PINNED by a Monte Carlo redraw of
+ *     one expert's noise, the k = n case and the vanishing-noise limit.
  *
  * Weight layouts (row-major):
  *   Wg, Wnoise : [d, C] where C = n (flat) or G + n (hierarchical: the first G
@@ -185,6 +189,87 @@ int oracle_gate_flat(int64_t T, int d, int n, int k, const double *x, const doub
         free(w);
     }
     return bad ? -1 : 0;
+}
+
+/*
+ * Load estimate of the flat noisy gate.  [Outrageously Large Neural Networks
+ * - 中文验证版] section 方法适配 and the wudongming97 note name a load loss
+ * beside the importance loss: it balances how many samples each expert
+ * receives.  A count is not smooth, so the load is estimated from the noise
+ * (the pages are cut off before the formula; this follows the paper's
+ * load-balancing appendix): for token t and expert i,
+ *   P(t, i) = probability that expert i is among the k best when only its own
+ *             noise is redrawn and the other experts' noisy scores stay fixed
+ *           = Phi((c_i - kth_excluding(H, k, i)) / softplus(r_i)),
+ * with c_i = (x.W_g)_i (+ bg_i), r_i = (x.W_noise)_i, H as in the gate, and
+ * kth_excluding(H, k, i) the k-th largest H_j over j != i (-inf when fewer
+ * than k others exist; ties ordered as in KeepTopK).  Phi(z) = erfc(-z/sqrt2)/2.
+ *   load[i] = sum_t P(t, i);  cv2 = population variance of load / mean^2.
+ * P[T,n] is written (caller-owned); the sums over t run in token order.
+ */
+int oracle_load(int64_t T, int d, int n, int k, const double *x, const double *Wg,
+                const double *Wn, const double *bg, const double *eps, double *P, double *load,
+                double *cv2) {
+    if (T < 0 || d <= 0 || n <= 0 || k <= 0 || k > n || !Wn || !eps) return -1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *c = (double *)malloc(sizeof(double) * (size_t)n);
+        double *sp = (double *)malloc(sizeof(double) * (size_t)n);
+        scored *order = (scored *)malloc(sizeof(scored) * (size_t)n);
+        char *in_top = (char *)malloc((size_t)n);
+        if (!c || !sp || !order || !in_top) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 8)
+            for (int64_t t = 0; t < T; ++t) {
+                const double *xt = x + t * d;
+                for (int i = 0; i < n; ++i) {
+                    double ci = 0.0, ri = 0.0;
+                    for (int j = 0; j < d; ++j) {
+                        ci += xt[j] * Wg[(int64_t)j * n + i];
+                        ri += xt[j] * Wn[(int64_t)j * n + i];
+                    }
+                    if (bg) ci += bg[i];
+                    c[i] = ci;
+                    sp[i] = oracle_softplus(ri);
+                    order[i].h = ci + eps[t * (int64_t)n + i] * sp[i];
+                    order[i].i = i;
+                }
+                qsort(order, (size_t)n, sizeof(scored), by_desc_h_then_index);
+                memset(in_top, 0, (size_t)n);
+                for (int q = 0; q < k; ++q) in_top[order[q].i] = 1;
+                /* k-th largest of the others: for a member the (k+1)-th overall,
+                 * for a non-member the k-th overall */
+                const double kth = order[k - 1].h;
+                const double next = (k < n) ? order[k].h : -INFINITY;
+                for (int i = 0; i < n; ++i) {
+                    const double thr = in_top[i] ? next : kth;
+                    P[t * (int64_t)n + i] =
+                        (thr == -INFINITY) ? 1.0 : 0.5 * erfc(-(c[i] - thr) / (sp[i] * sqrt(2.0)));
+                }
+            }
+        }
+        free(c);
+        free(sp);
+        free(order);
+        free(in_top);
+    }
+    if (bad) return -1;
+    double sum = 0.0;
+    for (int i = 0; i < n; ++i) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < T; ++t) acc += P[t * (int64_t)n + i];
+        load[i] = acc;
+        sum += acc;
+    }
+    const double mean = sum / n;
+    double var = 0.0;
+    for (int i = 0; i < n; ++i) var += (load[i] - mean) * (load[i] - mean);
+    var /= n;
+    *cv2 = mean != 0.0 ? var / (mean * mean) : 0.0;
+    return 0;
 }
 
 /*
