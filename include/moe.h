@@ -211,6 +211,29 @@ MOE_API moe_status moe_forward(const moe_shape *shape, const void *x, const floa
                        size_t ws_bytes, void *stream);
 
 /*
+ * Load estimate of the noisy gate, the smooth per-expert load that the load
+ * loss balances ("Outrageously Large Neural Networks - 中文验证版", section
+ * 方法适配: an importance loss and a load loss keep the samples spread over
+ * the experts; the pages stop before its formula, which is taken from the
+ * paper's load-balancing appendix).  For token t and expert i,
+ *   P(t, i) = Phi((c_i - thr_i) / softplus(r_i)),  c = x.W_g (+ bg), r = x.W_noise,
+ * thr_i = the k-th largest noisy score H of the other experts: the
+ * probability that i stays among the k kept when only its own noise is
+ * redrawn.  load[i] = sum over tokens of P(t, i) (fp64 sums in token order,
+ * rounded to fp32), load_cv2 = population variance(load) / mean^2.
+ * The call runs the gate too (idx, G as moe_gate).  Flat, noisy (eps and Wn
+ * required), bf16 shapes with k <= 15 only (MOE_ERR_UNSUPPORTED otherwise).
+ * lws: a second, caller-owned, 256-byte aligned workspace of
+ * moe_load_workspace_bytes(shape) bytes (8*T*n + 8*T + 8*n*ceil(T/256) + 8*n
+ * bytes, each region rounded up to 256); `ws` is the ordinary workspace.
+ */
+MOE_API size_t moe_load_workspace_bytes(const moe_shape *shape);
+MOE_API moe_status moe_gate_load(const moe_shape *shape, const void *x, const float *Wg,
+                                 const float *Wn, const float *bg, const float *eps, int32_t *idx,
+                                 float *G, float *load, float *load_cv2, void *ws,
+                                 size_t ws_bytes, void *lws, size_t lws_bytes, void *stream);
+
+/*
  * Synchronises `stream`, reads the workspace's device error word, clears it
  * and returns it (MOE_OK when no device error was recorded).  Returns
  * MOE_ERR_CUDA if the stream itself failed.

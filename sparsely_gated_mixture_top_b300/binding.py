@@ -29,7 +29,8 @@ MOE_BF16 = 1
 
 EXPORTS = ("moe_version", "moe_status_string", "moe_validate", "moe_workspace_bytes",
            "moe_workspace_init", "moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine",
-           "moe_forward", "moe_check", "moe_dispatch_noalloc")
+           "moe_forward", "moe_check", "moe_dispatch_noalloc", "moe_load_workspace_bytes",
+           "moe_gate_load")
 
 
 class MoEShape(ctypes.Structure):
@@ -62,8 +63,10 @@ def _load():
     lib.moe_forward.argtypes = [shp] + [vp] * 16 + [sz, vp]
     lib.moe_check.argtypes = [vp, vp]
     lib.moe_dispatch_noalloc.argtypes = [shp] + [vp] * 9
+    lib.moe_load_workspace_bytes.argtypes, lib.moe_load_workspace_bytes.restype = [shp], sz
+    lib.moe_gate_load.argtypes = [shp] + [vp] * 10 + [sz, vp, sz, vp]
     for f in ("moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
-              "moe_check", "moe_dispatch_noalloc"):
+              "moe_check", "moe_dispatch_noalloc", "moe_gate_load"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -140,6 +143,17 @@ def moe_dispatch_noalloc(shape, idx, G, counts, offsets, perm, inv_perm, importa
     _ok("moe_dispatch_noalloc", lib.moe_dispatch_noalloc(
         ctypes.byref(shape), _p(idx), _p(G), _p(counts), _p(offsets), _p(perm), _p(inv_perm),
         _p(importance), _p(cv2), _stream(stream)))
+
+
+def load_workspace_bytes(shape: MoEShape) -> int:
+    return lib.moe_load_workspace_bytes(ctypes.byref(shape))
+
+
+def moe_gate_load(shape, x, Wg, Wn, bg, eps, idx, G, load, load_cv2, ws, lws, stream=None):
+    """Gate plus the load estimate of the noisy gate (flat, noisy, bf16)."""
+    _ok("moe_gate_load", lib.moe_gate_load(
+        ctypes.byref(shape), _p(x), _p(Wg), _p(Wn), _p(bg), _p(eps), _p(idx), _p(G), _p(load),
+        _p(load_cv2), _p(ws), ws.numel(), _p(lws), lws.numel(), _stream(stream)))
 
 
 def moe_expert_ffn(shape, x, perm, offsets, W1, b1, W2, b2, Y_slot, ws, stream=None):

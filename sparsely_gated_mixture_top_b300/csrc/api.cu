@@ -184,6 +184,40 @@ moe_status moe_forward(const moe_shape *s, const void *x, const float *Wg, const
     return cuda_status(e);
 }
 
+static bool load_supported(const moe_shape *s) {
+    return s->groups == 0 && s->noisy == 1 && s->dtype == MOE_BF16 && s->k < MOE_MAX_K;
+}
+
+size_t moe_load_workspace_bytes(const moe_shape *s) {
+    if (moe_validate(s) != MOE_OK || !load_supported(s)) return 0;
+    return load_layout(*s).total;
+}
+
+moe_status moe_gate_load(const moe_shape *s, const void *x, const float *Wg, const float *Wn,
+                         const float *bg, const float *eps, int32_t *idx, float *G, float *load,
+                         float *load_cv2, void *ws, size_t ws_bytes, void *lws, size_t lws_bytes,
+                         void *stream) {
+    moe_status v = moe_validate(s);
+    if (v != MOE_OK) return v;
+    if (!load_supported(s)) return MOE_ERR_UNSUPPORTED;
+    if (!ok_ptr(Wg) || !ok_ptr(Wn) || !ok_opt(bg) || !ok_ptr(load) || !ok_ptr(load_cv2))
+        return MOE_ERR_INVALID_ARG;
+    if (s->T > 0 && (!ok_ptr(x) || !ok_ptr(eps) || !ok_ptr(idx) || !ok_ptr(G)))
+        return MOE_ERR_INVALID_ARG;
+    if ((v = check_ws(s, ws, ws_bytes)) != MOE_OK) return v;
+    const LoadLayout LL = load_layout(*s);
+    if (lws == nullptr || (reinterpret_cast<uintptr_t>(lws) & 255u) != 0 || lws_bytes < LL.total)
+        return MOE_ERR_WORKSPACE;
+    const WsLayout L = ws_layout(*s);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (s->T > 0)
+        e = launch_gate_tc_load(*s, x, Wg, Wn, bg, eps, idx, G, ws_ptr<float>(lws, LL.c),
+                                ws_ptr<float>(lws, LL.s), ws_ptr<float>(lws, LL.vk), ws, L, st);
+    if (e == cudaSuccess) e = launch_load(*s, idx, lws, LL, load, load_cv2, st);
+    return cuda_status(e);
+}
+
 moe_status moe_check(void *ws, void *stream) {
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

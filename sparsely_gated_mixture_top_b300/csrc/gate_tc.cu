@@ -212,6 +212,7 @@ struct GateArgs {
     int d;
     int k;             // outputs per token
     int kk;            // list length used: flat k; grouped k_inner
+    int kf;            // list depth kept exact: kk, or kk + 1 in load mode
     int ncols;         // score columns of one row's list (flat: C; grouped: m)
     int chunks;        // chunks per tile
     int ldE;           // eps row stride (floats)
@@ -223,6 +224,11 @@ struct GateArgs {
     const int32_t *tiles_g;    // [G+1] row-tile starts
     const float *gw;           // [T*kg] group weights
     int groups, kg, m;
+    // load mode (flat only): every column's clean score and noise scale, and
+    // each token's k-th and (k+1)-th noisy score
+    float *c_out;   // [T, ncols] or NULL
+    float *s_out;   // [T, ncols]
+    float *vk_out;  // [T, 2]
 };
 
 // Named barrier of the eight epilogue warps.
@@ -520,7 +526,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                 ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the votes below need every lane
                 if (ok) {
                     tc_fence_after();
-                    const float thr = list.kth(a.kk);  // fixed for the span
+                    const float thr = list.kth(a.kf);  // fixed for the span
 #pragma unroll
                     for (int piece = 0; piece < 2; ++piece) {
                         uint32_t cv[16], nv[16];
@@ -538,6 +544,18 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                         // so an equal score never displaces an entry: '>' is exact.
                         // Rows past the tile flag nothing but still take part in the
                         // votes.
+                        if (a.c_out && valid) {  // load mode: clean score, noise scale
+                            float *crow = a.c_out + t * a.ncols + col0 + piece * 16;
+                            float *srow = a.s_out + t * a.ncols + col0 + piece * 16;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int sc = col0 + piece * 16 + j;
+                                if (sc < a.ncols) {
+                                    crow[j] = __uint_as_float(cv[j]) + (bg_row ? __ldg(bg_row + sc) : 0.0f);
+                                    srow[j] = softplus_fast(__uint_as_float(nv[j]));
+                                }
+                            }
+                        }
                         uint32_t pass = 0;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -581,6 +599,10 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                     list.insert(xch_v[q * kGateRows + r], xch_i[q * kGateRows + r]);
                 float w[KM];
                 softmax_top<KM>(list, a.kk, w);
+                if (a.vk_out) {  // the k-th and (k+1)-th noisy score (-inf past the list)
+                    a.vk_out[2 * t] = list.kth(a.kk);
+                    a.vk_out[2 * t + 1] = a.kk < a.ncols ? list.kth(a.kk + 1) : -INFINITY;
+                }
                 const int id_off = kGrouped ? ti.g * a.m : 0;
 #pragma unroll
                 for (int q = 0; q < KM; ++q)
@@ -677,6 +699,40 @@ size_t gate_tc_pack_bytes(const moe_shape &s) {
 
 bool gate_tc_supported(const moe_shape &s) { return s.dtype == MOE_BF16; }
 
+cudaError_t launch_gate_tc_load(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
+                                const float *bg, const float *eps, int32_t *idx, float *G,
+                                float *c_out, float *s_out, float *vk_out, void *ws,
+                                const WsLayout &L, cudaStream_t st) {
+    // flat, noisy, k + 1 <= 16 (the list keeps the (k+1)-th score too)
+    const bool resident = s.d <= 512;
+    const int kblocks = s.d / 64;
+    uint8_t *pack = ws_ptr<uint8_t>(ws, L.gpack);
+    GateArgs ga{};
+    ga.bg = bg;
+    ga.eps = eps;
+    ga.T = s.T;
+    ga.d = s.d;
+    ga.ldE = s.n;
+    ga.noisy = 1;
+    ga.err = ws_ptr<int32_t>(ws, 0);
+    ga.idx = idx;
+    ga.G = G;
+    ga.k = ga.kk = s.k;
+    ga.kf = s.k + 1;  // the (k+1)-th score must be exact too
+    ga.ncols = s.n;
+    ga.chunks = chunks_of(s.n);
+    ga.c_out = c_out;
+    ga.s_out = s_out;
+    ga.vk_out = vk_out;
+    gate_pack<<<dim3(ga.chunks, 2, kblocks), 256, 0, st>>>(Wg, Wn, s.d, s.n, 0, s.n, 0, 1, 1, pack);
+    CUtensorMap mx;
+    if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
+        return cudaErrorInvalidValue;
+    const int tiles = static_cast<int>((s.T + kGateRows - 1) / kGateRows);
+    const int sms = sm_count();
+    return launch_gate_tc_km<false>(resident, s.k + 1, mx, pack, ga, tiles < sms ? tiles : sms, st);
+}
+
 cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
                            const float *bg, const float *eps, int32_t *idx, float *G, void *ws,
                            const WsLayout &L, cudaStream_t st) {
@@ -700,7 +756,7 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
         // flat: one pass over the tokens and the n columns
         ga.idx = idx;
         ga.G = G;
-        ga.k = ga.kk = s.k;
+        ga.k = ga.kk = ga.kf = s.k;
         ga.ncols = s.n;
         ga.chunks = chunks_of(s.n);
         gate_pack<<<dim3(ga.chunks, 2, kblocks), 256, 0, st>>>(Wg, Wnp, s.d, C, 0, s.n, 0, 1,
@@ -722,7 +778,7 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
     GateArgs gp = ga;
     gp.idx = gidx;
     gp.G = gw;
-    gp.k = gp.kk = kg;
+    gp.k = gp.kk = gp.kf = kg;
     gp.ncols = Gn;
     gp.chunks = pchunks;
     gate_pack<<<dim3(pchunks, 2, kblocks), 256, 0, st>>>(Wg, Wnp, s.d, C, 0, Gn, 0, 1, noisy, pack);
@@ -762,7 +818,7 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
     gi.idx = idx;
     gi.G = G;
     gi.k = s.k;
-    gi.kk = ki;
+    gi.kk = gi.kf = ki;
     gi.ncols = m;
     gi.chunks = mchunks;
     gi.perm_g = perm_g;

@@ -122,6 +122,24 @@ cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, cons
                                int n, int64_t S, int d, int k, __nv_bfloat16 *out, int32_t *err,
                                cudaStream_t st);
 
+// Load estimate (load.cu): its own workspace, [T,n] clean scores and noise
+// scales, [T,2] k-th / (k+1)-th noisy scores, per-chunk partial sums.
+struct LoadLayout {
+    size_t c = 0, s = 0, vk = 0, part = 0, load64 = 0, total = 0;
+    int chunks = 0;
+};
+LoadLayout load_layout(const moe_shape &s);
+
+// Tensor-core gate that also writes c, s and the k-th / (k+1)-th scores
+// (flat, noisy, bf16, k <= 15).
+cudaError_t launch_gate_tc_load(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
+                                const float *bg, const float *eps, int32_t *idx, float *G,
+                                float *c_out, float *s_out, float *vk_out, void *ws,
+                                const WsLayout &L, cudaStream_t st);
+
+cudaError_t launch_load(const moe_shape &s, const int32_t *idx, void *lws, const LoadLayout &L,
+                        float *load, float *cv2, cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
