@@ -224,7 +224,7 @@ MOE_API moe_status moe_forward(const moe_shape *shape, const void *x, const floa
  * The call runs the gate too (idx, G as moe_gate).  Flat, noisy (eps and Wn
  * required), bf16 shapes with k <= 15 only (MOE_ERR_UNSUPPORTED otherwise).
  * lws: a second, caller-owned, 256-byte aligned workspace of
- * moe_load_workspace_bytes(shape) bytes (8*T*n + 8*T + 8*n*ceil(T/256) + 8*n
+ * moe_load_workspace_bytes(shape) bytes (8*T*n + 8*T + 8*n*ceil(T/64) + 8*n
  * bytes, each region rounded up to 256); `ws` is the ordinary workspace.
  */
 MOE_API size_t moe_load_workspace_bytes(const moe_shape *shape);

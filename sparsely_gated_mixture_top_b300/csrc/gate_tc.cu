@@ -545,14 +545,31 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                         // Rows past the tile flag nothing but still take part in the
                         // votes.
                         if (a.c_out && valid) {  // load mode: clean score, noise scale
-                            float *crow = a.c_out + t * a.ncols + col0 + piece * 16;
-                            float *srow = a.s_out + t * a.ncols + col0 + piece * 16;
+                            const int cb = col0 + piece * 16;
+                            float *crow = a.c_out + t * a.ncols + cb;
+                            float *srow = a.s_out + t * a.ncols + cb;
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int sc = col0 + piece * 16 + j;
-                                if (sc < a.ncols) {
-                                    crow[j] = __uint_as_float(cv[j]) + (bg_row ? __ldg(bg_row + sc) : 0.0f);
-                                    srow[j] = softplus_fast(__uint_as_float(nv[j]));
+                            for (int q = 0; q < 4; ++q) {  // four columns at a time
+                                float cc[4], ss[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int j = 4 * q + e;
+                                    cc[e] = __uint_as_float(cv[j]) +
+                                            (bg_row && cb + j < a.ncols ? __ldg(bg_row + cb + j) : 0.0f);
+                                    ss[e] = softplus_fast(__uint_as_float(nv[j]));
+                                }
+                                if ((a.ncols & 3) == 0) {  // 16-byte rows: float4 stores
+                                    if (cb + 4 * q < a.ncols) {
+                                        reinterpret_cast<float4 *>(crow)[q] = make_float4(cc[0], cc[1], cc[2], cc[3]);
+                                        reinterpret_cast<float4 *>(srow)[q] = make_float4(ss[0], ss[1], ss[2], ss[3]);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        if (cb + 4 * q + e < a.ncols) {
+                                            crow[4 * q + e] = cc[e];
+                                            srow[4 * q + e] = ss[e];
+                                        }
                                 }
                             }
                         }

@@ -12,9 +12,9 @@
 // load[i] = sum_t P(t, i) and CV^2 = population variance / mean^2 of load.
 // The tensor-core gate (load mode) writes c, s and H_(k), H_(k+1); here
 //   load_accumulate  one thread per expert column, the tokens of one
-//                    256-token chunk in order: P in fp32 (erfcf), sums in fp64
-//   load_finish      one block: per expert the chunk sums in chunk order,
-//                    then CV^2
+//                    64-token chunk in order: P in fp32 (erfcf), sums in fp64
+//   load_colsum      one thread per expert: the chunk sums in chunk order
+//   load_cv2         one block: CV^2 of the load vector
 // so the same inputs always give the same bits.
 #include "moe_device.cuh"
 #include "moe_launch.h"
@@ -23,7 +23,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kLoadChunk = 256;  // tokens per partial sum
+constexpr int kLoadChunk = 64;  // tokens per partial sum
 
 __global__ void __launch_bounds__(256) load_accumulate(const float *__restrict__ c,
                                                        const float *__restrict__ s,
@@ -67,19 +67,24 @@ __device__ double block_sum_256(double v, double *sh) {
     return r;
 }
 
-__global__ void __launch_bounds__(256) load_finish(const double *__restrict__ part, int chunks,
+// One thread per expert: the chunk partials in chunk order.
+__global__ void __launch_bounds__(256) load_colsum(const double *__restrict__ part, int chunks,
                                                    int n, double *__restrict__ load64,
-                                                   float *__restrict__ load,
-                                                   float *__restrict__ cv2) {
+                                                   float *__restrict__ load) {
+    const int e = blockIdx.x * 256 + threadIdx.x;
+    if (e >= n) return;
+    double acc = 0.0;
+    for (int ch = 0; ch < chunks; ++ch) acc += part[static_cast<int64_t>(ch) * n + e];
+    load64[e] = acc;
+    load[e] = static_cast<float>(acc);
+}
+
+// One block: CV^2 = population variance / mean^2 of the load vector.
+__global__ void __launch_bounds__(256) load_cv2(const double *__restrict__ load64, int n,
+                                                float *__restrict__ cv2) {
     __shared__ double sh[8];
     double s = 0.0;
-    for (int e = threadIdx.x; e < n; e += 256) {
-        double acc = 0.0;
-        for (int ch = 0; ch < chunks; ++ch) acc += part[static_cast<int64_t>(ch) * n + e];
-        load64[e] = acc;
-        load[e] = static_cast<float>(acc);
-        s += acc;
-    }
+    for (int e = threadIdx.x; e < n; e += 256) s += load64[e];
     const double mean = block_sum_256(s, sh) / n;
     double q = 0.0;
     for (int e = threadIdx.x; e < n; e += 256) q += (load64[e] - mean) * (load64[e] - mean);
@@ -122,7 +127,9 @@ cudaError_t launch_load(const moe_shape &s, const int32_t *idx, void *lws, const
     double *part = ws_ptr<double>(lws, L.part);
     load_accumulate<<<dim3((s.n + 255) / 256, L.chunks), 256, 0, st>>>(c, sp, vk, idx, s.T, s.n, s.k,
                                                                       part);
-    load_finish<<<1, 256, 0, st>>>(part, L.chunks, s.n, ws_ptr<double>(lws, L.load64), load, cv2);
+    double *load64 = ws_ptr<double>(lws, L.load64);
+    load_colsum<<<(s.n + 255) / 256, 256, 0, st>>>(part, L.chunks, s.n, load64, load);
+    load_cv2<<<1, 256, 0, st>>>(load64, s.n, cv2);
     return cudaGetLastError();
 }
 
