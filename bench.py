@@ -407,48 +407,73 @@ def main():
                   "flops": alg["flops"], "experts_hit": alg["experts_hit"]}
 
     # ---- end to end: host buffers in, results out, through moe_forward ------
+    # ---- end to end: host buffers in, results out, through moe_forward ------
+    # Every step copies its x and eps in from pinned host memory and its y, G,
+    # idx, importance, cv2 and counts back.  As a serving loop would, the
+    # copies of neighbouring steps overlap the forward pass: inputs go in on
+    # one stream, the layer runs on another, results come back on a third,
+    # with device buffers double-buffered and ordered by events.
     e2e = None
     if rank == 0 or world > 1:
-        pin_x = [st[0].cpu().pin_memory() for st in sets[:2]]
-        pin_e = [st[1].cpu().pin_memory() if st[1] is not None else None for st in sets[:2]]
-        hy = torch.empty(out["y"].shape, dtype=out["y"].dtype, pin_memory=True)
-        hG = torch.empty(out["G"].shape, dtype=torch.float32, pin_memory=True)
-        hi = torch.empty(out["idx"].shape, dtype=torch.int32, pin_memory=True)
-        him = torch.empty(w.n, dtype=torch.float32, pin_memory=True)
-        hc = torch.empty(w.n, dtype=torch.int32, pin_memory=True)
-        hcv = torch.empty(1, dtype=torch.float32, pin_memory=True)
-        dx, de = torch.empty_like(dinp["x"]), (torch.empty_like(dinp["eps"]) if dinp["eps"] is not None else None)
-        h2d = pin_x[0].numel() * pin_x[0].element_size() + (pin_e[0].numel() * 4 if pin_e[0] is not None else 0)
-        d2h = sum(t.numel() * t.element_size() for t in (hy, hG, hi, him, hc, hcv))
+        nb = 2
+        pin_x = [st[0].cpu().pin_memory() for st in sets[:nb]]
+        pin_e = [st[1].cpu().pin_memory() if st[1] is not None else None for st in sets[:nb]]
+        dxs = [torch.empty_like(dinp["x"]) for _ in range(nb)]
+        des = [torch.empty_like(dinp["eps"]) if dinp["eps"] is not None else None for _ in range(nb)]
+        douts = [B.outputs(s, dev) for _ in range(nb)]
+        keys = ("y", "G", "idx", "importance", "cv2", "counts")
+        houts = [{k: torch.empty(douts[0][k].shape, dtype=douts[0][k].dtype, pin_memory=True)
+                  for k in keys} for _ in range(nb)]
+        h2d = pin_x[0].numel() * pin_x[0].element_size() + (
+            pin_e[0].numel() * 4 if pin_e[0] is not None else 0)
+        d2h = sum(t.numel() * t.element_size() for t in houts[0].values())
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(nb)]
+        ev_done = [torch.cuda.Event() for _ in range(nb)]
+        ev_out = [torch.cuda.Event() for _ in range(nb)]
+        for b in range(nb):  # all buffers start free
+            ev_done[b].record(stream)
+            ev_out[b].record(stream)
 
         def e2e_step(i):
-            dx.copy_(pin_x[i % 2], non_blocking=True)
-            if de is not None:
-                de.copy_(pin_e[i % 2], non_blocking=True)
-            B.moe_forward(s, dx, dinp["Wg"], dinp["Wn"], dinp["bg"], de, dinp["W1"], dinp["b1"],
-                          dinp["W2"], dinp["b2"], out["y"], out["G"], out["idx"],
-                          out["importance"], out["cv2"], out["counts"], ws, stream)
-            hy.copy_(out["y"], non_blocking=True)
-            hG.copy_(out["G"], non_blocking=True)
-            hi.copy_(out["idx"], non_blocking=True)
-            him.copy_(out["importance"], non_blocking=True)
-            hc.copy_(out["counts"], non_blocking=True)
-            hcv.copy_(out["cv2"], non_blocking=True)
+            b = i % nb
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_done[b])      # step i-2 finished reading these inputs
+                dxs[b].copy_(pin_x[i % nb], non_blocking=True)
+                if des[b] is not None:
+                    des[b].copy_(pin_e[i % nb], non_blocking=True)
+                ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])         # step i-2's results are out of these buffers
+            o = douts[b]
+            B.moe_forward(s, dxs[b], dinp["Wg"], dinp["Wn"], dinp["bg"], des[b], dinp["W1"],
+                          dinp["b1"], dinp["W2"], dinp["b2"], o["y"], o["G"], o["idx"],
+                          o["importance"], o["cv2"], o["counts"], ws, stream)
+            ev_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[b])
+                for k in keys:
+                    houts[b][k].copy_(o[k], non_blocking=True)
+                ev_out[b].record(s_out)
 
         for i in range(3):
             e2e_step(i)
         torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_in)
         for i in range(args.e2e_steps):
             e2e_step(i)
-        b.record(stream)
+        b_.record(s_out)
         torch.cuda.synchronize(dev)
-        e_ms, e_value = job_throughput(a.elapsed_time(b), w.T * args.e2e_steps, dist, dev)
+        status = B.moe_check(ws, stream)
+        if status != B.MOE_OK:
+            raise RuntimeError(f"device error in the end-to-end loop: {B.status_string(status)}")
+        e_ms, e_value = job_throughput(a.elapsed_time(b_), w.T * args.e2e_steps, dist, dev)
         e2e = {"value": e_value, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "steps": args.e2e_steps, "api": "moe_forward (pinned host x/eps in, y/G/idx/"
-                                                "importance/cv2/counts out)"}
+               "steps": args.e2e_steps,
+               "api": "moe_forward (pinned host x/eps in, y/G/idx/importance/cv2/counts out; "
+                      "copies of neighbouring steps overlap the forward pass on separate streams)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -44,22 +44,44 @@ __global__ void __launch_bounds__(1024) ffn_tiles(const int32_t *__restrict__ of
     if (threadIdx.x == 1023) tiles[n] = part[1023];
 }
 
-// One warp per row, 16-byte copies.
-__global__ void ffn_gather(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm,
-                           const int32_t *__restrict__ offsets, int n, int64_t S, int d, int k,
-                           __nv_bfloat16 *__restrict__ xperm, int32_t *err) {
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
-    if (r >= S || r >= offsets[n]) return;
+// Four rows per warp, 16-byte copies: the four rows' indices, then each
+// 16-byte column of the four rows loaded before any is stored.
+constexpr int kGatherRows = 4;
+
+__global__ void __launch_bounds__(256) ffn_gather(const __nv_bfloat16 *__restrict__ x,
+                                                  const int32_t *__restrict__ perm,
+                                                  const int32_t *__restrict__ offsets, int n,
+                                                  int64_t S, int d, int k,
+                                                  __nv_bfloat16 *__restrict__ xperm, int32_t *err) {
     const int lane = threadIdx.x & 31;
-    const int32_t s = perm[r];
-    uint4 *dst = reinterpret_cast<uint4 *>(xperm + r * d);
-    if (s < 0 || s >= S) {
-        if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteFfnPerm, static_cast<int32_t>(r));
-        for (int c = lane; c < d / 8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
-        return;
+    const int64_t r0 = (static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32) * kGatherRows;
+    const int64_t rows = S < offsets[n] ? S : offsets[n];
+    if (r0 >= rows) return;
+    const uint4 *src[kGatherRows];
+    uint4 *dst[kGatherRows];
+#pragma unroll
+    for (int i = 0; i < kGatherRows; ++i) {
+        const int64_t r = r0 + i;
+        src[i] = nullptr;
+        dst[i] = nullptr;
+        if (r < rows) {
+            dst[i] = reinterpret_cast<uint4 *>(xperm + r * d);
+            const int32_t s = perm[r];
+            if (s < 0 || s >= S) {
+                if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteFfnPerm, static_cast<int32_t>(r));
+            } else {
+                src[i] = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(s / k) * d);
+            }
+        }
     }
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(s / k) * d);
-    for (int c = lane; c < d / 8; c += 32) dst[c] = src[c];
+    for (int c = lane; c < d / 8; c += 32) {
+        uint4 v[kGatherRows];
+#pragma unroll
+        for (int i = 0; i < kGatherRows; ++i) v[i] = src[i] ? src[i][c] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < kGatherRows; ++i)
+            if (dst[i]) dst[i][c] = v[i];
+    }
 }
 
 constexpr int kSB = 64;  // rows and columns per SIMT tile
@@ -160,8 +182,8 @@ cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, cons
                                int n, int64_t S, int d, int k, __nv_bfloat16 *out, int32_t *err,
                                cudaStream_t st) {
     if (S == 0) return cudaSuccess;
-    ffn_gather<<<static_cast<unsigned>((S + 7) / 8), 256, 0, st>>>(x, perm, offsets, n, S, d, k, out,
-                                                                 err);
+    ffn_gather<<<static_cast<unsigned>((S + 8 * kGatherRows - 1) / (8 * kGatherRows)), 256, 0, st>>>(
+        x, perm, offsets, n, S, d, k, out, err);
     return cudaGetLastError();
 }
 
@@ -177,7 +199,7 @@ cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *
         ffn_tiles<<<1, 1024, 0, st>>>(offsets, s.n, kTcRows, tiles);
         __nv_bfloat16 *xperm = ws_ptr<__nv_bfloat16>(ws, L.xperm);
         __nv_bfloat16 *hid = ws_ptr<__nv_bfloat16>(ws, L.hidden);
-        ffn_gather<<<static_cast<unsigned>((S + 7) / 8), 256, 0, st>>>(
+        ffn_gather<<<static_cast<unsigned>((S + 8 * kGatherRows - 1) / (8 * kGatherRows)), 256, 0, st>>>(
             static_cast<const __nv_bfloat16 *>(x), perm, offsets, s.n, S, s.d, s.k, xperm, err);
         cudaError_t e = launch_grouped_gemm_tc(s, xperm, s.d, static_cast<const __nv_bfloat16 *>(W1),
                                                s.h, b1, 1, offsets, tiles, hid, err, st);
