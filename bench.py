@@ -49,7 +49,49 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target CPU seconds of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--traffic-summary", nargs=2, metavar=("NCU_CSV", "BENCH_JSON"),
+                   help="print the DRAM-traffic record of one expert-FFN stage from an ncu "
+                        "--csv log of the stage's launches (TRAFFIC_NCU) and the bench line "
+                        "of the same command, then exit")
     return p.parse_args()
+
+
+TRAFFIC_BENCH = "python bench.py --steps 3 --warmup 3 --e2e-steps 3 --no-cpu-baseline"
+TRAFFIC_NCU = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
+               "--clock-control none -k regex:ffn_ -s 12 -c 4 --csv --log-file traffic.csv ")
+
+
+def traffic_summary(csv_path: str, bench_json: str, w: wl.Workload) -> dict:
+    """DRAM bytes of the four launches of one expert-FFN stage (tile table,
+    gather, two grouped GEMMs) of the first timed step, as ncu counted them."""
+    import csv
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    rows = list(csv.DictReader(lines))
+    launches = {}
+    for r in rows:
+        k = launches.setdefault(int(r["ID"]), {"kernel": r["Kernel Name"].split("(")[0]})
+        v = float(r["Metric Value"].replace(",", ""))
+        unit = r["Metric Unit"]
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "ns": 1, "us": 1e3, "usecond": 1e3,
+                 "nsecond": 1, "ms": 1e6, "msecond": 1e6}[unit]
+        key = {"dram__bytes_read.sum": "dram_read_bytes", "dram__bytes_write.sum": "dram_write_bytes",
+               "gpu__time_duration.sum": "duration_ns_cold"}[r["Metric Name"]]
+        k[key] = int(round(v * scale))
+    kernels = [dict(launch=i, **launches[i]) for i in sorted(launches)]
+    with open(bench_json) as f:
+        line = json.loads(f.read().strip().splitlines()[-1])
+    total = sum(k["dram_read_bytes"] + k["dram_write_bytes"] for k in kernels)
+    return {
+        "workload": w.name,
+        "what": "DRAM bytes (read + write) of the four launches of one expert-FFN stage "
+                "(moe_expert_ffn), first timed step",
+        "command": f"{TRAFFIC_BENCH} (exit 0), then: {TRAFFIC_NCU}{TRAFFIC_BENCH}",
+        "source_sha256": source_digest(),
+        "ffn_stage_dram_bytes_per_launch": total,
+        "algorithmic_bytes_per_launch": line["roofline"]["algorithmic_per_launch"],
+        "kernels": kernels,
+    }
 
 
 # ---------------------------------------------------------------------------
@@ -66,15 +108,15 @@ def peaks():
         return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
 
 
+FFN_STAGE_SOURCES = ("ffn.cu", "ffn_tc.cu", "moe_device.cuh", "moe_launch.h")
+
+
 def source_digest() -> str:
-    """sha256 of the CUDA library's sources (kernels, headers, the C ABI)."""
-    import glob
+    """sha256 of the sources the expert-FFN stage's kernels are built from
+    (the kernels, their device helpers and the workspace layout)."""
     import hashlib
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "sparsely_gated_mixture_top_b300", "csrc", "*.cu")) +
-                   glob.glob(os.path.join(ROOT, "sparsely_gated_mixture_top_b300", "csrc", "*.cuh")) +
-                   glob.glob(os.path.join(ROOT, "sparsely_gated_mixture_top_b300", "csrc", "*.h")) +
-                   glob.glob(os.path.join(ROOT, "include", "*.h")))
+    files = [os.path.join(ROOT, "sparsely_gated_mixture_top_b300", "csrc", f) for f in FFN_STAGE_SOURCES]
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
@@ -281,6 +323,9 @@ def launches_per_step(w: wl.Workload) -> int:
 def main():
     args = parse()
     w = wl.WORKLOADS[args.workload]
+    if args.traffic_summary:
+        print(json.dumps(traffic_summary(*args.traffic_summary, w), indent=1))
+        return
     if args.impl == "reference":
         reference_arm(args, w)
         return

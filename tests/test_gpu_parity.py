@@ -39,6 +39,14 @@ SMALL = [
       seed=24),
     W("hier_stream_x", T=130, d=576, h=128, n=12, k=2, groups=3, k_groups=1, seed=25),
     W("flat_stream_x_k1", T=300, d=640, h=64, n=70, k=1, bias_std=0.1, seed=26),
+    W("big_experts_ragged", T=1500, d=256, h=512, n=5, k=2, bias_std=0.3, seed=27),
+    W("zipf_sparse_tail", T=4000, d=256, h=256, n=16, k=1, gate_bias="zipf", seed=28),
+    # Thousands of slots: many 128-row blocks per expert with ragged and
+    # exactly full last blocks, 96 experts with no rows beside one with 2424,
+    # and the FFN widths of the full-size workloads.
+    W("many_blocks_ragged", T=3000, d=256, h=512, n=24, k=4, bias_std=0.2, seed=29),
+    W("zipf_empty_experts", T=2500, d=256, h=256, n=200, k=4, gate_bias="zipf", seed=30),
+    W("full_widths_16_experts", T=2400, d=512, h=1024, n=16, k=4, bias_std=0.1, seed=31),
 ]
 
 
