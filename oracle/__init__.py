@@ -1,4 +1,4 @@
-"""CPU oracle of the MoE layer forward pass (ctypes front of `oracle.c`).
+"""CPU oracle of the MoE layer forward and backward passes (ctypes front of `oracle.c`).
 
 TEST INFRASTRUCTURE ONLY: the tests, the package entry file's smoke check and
 the benchmark's CPU-baseline leg may import this module; the product path never
@@ -54,6 +54,8 @@ def _lib_():
         lib.oracle_load.restype = i32
         lib.oracle_combine_rows.argtypes = [i64, i32, i32, i64] + [vp] * 4
         lib.oracle_combine_rows.restype = i32
+        lib.oracle_backward_flat.argtypes = [i64, i32, i32, i32, i32] + [vp] * 10 + [dbl] + [vp] * 10
+        lib.oracle_backward_flat.restype = i32
         _lib = lib
     return _lib
 
@@ -246,4 +248,26 @@ def forward(x, Wg, Wn, bg, eps, W1, b1, W2, b2, k: int, groups: int = 0, k_group
     out["cv2"] = cv2.value
     out["perm"] = out["perm"][:S]
     out["inv_perm"] = out["inv_perm"][:S]
+    return out
+
+
+def backward(x, Wg, Wn, bg, eps, W1, b1, W2, b2, dy, k: int, w_imp: float = 0.0):
+    """Gradients of L = sum_t <dy_t, y_t> + w_imp * CV^2(importance) for the
+    flat layer, the selection held fixed.  Returns a dict with dx, dWg, dWn,
+    dbg, dW1, db1, dW2, db2 (float64, the shapes of the inputs; dbg, db1, db2
+    are None when the bias is None) and the forward's idx, G."""
+    x, Wg, Wn, bg, eps, W1, b1, W2, b2, dy = map(_f64, (x, Wg, Wn, bg, eps, W1, b1, W2, b2, dy))
+    T, d = x.shape
+    n, h, _ = W1.shape
+    out = dict(dx=np.zeros((T, d)), dWg=np.zeros((d, n)), dWn=np.zeros((d, n)),
+               dbg=np.zeros(n) if bg is not None else None,
+               dW1=np.zeros((n, h, d)), db1=np.zeros((n, h)) if b1 is not None else None,
+               dW2=np.zeros((n, d, h)), db2=np.zeros((n, d)) if b2 is not None else None,
+               idx=np.zeros((T, k), np.int32), G=np.zeros((T, k)))
+    rc = _lib_().oracle_backward_flat(
+        T, d, h, n, k, _p(x), _p(Wg), _p(Wn), _p(bg), _p(eps), _p(W1), _p(b1), _p(W2), _p(b2),
+        _p(dy), float(w_imp), _p(out["dx"]), _p(out["dWg"]), _p(out["dWn"]), _p(out["dbg"]),
+        _p(out["dW1"]), _p(out["db1"]), _p(out["dW2"]), _p(out["db2"]), _p(out["idx"]), _p(out["G"]))
+    if rc:
+        raise ValueError("oracle_backward_flat: bad arguments")
     return out

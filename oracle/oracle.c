@@ -1,7 +1,7 @@
 /*
- * oracle.c -- plain, slow CPU oracle for the forward pass of the
- * Sparsely-Gated Mixture-of-Experts layer (Shazeer et al. 2017,
- * "Outrageously Large Neural Networks").
+ * oracle.c -- plain, slow CPU oracle for the forward pass (and, for flat
+ * gating, the backward pass) of the Sparsely-Gated Mixture-of-Experts layer
+ * (Shazeer et al. 2017, "Outrageously Large Neural Networks").
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check of the package
  * entry file and the CPU-baseline leg of the benchmark may load or call this
@@ -515,4 +515,198 @@ int oracle_combine_rows(int64_t T, int d, int k, int64_t S, const double *Y,
         }
     }
     return 0;
+}
+
+/*
+ * Backward pass of the flat layer.  [MoE:稀疏门控混合专家] section 四 and the
+ * wudongming97 note train the layer (noise during training, the importance
+ * loss beside the task loss); the pages give no formula for the gradients, so
+ * they are the chain rule of the forward definition above, taken with the
+ * selection held fixed (KeepTopK is piecewise constant in its inputs), for
+ *
+ *   L = sum_t <dy_t, y_t>  +  w_imp * CV^2(importance)
+ *
+ * dy [T, d] is the upstream gradient of y, w_imp the weight of the importance
+ * loss.  Written out, for token t and slot j with expert e = idx[t, j]:
+ *   z = W1[e] x_t + b1[e],  a = max(z, 0),  E = W2[e] a + b2[e]
+ *   dG_j   = <dy_t, E> + w_imp * dCV2/dimp_e
+ *            dCV2/dimp_e = 2 (imp_e - mu) / (n mu^2) - 2 var / (n mu^3)
+ *            (mu, var: mean and population variance of importance; 0 if mu = 0)
+ *   dH_j   = G_j (dG_j - sum_l G_l dG_l)                   (softmax over the k kept)
+ *   dc_j   = dH_j;  dr_j = dH_j * eps[t, e] * sigmoid(r_j),  r_j = x_t . Wn[:, e]
+ *   dE     = G_j dy_t;  da = W2[e]^T dE;  dz = da * [z > 0]
+ *   dx_t  += dc_j Wg[:, e] + dr_j Wn[:, e] + W1[e]^T dz
+ *   dWg[:, e] += dc_j x_t;  dWn[:, e] += dr_j x_t;  dbg[e] += dc_j
+ *   dW2[e] += dE a^T;  db2[e] += dE;  dW1[e] += dz x_t^T;  db1[e] += dz
+ * The per-token part runs in parallel over tokens; the per-expert sums run in
+ * parallel over experts, each over its slots in token order.  idx_out [T, k]
+ * and G_out [T, k] (the gate of the forward) may be NULL.  eps NULL = no noise
+ * (then dWn is all zeros).  Every output is overwritten.
+ */
+int oracle_backward_flat(int64_t T, int d, int h, int n, int k, const double *x,
+                         const double *Wg, const double *Wn, const double *bg, const double *eps,
+                         const double *W1, const double *b1, const double *W2, const double *b2,
+                         const double *dy, double w_imp, double *dx, double *dWg, double *dWn,
+                         double *dbg, double *dW1, double *db1, double *dW2, double *db2,
+                         int32_t *idx_out, double *G_out) {
+    if (T < 0 || d <= 0 || h <= 0 || n <= 0 || k <= 0 || k > n) return -1;
+    const int64_t S = T * k;
+    int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)(S > 0 ? S : 1));
+    double *G = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    double *dc = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    double *dr = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    double *imp = (double *)calloc((size_t)n, sizeof(double));
+    double *gimp = (double *)calloc((size_t)n, sizeof(double));
+    if (!idx || !G || !dc || !dr || !imp || !gimp) return -1;
+    int rc = oracle_gate_flat(T, d, n, k, x, Wg, Wn, bg, eps, idx, G, NULL, NULL);
+    if (rc) return rc;
+
+    /* importance and the gradient of w_imp * CV^2 with respect to it */
+    for (int64_t s = 0; s < S; ++s) imp[idx[s]] += G[s];
+    double mu = 0.0, var = 0.0;
+    for (int e = 0; e < n; ++e) mu += imp[e];
+    mu /= n;
+    for (int e = 0; e < n; ++e) var += (imp[e] - mu) * (imp[e] - mu);
+    var /= n;
+    if (mu != 0.0)
+        for (int e = 0; e < n; ++e)
+            gimp[e] = w_imp * (2.0 * (imp[e] - mu) / (n * mu * mu) - 2.0 * var / (n * mu * mu * mu));
+
+    int bad = 0;
+    /* per token: dG, dH, dc, dr and the whole of dx_t */
+#pragma omp parallel
+    {
+        double *z = (double *)malloc(sizeof(double) * (size_t)h);
+        double *a = (double *)malloc(sizeof(double) * (size_t)h);
+        double *E = (double *)malloc(sizeof(double) * (size_t)d);
+        double *dG = (double *)malloc(sizeof(double) * (size_t)k);
+        if (!z || !a || !E || !dG) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t t = 0; t < T; ++t) {
+                const double *xt = x + t * d;
+                const double *dyt = dy + t * d;
+                double *dxt = dx + t * d;
+                for (int o = 0; o < d; ++o) dxt[o] = 0.0;
+                for (int j = 0; j < k; ++j) {
+                    const int e = idx[t * k + j];
+                    const double *W1e = W1 + (int64_t)e * h * d, *W2e = W2 + (int64_t)e * d * h;
+                    for (int i = 0; i < h; ++i) {
+                        double v = b1 ? b1[(int64_t)e * h + i] : 0.0;
+                        for (int q = 0; q < d; ++q) v += W1e[(int64_t)i * d + q] * xt[q];
+                        z[i] = v;
+                        a[i] = v > 0.0 ? v : 0.0;
+                    }
+                    double g = gimp[e];
+                    for (int o = 0; o < d; ++o) {
+                        double v = b2 ? b2[(int64_t)e * d + o] : 0.0;
+                        for (int i = 0; i < h; ++i) v += W2e[(int64_t)o * h + i] * a[i];
+                        E[o] = v;
+                        g += dyt[o] * v;
+                    }
+                    dG[j] = g;
+                }
+                double sGdG = 0.0;
+                for (int j = 0; j < k; ++j) sGdG += G[t * k + j] * dG[j];
+                for (int j = 0; j < k; ++j) {
+                    const int64_t s = t * k + j;
+                    const int e = idx[s];
+                    const double dH = G[s] * (dG[j] - sGdG);
+                    double r = 0.0;
+                    for (int q = 0; q < d; ++q) r += xt[q] * Wn[(int64_t)q * n + e];
+                    const double dr_s = eps ? dH * eps[t * (int64_t)n + e] / (1.0 + exp(-r)) : 0.0;
+                    dc[s] = dH;
+                    dr[s] = dr_s;
+                    for (int q = 0; q < d; ++q)
+                        dxt[q] += dH * Wg[(int64_t)q * n + e] + dr_s * Wn[(int64_t)q * n + e];
+                    /* expert part: dz = (W2[e]^T (G dy_t)) * [z > 0]; dx_t += W1[e]^T dz */
+                    const double *W1e = W1 + (int64_t)e * h * d, *W2e = W2 + (int64_t)e * d * h;
+                    for (int i = 0; i < h; ++i) {
+                        double v = b1 ? b1[(int64_t)e * h + i] : 0.0;
+                        for (int q = 0; q < d; ++q) v += W1e[(int64_t)i * d + q] * xt[q];
+                        double da = 0.0;
+                        for (int o = 0; o < d; ++o) da += W2e[(int64_t)o * h + i] * G[s] * dyt[o];
+                        const double dz = v > 0.0 ? da : 0.0;
+                        for (int q = 0; q < d; ++q) dxt[q] += W1e[(int64_t)i * d + q] * dz;
+                    }
+                }
+            }
+        }
+        free(z);
+        free(a);
+        free(E);
+        free(dG);
+    }
+    if (bad) return -1;
+
+    /* per expert: weight and bias gradients, summed over its slots in token order */
+#pragma omp parallel
+    {
+        double *a = (double *)malloc(sizeof(double) * (size_t)h);
+        double *dz = (double *)malloc(sizeof(double) * (size_t)h);
+        double *dE = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!a || !dz || !dE) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int e = 0; e < n; ++e) {
+                const double *W1e = W1 + (int64_t)e * h * d, *W2e = W2 + (int64_t)e * d * h;
+                double *dW1e = dW1 + (int64_t)e * h * d, *dW2e = dW2 + (int64_t)e * d * h;
+                memset(dW1e, 0, sizeof(double) * (size_t)h * d);
+                memset(dW2e, 0, sizeof(double) * (size_t)d * h);
+                if (db1) memset(db1 + (int64_t)e * h, 0, sizeof(double) * (size_t)h);
+                if (db2) memset(db2 + (int64_t)e * d, 0, sizeof(double) * (size_t)d);
+                for (int q = 0; q < d; ++q) {
+                    dWg[(int64_t)q * n + e] = 0.0;
+                    if (dWn) dWn[(int64_t)q * n + e] = 0.0;
+                }
+                if (dbg) dbg[e] = 0.0;
+                for (int64_t s = 0; s < S; ++s) {
+                    if (idx[s] != e) continue;
+                    const double *xt = x + (s / k) * d;
+                    const double *dyt = dy + (s / k) * d;
+                    for (int i = 0; i < h; ++i) {
+                        double v = b1 ? b1[(int64_t)e * h + i] : 0.0;
+                        for (int q = 0; q < d; ++q) v += W1e[(int64_t)i * d + q] * xt[q];
+                        a[i] = v > 0.0 ? v : 0.0;
+                        dz[i] = v;  /* pre-activation, masked below */
+                    }
+                    for (int o = 0; o < d; ++o) dE[o] = G[s] * dyt[o];
+                    for (int i = 0; i < h; ++i) {
+                        double da = 0.0;
+                        for (int o = 0; o < d; ++o) da += W2e[(int64_t)o * h + i] * dE[o];
+                        dz[i] = dz[i] > 0.0 ? da : 0.0;
+                    }
+                    for (int o = 0; o < d; ++o) {
+                        for (int i = 0; i < h; ++i) dW2e[(int64_t)o * h + i] += dE[o] * a[i];
+                        if (db2) db2[(int64_t)e * d + o] += dE[o];
+                    }
+                    for (int i = 0; i < h; ++i) {
+                        for (int q = 0; q < d; ++q) dW1e[(int64_t)i * d + q] += dz[i] * xt[q];
+                        if (db1) db1[(int64_t)e * h + i] += dz[i];
+                    }
+                    for (int q = 0; q < d; ++q) {
+                        dWg[(int64_t)q * n + e] += dc[s] * xt[q];
+                        if (dWn) dWn[(int64_t)q * n + e] += dr[s] * xt[q];
+                    }
+                    if (dbg) dbg[e] += dc[s];
+                }
+            }
+        }
+        free(a);
+        free(dz);
+        free(dE);
+    }
+    if (idx_out) memcpy(idx_out, idx, sizeof(int32_t) * (size_t)S);
+    if (G_out) memcpy(G_out, G, sizeof(double) * (size_t)S);
+    free(idx);
+    free(G);
+    free(dc);
+    free(dr);
+    free(imp);
+    free(gimp);
+    return bad ? -1 : 0;
 }
