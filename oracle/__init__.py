@@ -254,16 +254,14 @@ def forward(x, Wg, Wn, bg, eps, W1, b1, W2, b2, k: int, groups: int = 0, k_group
 def backward(x, Wg, Wn, bg, eps, W1, b1, W2, b2, dy, k: int, w_imp: float = 0.0):
     """Gradients of L = sum_t <dy_t, y_t> + w_imp * CV^2(importance) for the
     flat layer, the selection held fixed.  Returns a dict with dx, dWg, dWn,
-    dbg, dW1, db1, dW2, db2 (float64, the shapes of the inputs; dbg, db1, db2
-    are None when the bias is None) and the forward's idx, G."""
+    dbg, dW1, db1, dW2, db2 (float64, the shapes of the inputs; a bias given as
+    None counts as zero and still gets its gradient) and the forward's idx, G."""
     x, Wg, Wn, bg, eps, W1, b1, W2, b2, dy = map(_f64, (x, Wg, Wn, bg, eps, W1, b1, W2, b2, dy))
     T, d = x.shape
     n, h, _ = W1.shape
-    out = dict(dx=np.zeros((T, d)), dWg=np.zeros((d, n)), dWn=np.zeros((d, n)),
-               dbg=np.zeros(n) if bg is not None else None,
-               dW1=np.zeros((n, h, d)), db1=np.zeros((n, h)) if b1 is not None else None,
-               dW2=np.zeros((n, d, h)), db2=np.zeros((n, d)) if b2 is not None else None,
-               idx=np.zeros((T, k), np.int32), G=np.zeros((T, k)))
+    out = dict(dx=np.zeros((T, d)), dWg=np.zeros((d, n)), dWn=np.zeros((d, n)), dbg=np.zeros(n),
+               dW1=np.zeros((n, h, d)), db1=np.zeros((n, h)), dW2=np.zeros((n, d, h)),
+               db2=np.zeros((n, d)), idx=np.zeros((T, k), np.int32), G=np.zeros((T, k)))
     rc = _lib_().oracle_backward_flat(
         T, d, h, n, k, _p(x), _p(Wg), _p(Wn), _p(bg), _p(eps), _p(W1), _p(b1), _p(W2), _p(b2),
         _p(dy), float(w_imp), _p(out["dx"]), _p(out["dWg"]), _p(out["dWn"]), _p(out["dbg"]),
