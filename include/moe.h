@@ -234,6 +234,36 @@ MOE_API moe_status moe_gate_load(const moe_shape *shape, const void *x, const fl
                                  size_t ws_bytes, void *lws, size_t lws_bytes, void *stream);
 
 /*
+ * Backward pass of the flat layer (groups == 0; MOE_ERR_UNSUPPORTED for the
+ * hierarchical gate).  The pages train the layer with noise in the gate
+ * ("MoE:稀疏门控混合专家", section 四) and an importance loss beside the task
+ * loss ("Outrageously Large Neural Networks — MoE 怎样让模型“很大但不每次全算”",
+ * section 方法怎么做); the gradients are the chain rule of the forward pass
+ * with the forward's selection idx held fixed, for the loss
+ *   L = sum_t <dy[t], y[t]> + w_importance * CV^2(importance).
+ * Inputs: the forward's inputs (x, W1, W2, dy in the shape's dtype; Wg, Wnoise
+ * [d,n], eps [T,n], b1, b2 fp32; bg is not needed), its outputs idx [T,k], G
+ * [T,k] and importance [n] (only read when w_importance != 0), and dy [T,d].
+ * Outputs, all fp32 and overwritten: dx [T,d], dWg [d,n], dWnoise [d,n] (all
+ * zero when noisy == 0; may then be NULL), dbg [n], dW1 [n,h,d], db1 [n,h],
+ * dW2 [n,d,h], db2 [n,d]; dbg, db1, db2 may be NULL when not wanted.
+ * All arithmetic is fp32 on the CUDA cores with every sum in a fixed order, so
+ * results are bit-reproducible.  ws: a caller-owned, 256-byte aligned
+ * workspace of moe_backward_workspace_bytes(shape) bytes (about
+ * 4*S*(2h + 2d + 8) + 8*n*d bytes, S = T*k); its first 256 bytes are the
+ * error header that moe_check reads.  An idx or routing entry out of range
+ * sets MOE_ERR_DEVICE.
+ */
+MOE_API size_t moe_backward_workspace_bytes(const moe_shape *shape);
+MOE_API moe_status moe_backward(const moe_shape *shape, const void *x, const float *Wg,
+                                const float *Wnoise, const float *eps, const void *W1,
+                                const float *b1, const void *W2, const float *b2,
+                                const int32_t *idx, const float *G, const float *importance,
+                                const void *dy, float w_importance, float *dx, float *dWg,
+                                float *dWnoise, float *dbg, float *dW1, float *db1, float *dW2,
+                                float *db2, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * Synchronises `stream`, reads the workspace's device error word, clears it
  * and returns it (MOE_OK when no device error was recorded).  Returns
  * MOE_ERR_CUDA if the stream itself failed.

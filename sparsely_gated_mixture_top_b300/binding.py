@@ -30,7 +30,7 @@ MOE_BF16 = 1
 EXPORTS = ("moe_version", "moe_status_string", "moe_validate", "moe_workspace_bytes",
            "moe_workspace_init", "moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine",
            "moe_forward", "moe_check", "moe_dispatch_noalloc", "moe_load_workspace_bytes",
-           "moe_gate_load")
+           "moe_gate_load", "moe_backward_workspace_bytes", "moe_backward")
 
 
 class MoEShape(ctypes.Structure):
@@ -65,8 +65,11 @@ def _load():
     lib.moe_dispatch_noalloc.argtypes = [shp] + [vp] * 9
     lib.moe_load_workspace_bytes.argtypes, lib.moe_load_workspace_bytes.restype = [shp], sz
     lib.moe_gate_load.argtypes = [shp] + [vp] * 10 + [sz, vp, sz, vp]
+    lib.moe_backward_workspace_bytes.argtypes = [shp]
+    lib.moe_backward_workspace_bytes.restype = sz
+    lib.moe_backward.argtypes = [shp] + [vp] * 12 + [ctypes.c_float] + [vp] * 9 + [sz, vp]
     for f in ("moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
-              "moe_check", "moe_dispatch_noalloc", "moe_gate_load"):
+              "moe_check", "moe_dispatch_noalloc", "moe_gate_load", "moe_backward"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -209,3 +212,26 @@ def forward(shape: MoEShape, inp: dict, ws=None, out=None, stream=None) -> dict:
                 inp["W1"], inp.get("b1"), inp["W2"], inp.get("b2"), out["y"], out["G"],
                 out["idx"], out["importance"], out["cv2"], out["counts"], ws, stream)
     return out
+
+
+def backward_workspace_bytes(shape: MoEShape) -> int:
+    return lib.moe_backward_workspace_bytes(ctypes.byref(shape))
+
+
+def backward_workspace(shape: MoEShape, device="cuda", stream=None) -> torch.Tensor:
+    """A fresh backward workspace (uint8 device tensor) with its error word cleared."""
+    nbytes = backward_workspace_bytes(shape)
+    if nbytes == 0:
+        raise MoEError("moe_backward_workspace_bytes", validate(shape) or MOE_ERR_UNSUPPORTED)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    _ok("moe_workspace_init", lib.moe_workspace_init(_p(ws), nbytes, _stream(stream)))
+    return ws
+
+
+def moe_backward(shape, x, Wg, Wn, eps, W1, b1, W2, b2, idx, G, importance, dy, w_importance,
+                 dx, dWg, dWn, dbg, dW1, db1, dW2, db2, ws, stream=None):
+    """Gradients of sum <dy, y> + w_importance * CV^2(importance) (flat layer)."""
+    _ok("moe_backward", lib.moe_backward(
+        ctypes.byref(shape), _p(x), _p(Wg), _p(Wn), _p(eps), _p(W1), _p(b1), _p(W2), _p(b2),
+        _p(idx), _p(G), _p(importance), _p(dy), float(w_importance), _p(dx), _p(dWg), _p(dWn),
+        _p(dbg), _p(dW1), _p(db1), _p(dW2), _p(db2), _p(ws), ws.numel(), _stream(stream)))

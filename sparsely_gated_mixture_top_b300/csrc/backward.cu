@@ -1,0 +1,673 @@
+// backward.cu -- the backward pass of the flat layer (moe_backward in moe.h).
+//
+// The pages train the layer: noise in the gate during training
+// ("MoE:稀疏门控混合专家", section 四) and an importance loss beside the task
+// loss ("Outrageously Large Neural Networks — MoE 怎样让模型“很大但不每次全算”",
+// section 方法怎么做).  With the selection of the forward pass held fixed
+// (KeepTopK is piecewise constant), the gradients of
+//     L = sum_t <dy_t, y_t> + w_imp * CV^2(importance)
+// are the chain rule through the combine, the experts, the softmax over the
+// kept scores, the noise scale and the importance sum:
+//   z = W1[e] x + b1[e], a = ReLU(z), E = W2[e] a + b2[e]      (per slot, recomputed)
+//   dG_j  = <dy_t, E_j> + w_imp dCV^2/dimp_e
+//   dH_j  = G_j (dG_j - sum_l G_l dG_l)
+//   dc_j  = dH_j,  dr_j = dH_j eps[t,e] sigmoid(x_t . Wn[:,e])
+//   dE    = G_j dy_t,  dz = (W2[e]^T dE) * [z > 0]
+//   dx_t  = sum_j dc_j Wg[:,e_j] + dr_j Wn[:,e_j] + W1[e_j]^T dz_j
+//   dWg[:,e] = sum dc x,  dWn[:,e] = sum dr x,  dbg[e] = sum dc
+//   dW2[e] = sum dE a^T,  db2[e] = sum dE,  dW1[e] = sum dz x^T,  db1[e] = sum dz
+//
+// Everything runs in fp32 on the CUDA cores (inputs of either dtype are read
+// exactly), every sum in a fixed order, so results are bit-reproducible.
+// Stages, in launch order:
+//   dispatch of idx (counts, offsets, perm, inv_perm) and a 64-row tile table
+//   bwd_row_gemm  Z = X W1^T + b1 (pre-activation, kept), E = ReLU(Z) W2^T + b2,
+//                 dZ = (dE W2) * [Z > 0] with dE rows = G dy rows, dXs = dZ W1
+//   bwd_transpose Wg^T, Wn^T;  bwd_gimp  w_imp dCV^2/dimp
+//   bwd_token     dG, dH, dc, dr and dx (one warp per token)
+//   bwd_gate_wgrad  dWg, dWn, dbg (one thread per input column per expert)
+//   bwd_wgrad     dW2, dW1 (per expert, summed over its rows);  bwd_colsum  db2, db1
+#include "moe_device.cuh"
+#include "moe_launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int32_t kSiteBwdPerm = 20;
+constexpr int kBT = 64;  // rows and columns of a SIMT tile
+constexpr int kBK = 16;  // k per shared-memory step
+
+struct BwdLayout {
+    size_t local_rank = 0, chunk = 0, chunk_imp = 0, imp64 = 0;
+    size_t counts = 0, offsets = 0, perm = 0, inv_perm = 0, imp = 0, cv2 = 0, tiles = 0;
+    size_t WgT = 0, WnT = 0, gimp = 0, dc = 0, dr = 0;
+    size_t Z = 0, dZ = 0, E = 0, dXs = 0;
+    size_t total = 0;
+};
+
+BwdLayout bwd_layout(const moe_shape &s) {
+    BwdLayout L;
+    const size_t S = static_cast<size_t>(slots(s));
+    const size_t n = static_cast<size_t>(s.n), d = static_cast<size_t>(s.d),
+                 h = static_cast<size_t>(s.h);
+    const size_t chunks = (S + kRouteChunk - 1) / kRouteChunk;
+    size_t o = kWsHeaderBytes;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.local_rank = take(S * 4);
+    L.chunk = take(chunks * n * 4);
+    L.chunk_imp = take(chunks * n * 8);
+    L.imp64 = take(n * 8);
+    L.counts = take(n * 4);
+    L.offsets = take((n + 1) * 4);
+    L.perm = take(S * 4);
+    L.inv_perm = take(S * 4);
+    L.imp = take(n * 4);
+    L.cv2 = take(4);
+    L.tiles = take((n + 1) * 4);
+    L.WgT = take(n * d * 4);
+    L.WnT = take(n * d * 4);
+    L.gimp = take(n * 4);
+    L.dc = take(S * 4);
+    L.dr = take(S * 4);
+    L.Z = take(S * h * 4);
+    L.dZ = take(S * h * 4);
+    L.E = take(S * d * 4);
+    L.dXs = take(S * d * 4);
+    L.total = o;
+    return L;
+}
+
+__device__ __forceinline__ float ldf(const void *p, int64_t i, int bf16) {
+    return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i])
+                : static_cast<const float *>(p)[i];
+}
+
+__device__ __forceinline__ int expert_of_tile(const int32_t *__restrict__ tiles, int n, int rt) {
+    int lo = 0, hi = n - 1;  // largest e with tiles[e] <= rt
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tiles[mid] <= rt)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Row-side operand: value (r, c) = scale * act(P[row(r), c]) where row(r) =
+// perm[r] / kdiv when perm is given (else r) and scale = sc[perm[r]] when sc
+// is given (else 1); act = ReLU when relu.
+struct RowOp {
+    const void *p;
+    int bf16;
+    int64_t ld;
+    const int32_t *perm;
+    int kdiv;
+    const float *sc;
+    int relu;
+};
+
+// out[r, c] = epi( sum_k A(r, k) B_e(k, c) ) for the rows r of expert e, with
+// B_e(k, c) = B[e*bse + k*bsk + c*bsc], epi = + bias[e*N + c], then * [mask[r, c] > 0].
+struct RowGemm {
+    RowOp a;
+    const void *B;
+    int b_bf16;
+    int64_t bse, bsk, bsc;
+    const float *bias;
+    const float *mask;
+    float *out;
+    int K, N;
+    const int32_t *offsets, *tiles;
+    int n;
+    int64_t S;
+    int32_t *err;
+};
+
+__global__ void __launch_bounds__(256) bwd_row_gemm(const RowGemm g) {
+    __shared__ float As[kBK][kBT + 4];
+    __shared__ float Bs[kBK][kBT + 4];
+    __shared__ int64_t arow[kBT];
+    __shared__ float ascale[kBT];
+    const int rt = blockIdx.x;
+    if (rt >= g.tiles[g.n]) return;
+    const int e = expert_of_tile(g.tiles, g.n, rt);
+    const int row0 = g.offsets[e] + (rt - g.tiles[e]) * kBT;
+    const int rows = min(kBT, g.offsets[e + 1] - row0);
+    const int c0 = blockIdx.y * kBT;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    if (tid < kBT) {
+        int64_t ar = -1;
+        float sc = 1.0f;
+        if (tid < rows) {
+            const int64_t r = row0 + tid;
+            if (g.a.perm) {
+                const int32_t s = g.a.perm[r];
+                if (s < 0 || s >= g.S) {
+                    report(g.err, MOE_ERR_DEVICE, kSiteBwdPerm, static_cast<int32_t>(r));
+                } else {
+                    ar = s / g.a.kdiv;
+                    if (g.a.sc) sc = g.a.sc[s];
+                }
+            } else {
+                ar = r;
+            }
+        }
+        arow[tid] = ar;
+        ascale[tid] = sc;
+    }
+    __syncthreads();
+    const int64_t bbase = static_cast<int64_t>(e) * g.bse;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < g.K; k0 += kBK) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * 256;
+            {
+                const int r = idx / kBK, kk = idx % kBK;
+                const int64_t ar = arow[r];
+                float v = 0.0f;
+                if (ar >= 0) {
+                    v = ldf(g.a.p, ar * g.a.ld + k0 + kk, g.a.bf16);
+                    if (g.a.relu) v = fmaxf(v, 0.0f);
+                    v *= ascale[r];
+                }
+                As[kk][r] = v;
+            }
+            {
+                // consecutive threads walk the contiguous dimension of B
+                int kk, c;
+                if (g.bsc == 1) {
+                    kk = idx / kBT;
+                    c = idx % kBT;
+                } else {
+                    kk = idx % kBK;
+                    c = idx / kBK;
+                }
+                Bs[kk][c] = ldf(g.B, bbase + (k0 + kk) * g.bsk + (c0 + c) * g.bsc, g.b_bf16);
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < kBK; ++kk) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                av[i] = As[kk][ty * 4 + i];
+                bv[i] = Bs[kk][tx * 4 + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = ty * 4 + i;
+        if (r >= rows) continue;
+        const int64_t orow = static_cast<int64_t>(row0 + r) * g.N;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = c0 + tx * 4 + j;
+            float v = acc[i][j];
+            if (g.bias) v += g.bias[static_cast<int64_t>(e) * g.N + c];
+            if (g.mask && !(g.mask[orow + c] > 0.0f)) v = 0.0f;
+            g.out[orow + c] = v;
+        }
+    }
+}
+
+// out[e][i, j] = sum over the rows r of expert e, in order, of P(r, i) Q(r, j).
+__global__ void __launch_bounds__(256) bwd_wgrad(RowOp P, RowOp Q, int M, int N,
+                                                 const int32_t *__restrict__ offsets, int64_t S,
+                                                 float *__restrict__ out, int32_t *err) {
+    __shared__ float Ps[kBK][kBT + 4];
+    __shared__ float Qs[kBK][kBT + 4];
+    __shared__ int64_t prow[kBK], qrow[kBK];
+    __shared__ float psc[kBK], qsc[kBK];
+    const int e = blockIdx.z;
+    const int i0 = blockIdx.y * kBT, j0 = blockIdx.x * kBT;
+    const int r_begin = offsets[e], r_end = offsets[e + 1];
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    float acc[4][4] = {};
+    for (int rb = r_begin; rb < r_end; rb += kBK) {
+        if (tid < 2 * kBK) {
+            const bool isq = tid >= kBK;
+            const RowOp op = isq ? Q : P;
+            const int rr = tid % kBK;
+            const int64_t r = rb + rr;
+            int64_t row = -1;
+            float sc = 1.0f;
+            if (r < r_end) {
+                if (op.perm) {
+                    const int32_t s = op.perm[r];
+                    if (s < 0 || s >= S) {
+                        report(err, MOE_ERR_DEVICE, kSiteBwdPerm, static_cast<int32_t>(r));
+                    } else {
+                        row = s / op.kdiv;
+                        if (op.sc) sc = op.sc[s];
+                    }
+                } else {
+                    row = r;
+                }
+            }
+            if (isq) {
+                qrow[rr] = row;
+                qsc[rr] = sc;
+            } else {
+                prow[rr] = row;
+                psc[rr] = sc;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * 256;
+            const int rr = idx / kBT, c = idx % kBT;
+            float pv = 0.0f, qv = 0.0f;
+            if (prow[rr] >= 0) {
+                pv = ldf(P.p, prow[rr] * P.ld + i0 + c, P.bf16);
+                if (P.relu) pv = fmaxf(pv, 0.0f);
+                pv *= psc[rr];
+            }
+            if (qrow[rr] >= 0) {
+                qv = ldf(Q.p, qrow[rr] * Q.ld + j0 + c, Q.bf16);
+                if (Q.relu) qv = fmaxf(qv, 0.0f);
+                qv *= qsc[rr];
+            }
+            Ps[rr][c] = pv;
+            Qs[rr][c] = qv;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int rr = 0; rr < kBK; ++rr) {
+            float pv[4], qv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                pv[i] = Ps[rr][ty * 4 + i];
+                qv[i] = Qs[rr][tx * 4 + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(pv[i], qv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    float *oe = out + static_cast<int64_t>(e) * M * N;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            oe[static_cast<int64_t>(i0 + ty * 4 + i) * N + j0 + tx * 4 + j] = acc[i][j];
+}
+
+// out[e][c] = sum over the rows r of expert e, in order, of P(r, c).
+__global__ void __launch_bounds__(256) bwd_colsum(RowOp P, int M, const int32_t *__restrict__ offsets,
+                                                  int64_t S, float *__restrict__ out, int32_t *err) {
+    const int e = blockIdx.y;
+    const int c = blockIdx.x * 256 + threadIdx.x;
+    if (c >= M) return;
+    float acc = 0.0f;
+    for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+        int64_t row = r;
+        float sc = 1.0f;
+        if (P.perm) {
+            const int32_t s = P.perm[r];
+            if (s < 0 || s >= S) {
+                report(err, MOE_ERR_DEVICE, kSiteBwdPerm, r);
+                continue;
+            }
+            row = s / P.kdiv;
+            if (P.sc) sc = P.sc[s];
+        }
+        float v = ldf(P.p, row * P.ld + c, P.bf16);
+        if (P.relu) v = fmaxf(v, 0.0f);
+        acc = fmaf(v, sc, acc);
+    }
+    out[static_cast<int64_t>(e) * M + c] = acc;
+}
+
+// WT[i, j] = W[j, i] for W [rows, cols] fp32.
+__global__ void bwd_transpose(const float *__restrict__ W, int rows, int cols, float *__restrict__ WT) {
+    __shared__ float t[32][33];
+    const int c = blockIdx.x * 32 + threadIdx.x;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int r = blockIdx.y * 32 + i;
+        if (r < rows && c < cols) t[i][threadIdx.x] = W[static_cast<int64_t>(r) * cols + c];
+    }
+    __syncthreads();
+    const int r2 = blockIdx.y * 32 + threadIdx.x;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int c2 = blockIdx.x * 32 + i;
+        if (c2 < cols && r2 < rows) WT[static_cast<int64_t>(c2) * rows + r2] = t[threadIdx.x][i];
+    }
+}
+
+// gimp[e] = w_imp * dCV^2/dimp_e with CV^2 = population variance / mean^2 of
+// the n importances (0 where the mean is 0); the sums in fp64, fixed order.
+__global__ void __launch_bounds__(256) bwd_gimp(const float *__restrict__ imp, int n, float w_imp,
+                                                float *__restrict__ gimp) {
+    __shared__ double part[256];
+    __shared__ double mu_s, var_s;
+    double acc = 0.0;
+    for (int e = threadIdx.x; e < n; e += 256) acc += imp ? static_cast<double>(imp[e]) : 0.0;
+    part[threadIdx.x] = acc;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o) part[threadIdx.x] += part[threadIdx.x + o];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) mu_s = part[0] / n;
+    __syncthreads();
+    const double mu = mu_s;
+    acc = 0.0;
+    for (int e = threadIdx.x; e < n; e += 256) {
+        const double dv = (imp ? static_cast<double>(imp[e]) : 0.0) - mu;
+        acc += dv * dv;
+    }
+    part[threadIdx.x] = acc;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o) part[threadIdx.x] += part[threadIdx.x + o];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) var_s = part[0] / n;
+    __syncthreads();
+    const double var = var_s;
+    for (int e = threadIdx.x; e < n; e += 256) {
+        double g = 0.0;
+        if (mu != 0.0 && w_imp != 0.0)
+            g = w_imp * (2.0 * ((imp ? static_cast<double>(imp[e]) : 0.0) - mu) / (n * mu * mu) -
+                         2.0 * var / (n * mu * mu * mu));
+        gimp[e] = static_cast<float>(g);
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// One warp per token: dG, dH, dc, dr of its k slots and the whole of dx_t.
+__global__ void __launch_bounds__(256) bwd_token(
+    int64_t T, int d, int n, int k, const void *__restrict__ x, const void *__restrict__ dy,
+    int bf16, const float *__restrict__ E, const float *__restrict__ dXs,
+    const int32_t *__restrict__ inv_perm, const int32_t *__restrict__ idx,
+    const float *__restrict__ G, const float *__restrict__ gimp, const float *__restrict__ WgT,
+    const float *__restrict__ WnT, const float *__restrict__ eps, float *__restrict__ dc,
+    float *__restrict__ dr, float *__restrict__ dx, int32_t *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+    if (t >= T) return;
+    const int64_t S = T * k;
+    float dG[MOE_MAX_K], dH[MOE_MAX_K], drv[MOE_MAX_K];
+    int ex[MOE_MAX_K], row[MOE_MAX_K];
+    float sGdG = 0.0f;
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_K; ++j) {
+        if (j >= k) break;
+        const int64_t s = t * k + j;
+        int e = idx[s];
+        int r = inv_perm[s];
+        if (e < 0 || e >= n || r < 0 || r >= S) {
+            if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteBwdPerm, static_cast<int32_t>(s));
+            e = 0;
+            r = -1;
+        }
+        ex[j] = e;
+        row[j] = r;
+        float acc = 0.0f;
+        if (r >= 0)
+            for (int c = lane; c < d; c += 32)
+                acc = fmaf(ldf(dy, t * d + c, bf16), E[static_cast<int64_t>(r) * d + c], acc);
+        dG[j] = warp_sum(acc) + gimp[e];
+        sGdG = fmaf(G[s], dG[j], sGdG);
+    }
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_K; ++j) {
+        if (j >= k) break;
+        const int64_t s = t * k + j;
+        dH[j] = G[s] * (dG[j] - sGdG);
+        float dv = 0.0f;
+        if (eps) {
+            float acc = 0.0f;
+            for (int c = lane; c < d; c += 32)
+                acc = fmaf(ldf(x, t * d + c, bf16), WnT[static_cast<int64_t>(ex[j]) * d + c], acc);
+            const float r = warp_sum(acc);
+            dv = dH[j] * eps[t * n + ex[j]] / (1.0f + __expf(-r));
+        }
+        drv[j] = dv;
+        if (lane == 0) {
+            dc[s] = dH[j];
+            dr[s] = dv;
+        }
+    }
+    for (int c = lane; c < d; c += 32) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j) {
+            if (j >= k) break;
+            const int64_t we = static_cast<int64_t>(ex[j]) * d + c;
+            acc = fmaf(dH[j], WgT[we], acc);
+            if (eps) acc = fmaf(drv[j], WnT[we], acc);
+            if (row[j] >= 0) acc += dXs[static_cast<int64_t>(row[j]) * d + c];
+        }
+        dx[t * d + c] = acc;
+    }
+}
+
+// dWg[q, e] = sum over e's rows of x[t, q] dc[s]; the same with dr for dWn;
+// dbg[e] = sum of dc.  One thread per input column q, rows in order.
+__global__ void __launch_bounds__(256) bwd_gate_wgrad(
+    int d, int n, int k, int64_t S, const void *__restrict__ x, int bf16,
+    const int32_t *__restrict__ perm, const int32_t *__restrict__ offsets,
+    const float *__restrict__ dc, const float *__restrict__ dr, float *__restrict__ dWg,
+    float *__restrict__ dWn, float *__restrict__ dbg, int32_t *err) {
+    const int e = blockIdx.y;
+    const int q = blockIdx.x * 256 + threadIdx.x;
+    float ag = 0.0f, an = 0.0f, ab = 0.0f;
+    for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+        const int32_t s = perm[r];
+        if (s < 0 || s >= S) {
+            if (q == 0) report(err, MOE_ERR_DEVICE, kSiteBwdPerm, r);
+            continue;
+        }
+        const float g = dc[s];
+        ab += g;
+        if (q < d) {
+            const float xv = ldf(x, static_cast<int64_t>(s / k) * d + q, bf16);
+            ag = fmaf(xv, g, ag);
+            an = fmaf(xv, dr[s], an);
+        }
+    }
+    if (q < d) {
+        dWg[static_cast<int64_t>(q) * n + e] = ag;
+        if (dWn) dWn[static_cast<int64_t>(q) * n + e] = an;
+    }
+    if (dbg && blockIdx.x == 0 && threadIdx.x == 0) dbg[e] = ab;
+}
+
+cudaError_t row_gemm(const RowGemm &g, int64_t S, int n, cudaStream_t st) {
+    const unsigned max_rt = static_cast<unsigned>((S + kBT - 1) / kBT + n);
+    bwd_row_gemm<<<dim3(max_rt, g.N / kBT), 256, 0, st>>>(g);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t backward_workspace_bytes(const moe_shape &s) { return bwd_layout(s).total; }
+
+namespace {
+
+cudaError_t launch_backward(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
+                            const float *eps, const void *W1, const float *b1, const void *W2,
+                            const float *b2, const int32_t *idx, const float *G,
+                            const float *importance, const void *dy, float w_imp, float *dx,
+                            float *dWg, float *dWn, float *dbg, float *dW1, float *db1, float *dW2,
+                            float *db2, void *ws, cudaStream_t st) {
+    const BwdLayout B = bwd_layout(s);
+    const int64_t S = slots(s);
+    const int n = s.n, d = s.d, h = s.h, k = s.k;
+    const int bf16 = s.dtype == MOE_BF16 ? 1 : 0;
+    int32_t *err = ws_ptr<int32_t>(ws, 0);
+    int32_t *offsets = ws_ptr<int32_t>(ws, B.offsets);
+    int32_t *perm = ws_ptr<int32_t>(ws, B.perm);
+    int32_t *inv = ws_ptr<int32_t>(ws, B.inv_perm);
+    int32_t *tiles = ws_ptr<int32_t>(ws, B.tiles);
+    float *WgT = ws_ptr<float>(ws, B.WgT), *WnT = ws_ptr<float>(ws, B.WnT);
+    float *gimp = ws_ptr<float>(ws, B.gimp), *dc = ws_ptr<float>(ws, B.dc), *dr = ws_ptr<float>(ws, B.dr);
+    float *Z = ws_ptr<float>(ws, B.Z), *dZ = ws_ptr<float>(ws, B.dZ);
+    float *E = ws_ptr<float>(ws, B.E), *dXs = ws_ptr<float>(ws, B.dXs);
+    const float *eps_used = s.noisy ? eps : nullptr;
+    float *dWn_used = s.noisy ? dWn : nullptr;
+    if (!s.noisy && dWn) cudaMemsetAsync(dWn, 0, sizeof(float) * d * n, st);
+
+    // routing of the forward's selection (the dispatch's own chunk regions)
+    WsLayout RL{};
+    RL.local_rank = B.local_rank;
+    RL.chunk = B.chunk;
+    RL.chunk_imp = B.chunk_imp;
+    RL.imp64 = B.imp64;
+    cudaError_t e = launch_dispatch(s, idx, G, ws_ptr<int32_t>(ws, B.counts), offsets, perm, inv,
+                                    ws_ptr<float>(ws, B.imp), ws_ptr<float>(ws, B.cv2), ws, RL, st);
+    if (e == cudaSuccess) e = launch_row_tiles(offsets, n, kBT, tiles, st);
+    if (e != cudaSuccess) return e;
+
+    RowGemm g{};
+    g.offsets = offsets;
+    g.tiles = tiles;
+    g.n = n;
+    g.S = S;
+    g.err = err;
+    // Z = X W1^T + b1   (W1[e] is [h, d]: B_e(k, c) = W1[e][c][k])
+    g.a = RowOp{x, bf16, d, perm, k, nullptr, 0};
+    g.B = W1;
+    g.b_bf16 = bf16;
+    g.bse = static_cast<int64_t>(h) * d;
+    g.bsk = 1;
+    g.bsc = d;
+    g.bias = b1;
+    g.mask = nullptr;
+    g.out = Z;
+    g.K = d;
+    g.N = h;
+    if ((e = row_gemm(g, S, n, st)) != cudaSuccess) return e;
+    // E = ReLU(Z) W2^T + b2   (W2[e] is [d, h])
+    g.a = RowOp{Z, 0, h, nullptr, 1, nullptr, 1};
+    g.B = W2;
+    g.bse = static_cast<int64_t>(d) * h;
+    g.bsk = 1;
+    g.bsc = h;
+    g.bias = b2;
+    g.out = E;
+    g.K = h;
+    g.N = d;
+    if ((e = row_gemm(g, S, n, st)) != cudaSuccess) return e;
+    // dZ = (dE W2) * [Z > 0],  dE rows = G[s] dy[t]   (B_e(k, c) = W2[e][k][c])
+    g.a = RowOp{dy, bf16, d, perm, k, G, 0};
+    g.bsk = h;
+    g.bsc = 1;
+    g.bias = nullptr;
+    g.mask = Z;
+    g.out = dZ;
+    g.K = d;
+    g.N = h;
+    if ((e = row_gemm(g, S, n, st)) != cudaSuccess) return e;
+    // dXs = dZ W1   (B_e(k, c) = W1[e][k][c])
+    g.a = RowOp{dZ, 0, h, nullptr, 1, nullptr, 0};
+    g.B = W1;
+    g.bse = static_cast<int64_t>(h) * d;
+    g.bsk = d;
+    g.bsc = 1;
+    g.mask = nullptr;
+    g.out = dXs;
+    g.K = h;
+    g.N = d;
+    if ((e = row_gemm(g, S, n, st)) != cudaSuccess) return e;
+
+    bwd_transpose<<<dim3((n + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wg, d, n, WgT);
+    if (eps_used)
+        bwd_transpose<<<dim3((n + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wn, d, n, WnT);
+    bwd_gimp<<<1, 256, 0, st>>>(w_imp != 0.0f ? importance : nullptr, n, w_imp, gimp);
+    bwd_token<<<static_cast<unsigned>((s.T + 7) / 8), 256, 0, st>>>(
+        s.T, d, n, k, x, dy, bf16, E, dXs, inv, idx, G, gimp, WgT, WnT, eps_used, dc, dr, dx, err);
+    bwd_gate_wgrad<<<dim3((d + 255) / 256, n), 256, 0, st>>>(d, n, k, S, x, bf16, perm, offsets, dc,
+                                                             dr, dWg, dWn_used, dbg, err);
+    // dW2[e] = sum dE a^T  (M = d, N = h),  dW1[e] = sum dz x^T  (M = h, N = d)
+    const RowOp dE_op{dy, bf16, d, perm, k, G, 0};
+    const RowOp a_op{Z, 0, h, nullptr, 1, nullptr, 1};
+    const RowOp dz_op{dZ, 0, h, nullptr, 1, nullptr, 0};
+    const RowOp x_op{x, bf16, d, perm, k, nullptr, 0};
+    bwd_wgrad<<<dim3(h / kBT, d / kBT, n), 256, 0, st>>>(dE_op, a_op, d, h, offsets, S, dW2, err);
+    bwd_wgrad<<<dim3(d / kBT, h / kBT, n), 256, 0, st>>>(dz_op, x_op, h, d, offsets, S, dW1, err);
+    if (db2) bwd_colsum<<<dim3((d + 255) / 256, n), 256, 0, st>>>(dE_op, d, offsets, S, db2, err);
+    if (db1) bwd_colsum<<<dim3((h + 255) / 256, n), 256, 0, st>>>(dz_op, h, offsets, S, db1, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_backward_workspace_bytes(const moe_shape *s) {
+    if (moe_validate(s) != MOE_OK || s->groups != 0) return 0;
+    return backward_workspace_bytes(*s);
+}
+
+moe_status moe_backward(const moe_shape *s, const void *x, const float *Wg, const float *Wnoise,
+                        const float *eps, const void *W1, const float *b1, const void *W2,
+                        const float *b2, const int32_t *idx, const float *G,
+                        const float *importance, const void *dy, float w_importance, float *dx,
+                        float *dWg, float *dWnoise, float *dbg, float *dW1, float *db1, float *dW2,
+                        float *db2, void *ws, size_t ws_bytes, void *stream) {
+    moe_status v = moe_validate(s);
+    if (v != MOE_OK) return v;
+    if (s->groups != 0) return MOE_ERR_UNSUPPORTED;
+    auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    auto req = [&](const void *p) { return p != nullptr && al(p); };
+    auto opt = [&](const void *p) { return p == nullptr || al(p); };
+    if (!req(Wg) || !req(W1) || !req(W2) || !req(dWg) || !req(dW1) || !req(dW2))
+        return MOE_ERR_INVALID_ARG;
+    if (!opt(b1) || !opt(b2) || !opt(dbg) || !opt(db1) || !opt(db2) || !opt(Wnoise) || !opt(eps) ||
+        !opt(dWnoise) || !opt(importance))
+        return MOE_ERR_INVALID_ARG;
+    if (s->noisy && (!req(Wnoise) || !req(dWnoise))) return MOE_ERR_INVALID_ARG;
+    if (w_importance != 0.0f && !req(importance)) return MOE_ERR_INVALID_ARG;
+    if (!(w_importance == w_importance)) return MOE_ERR_INVALID_ARG;  // NaN
+    if (s->T > 0 && (!req(x) || !req(idx) || !req(G) || !req(dy) || !req(dx)))
+        return MOE_ERR_INVALID_ARG;
+    if (s->T > 0 && s->noisy && !req(eps)) return MOE_ERR_INVALID_ARG;
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 ||
+        ws_bytes < backward_workspace_bytes(*s))
+        return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t n = s->n, d = s->d, h = s->h;
+    if (s->T == 0) {
+        // no slot: every gradient is zero
+        cudaMemsetAsync(dWg, 0, sizeof(float) * d * n, st);
+        if (dWnoise) cudaMemsetAsync(dWnoise, 0, sizeof(float) * d * n, st);
+        if (dbg) cudaMemsetAsync(dbg, 0, sizeof(float) * n, st);
+        cudaMemsetAsync(dW1, 0, sizeof(float) * n * h * d, st);
+        cudaMemsetAsync(dW2, 0, sizeof(float) * n * d * h, st);
+        if (db1) cudaMemsetAsync(db1, 0, sizeof(float) * n * h, st);
+        if (db2) cudaMemsetAsync(db2, 0, sizeof(float) * n * d, st);
+        return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
+    const cudaError_t e = launch_backward(*s, x, Wg, Wnoise, eps, W1, b1, W2, b2, idx, G, importance,
+                                          dy, w_importance, dx, dWg, dWnoise, dbg, dW1, db1, dW2,
+                                          db2, ws, st);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

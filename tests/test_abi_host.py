@@ -103,3 +103,30 @@ def test_bad_pointers_rejected_before_any_launch():
                            None, None, None, ok, n, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_check(mis, None) == B.MOE_ERR_WORKSPACE
     assert lib.moe_workspace_init(mis, n, None) == B.MOE_ERR_WORKSPACE
+
+
+def test_backward_rejects_bad_arguments_before_any_launch():
+    s = B.make_shape(**GOOD)
+    n = B.backward_workspace_bytes(s)
+    assert n > 0 and n % 256 == 0
+    ok, mis = _fake(1 << 20), _fake((1 << 20) + 8)
+    lib = B.lib
+
+    def call(shape=s, x=ok, Wg=ok, Wn=ok, eps=ok, W1=ok, b1=None, W2=ok, b2=None, idx=ok, G=ok,
+             imp=ok, dy=ok, w=0.5, dx=ok, dWg=ok, dWn=ok, dbg=None, dW1=ok, db1=None, dW2=ok,
+             db2=None, ws=ok, nbytes=n):
+        return lib.moe_backward(ctypes.byref(shape), x, Wg, Wn, eps, W1, b1, W2, b2, idx, G, imp,
+                                dy, w, dx, dWg, dWn, dbg, dW1, db1, dW2, db2, ws, nbytes, None)
+
+    assert call(x=mis) == B.MOE_ERR_INVALID_ARG
+    assert call(dy=None) == B.MOE_ERR_INVALID_ARG
+    assert call(dWn=None) == B.MOE_ERR_INVALID_ARG            # noisy shape needs dWnoise
+    assert call(eps=None) == B.MOE_ERR_INVALID_ARG
+    assert call(imp=None) == B.MOE_ERR_INVALID_ARG            # w_importance != 0 needs importance
+    assert call(w=float("nan")) == B.MOE_ERR_INVALID_ARG
+    assert call(nbytes=n - 256) == B.MOE_ERR_WORKSPACE
+    assert call(ws=mis) == B.MOE_ERR_WORKSPACE
+    hier = B.make_shape(**dict(GOOD, n=16, groups=4, k_groups=2, k=4))
+    assert B.backward_workspace_bytes(hier) == 0
+    assert call(shape=hier) == B.MOE_ERR_UNSUPPORTED
+    assert call(shape=B.make_shape(**dict(GOOD, k=0))) == B.MOE_ERR_INVALID_ARG

@@ -1,0 +1,165 @@
+"""Parity of the backward pass (moe_backward, through the C ABI) with the CPU
+oracle's backward (fp64, pinned by finite differences of the oracle forward).
+
+The CUDA backward takes the selection (idx, G, importance) of the CUDA
+forward; the oracle runs its own gate, and the two selections are checked to
+be identical first.  All gradients are fp32 on the CUDA side from the exact
+stored inputs, so the bar is a relative Frobenius error of 1e-4 for every
+gradient in both dtypes (fp32 rounding over sums of at most a few thousand
+terms, against fp64).  Small cases compare every element; the full-size
+default workload compares the gradients of three whole experts and of a
+sample of tokens (without the importance term, each of those depends only on
+the tokens that chose the expert, or on the token itself, so the oracle
+computes them on that subset alone) and checks properties of the rest.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import prepared_inputs, rel_fro, run_forward, to_dev
+from sparsely_gated_mixture_top_b300 import binding as B
+from sparsely_gated_mixture_top_b300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+GRADS = ("dx", "dWg", "dWn", "dbg", "dW1", "db1", "dW2", "db2")
+
+W = wl.Workload
+CASES = [
+    (W("bwd_bf16_ragged", T=37, d=64, h=128, n=5, k=2, bias_std=0.1, seed=41), 0.7),
+    (W("bwd_f32_ragged", T=37, d=64, h=128, n=5, k=2, dtype="f32", bias_std=0.1, seed=42), 0.7),
+    (W("bwd_bf16_tiles", T=600, d=192, h=320, n=7, k=3, bias_std=0.05, seed=43), 1.5),
+    (W("bwd_k1", T=100, d=64, h=64, n=6, k=1, bias_std=0.1, seed=44), 0.3),
+    (W("bwd_dense_k_eq_n_f32", T=64, d=128, h=128, n=8, k=8, dtype="f32", seed=45), 2.0),
+    (W("bwd_noise_off", T=80, d=64, h=128, n=6, k=2, noisy=False, seed=46), 0.5),
+    (W("bwd_many_empty_experts", T=20, d=128, h=256, n=64, k=2, seed=47), 1.0),
+    (W("bwd_zipf_empty_experts", T=2500, d=256, h=256, n=200, k=4, gate_bias="zipf", seed=48), 0.2),
+    (W("bwd_no_aux_loss_k16", T=50, d=64, h=64, n=20, k=16, seed=49), 0.0),
+]
+
+
+@pytest.fixture(autouse=True)
+def _free_cuda():
+    yield
+    torch.cuda.empty_cache()
+
+
+def make_dy(w, T=None, seed=None):
+    T = w.T if T is None else T
+    rng = np.random.default_rng(1000 + (w.seed if seed is None else seed))
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    return torch.from_numpy(rng.normal(size=(T, w.d)).astype(np.float32)).to(dt)
+
+
+def run_backward(w, dinp, fwd, dy, w_imp):
+    s = B.shape_of(w)
+    ws = B.backward_workspace(s)
+    T, d, h, n = w.T, w.d, w.h, w.n
+
+    def f32(*shape):
+        return torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+
+    g = dict(dx=f32(T, d), dWg=f32(d, n), dWn=f32(d, n), dbg=f32(n), dW1=f32(n, h, d),
+             db1=f32(n, h), dW2=f32(n, d, h), db2=f32(n, d))
+    B.moe_backward(s, dinp["x"], dinp["Wg"], dinp["Wn"], dinp["eps"] if w.noisy else None,
+                   dinp["W1"], dinp["b1"], dinp["W2"], dinp["b2"], fwd["idx"], fwd["G"],
+                   fwd["importance"], dy.cuda(), w_imp, g["dx"], g["dWg"], g["dWn"], g["dbg"],
+                   g["dW1"], g["db1"], g["dW2"], g["db2"], ws)
+    status = B.moe_check(ws)
+    assert status == B.MOE_OK, B.status_string(status)
+    return {k: v.cpu().numpy() for k, v in g.items()}
+
+
+def oracle_backward(w, inp, dy, w_imp):
+    return oracle.backward(inp["x"], inp["Wg"], inp["Wn"], inp["bg"],
+                           inp["eps"] if w.noisy else None, inp["W1"], inp["b1"], inp["W2"],
+                           inp["b2"], dy, w.k, w_imp)
+
+
+@pytest.mark.parametrize("w,w_imp", CASES, ids=[c[0].name for c in CASES])
+def test_backward_matches_oracle(w, w_imp):
+    inp = prepared_inputs(w)
+    dinp = to_dev(inp)
+    fwd, _ = run_forward(w, dinp)
+    dy = make_dy(w)
+    got = run_backward(w, dinp, fwd, dy, w_imp)
+    ref = oracle_backward(w, inp, dy, w_imp)
+    np.testing.assert_array_equal(fwd["idx"].cpu().numpy(), ref["idx"])
+    for key in GRADS:
+        assert np.isfinite(got[key]).all(), key
+        err = rel_fro(got[key], ref[key])
+        assert err <= TOL, (key, err)
+    if not w.noisy:
+        assert not got["dWn"].any()
+    if w.k == 1:
+        assert not got["dWg"].any() and not got["dbg"].any()
+
+
+def test_backward_is_deterministic():
+    w, w_imp = CASES[2]
+    inp = prepared_inputs(w)
+    dinp = to_dev(inp)
+    fwd, _ = run_forward(w, dinp)
+    dy = make_dy(w)
+    a = run_backward(w, dinp, fwd, dy, w_imp)
+    b = run_backward(w, dinp, fwd, dy, w_imp)
+    for key in GRADS:
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_backward_of_empty_input_is_zero():
+    w = W("bwd_empty", T=0, d=64, h=64, n=4, k=2, seed=50)
+    s = B.shape_of(w)
+    ws = B.backward_workspace(s)
+    dev = "cuda"
+    nan = lambda *sh: torch.full(sh, float("nan"), device=dev)  # noqa: E731
+    Wg, Wn = torch.zeros(64, 4, device=dev), torch.zeros(64, 4, device=dev)
+    W1 = torch.zeros(4, 64, 64, dtype=torch.bfloat16, device=dev)
+    W2 = torch.zeros(4, 64, 64, dtype=torch.bfloat16, device=dev)
+    g = dict(dWg=nan(64, 4), dWn=nan(64, 4), dbg=nan(4), dW1=nan(4, 64, 64), db1=nan(4, 64),
+             dW2=nan(4, 64, 64), db2=nan(4, 64))
+    B.moe_backward(s, None, Wg, Wn, None, W1, None, W2, None, None, None, None, None, 0.0, None,
+                   g["dWg"], g["dWn"], g["dbg"], g["dW1"], g["db1"], g["dW2"], g["db2"], ws)
+    assert B.moe_check(ws) == B.MOE_OK
+    for key, v in g.items():
+        assert not v.any(), key
+
+
+def test_full_size_workload_sampled():
+    """flat_n256_k4 (T=16384, d=512, h=1024, n=256, k=4), no importance term:
+    three whole experts (fewest, median and most rows) and 64 tokens against
+    the oracle on their own token subsets; properties of all gradients."""
+    w = wl.WORKLOADS["flat_n256_k4"]
+    inp = prepared_inputs(w)
+    dinp = to_dev(inp)
+    fwd, _ = run_forward(w, dinp)
+    dy = make_dy(w)
+    got = run_backward(w, dinp, fwd, dy, 0.0)
+    for key in GRADS:
+        assert np.isfinite(got[key]).all(), key
+    # the oracle's own selection decides which tokens each expert saw
+    idx_ref, _, _, _ = oracle.gate_flat(inp["x"], inp["Wg"], inp["Wn"], inp["bg"], inp["eps"], w.k)
+    np.testing.assert_array_equal(fwd["idx"].cpu().numpy(), idx_ref)
+    counts = np.bincount(idx_ref.ravel(), minlength=w.n)
+    order = np.argsort(counts, kind="stable")
+    experts = [int(order[0]), int(order[w.n // 2]), int(order[-1])]
+
+    def sub(rows):
+        return {k: (v[rows] if k in ("x", "eps") and v is not None else v) for k, v in inp.items()}
+
+    for e in experts:
+        rows = np.nonzero((idx_ref == e).any(axis=1))[0]
+        ref = oracle_backward(w, sub(rows), dy[torch.from_numpy(rows)], 0.0)
+        for key in ("dW1", "db1", "dW2", "db2"):
+            assert rel_fro(got[key][e], ref[key][e]) <= TOL, (e, key)
+        for key in ("dWg", "dWn"):
+            assert rel_fro(got[key][:, e], ref[key][:, e]) <= TOL, (e, key)
+        assert abs(got["dbg"][e] - ref["dbg"][e]) <= TOL * (1 + abs(ref["dbg"][e]))
+    rng = np.random.default_rng(7)
+    tokens = np.sort(rng.choice(w.T, 64, replace=False))
+    ref = oracle_backward(w, sub(tokens), dy[torch.from_numpy(tokens)], 0.0)
+    assert rel_fro(got["dx"][tokens], ref["dx"]) <= TOL
+    # softmax shift invariance: the gate bias gradients sum to zero
+    assert abs(float(got["dbg"].astype(np.float64).sum())) <= 1e-3 * float(np.abs(got["dbg"]).sum())
