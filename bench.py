@@ -49,6 +49,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target CPU seconds of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--pass", dest="which", choices=["forward", "backward"], default="forward",
+                   help="forward: moe_forward (the headline); backward: moe_backward of the flat "
+                        "layer with the forward's selection")
     p.add_argument("--traffic-summary", nargs=2, metavar=("NCU_CSV", "BENCH_JSON"),
                    help="print the DRAM-traffic record of one expert-FFN stage from an ncu "
                         "--csv log of the stage's launches (TRAFFIC_NCU) and the bench line "
@@ -320,6 +323,119 @@ def launches_per_step(w: wl.Workload) -> int:
     return gate + dispatch + ffn + combine
 
 
+def backward_launches(w: wl.Workload) -> int:
+    """Kernels one moe_backward call launches (bf16 tensor-core path): dispatch
+    (4), recompute of the expert stage (4), weight transposes (2), dE rows,
+    two row GEMMs and the ReLU mask, k-block table, four padded transposes,
+    two weight-gradient GEMMs, Wg^T (and Wn^T), importance gradient, token
+    kernel, chunk table and the chunked row sums (gate, db2, db1: 6)."""
+    return 4 + 4 + 2 + 1 + 3 + 1 + 4 + 2 + (2 if w.noisy else 1) + 1 + 1 + 1 + 6
+
+
+def backward_arm(args, w: wl.Workload):
+    """Times moe_backward (flat layer) on the workload: the forward runs once
+    for idx, G and importance; each timed step is one backward call with the
+    upstream gradient dy resident on the device."""
+    from sparsely_gated_mixture_top_b300 import binding as B
+    if w.groups:
+        print(json.dumps({"metric": "MoE-layer backward tokens/sec", "unavailable":
+                          "the backward pass covers flat gating only"}))
+        return
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    host = wl.make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    s = B.shape_of(w)
+    ws = B.workspace(s, dev)
+    fwd = B.forward(s, d, ws=ws)
+    bws = B.backward_workspace(s, dev)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    gen = torch.Generator(device="cpu").manual_seed(w.seed + 31)
+    dy = torch.randn((w.T, w.d), generator=gen).to(dt).to(dev)
+    w_imp = 0.01
+
+    def f32(*shape):
+        return torch.empty(shape, dtype=torch.float32, device=dev)
+
+    g = dict(dx=f32(w.T, w.d), dWg=f32(w.d, w.n), dWn=f32(w.d, w.n), dbg=f32(w.n),
+             dW1=f32(w.n, w.h, w.d), db1=f32(w.n, w.h), dW2=f32(w.n, w.d, w.h), db2=f32(w.n, w.d))
+
+    def step():
+        B.moe_backward(s, d["x"], d["Wg"], d["Wn"], d["eps"], d["W1"], d["b1"], d["W2"], d["b2"],
+                       fwd["idx"], fwd["G"], fwd["importance"], dy, w_imp, g["dx"], g["dWg"],
+                       g["dWn"], g["dbg"], g["dW1"], g["db1"], g["dW2"], g["db2"], bws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if B.moe_check(bws, stream) != B.MOE_OK:
+        raise RuntimeError("device error during warm-up")
+    clocks = ClockSampler(0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    status = B.moe_check(bws, stream)
+    if status != B.MOE_OK:
+        raise RuntimeError(f"device error in the timed region: {B.status_string(status)}")
+    ms = e0.elapsed_time(e1) / args.steps
+    counts = fwd["counts"].cpu().numpy()
+    hit = int((counts > 0).sum())
+    eb = 2 if w.dtype == "bf16" else 4
+    S = w.T * w.k
+    # algorithmic: read the weights of the experts hit, x, dy, eps, the gate
+    # matrices; write their gradients (fp32) and dx; contractions: the four
+    # backward GEMMs (8 S d h) and the first layer recomputed for a (2 S d h)
+    bytes_ = (hit * 2 * w.d * w.h * (eb + 4) + w.T * w.d * (2 * eb + 4) +
+              (w.T * w.n * 4 if w.noisy else 0) + 4 * w.d * w.n * 4 + S * 8)
+    flops = 10.0 * S * w.d * w.h
+    pk = peaks()
+    long_run = ms * args.steps > 1000.0
+    tc_peak = pk["bf16_sustained"] if long_run else pk["bf16"]
+    t_hbm, t_tc = bytes_ / (pk["hbm"] * 1e9), flops / (tc_peak * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": bytes_ / (ms / 1e3) / 1e9, "peak": pk["hbm"],
+                "unit": "GB/s", "peak_source": pk["source"] + " copy bandwidth"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / (ms / 1e3) / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s", "peak_source": pk["source"] + " bf16"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = "whole moe_backward call"
+    roof["algorithmic_per_launch"] = bytes_ if t_hbm >= t_tc else flops
+    roof["ms_per_launch"] = ms
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        ntok = min(w.T, 64)
+        t0 = time.time()
+        oracle.backward(host["x"][:ntok], host["Wg"], host["Wn"], host["bg"],
+                        host["eps"][:ntok] if host["eps"] is not None else None, host["W1"],
+                        host["b1"], host["W2"], host["b2"], dy[:ntok].cpu(), w.k, w_imp)
+        dt_cpu = time.time() - t0
+        cpu = {"value": ntok / dt_cpu, "unit": "tokens/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": f"first {ntok} tokens, one fp64 oracle backward "
+                                            f"({dt_cpu:.1f} s, its forward gate included)"}
+    line = {
+        "metric": "MoE-layer backward tokens/sec (moe_backward, 1xB300)",
+        "value": w.T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded counter-based normal)",
+        "config": dict(config_of(w), w_importance=w_imp,
+                       path="tensor cores" if (w.dtype == "bf16" and w.d % 128 == 0 and
+                                               w.h % 128 == 0) else "CUDA cores"),
+        "tflops": flops / (ms / 1e3) / 1e12,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": None,
+        "gpu_launches": backward_launches(w) * args.steps, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     w = wl.WORKLOADS[args.workload]
@@ -328,6 +444,9 @@ def main():
         return
     if args.impl == "reference":
         reference_arm(args, w)
+        return
+    if args.which == "backward":
+        backward_arm(args, w)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

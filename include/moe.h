@@ -247,12 +247,17 @@ MOE_API moe_status moe_gate_load(const moe_shape *shape, const void *x, const fl
  * Outputs, all fp32 and overwritten: dx [T,d], dWg [d,n], dWnoise [d,n] (all
  * zero when noisy == 0; may then be NULL), dbg [n], dW1 [n,h,d], db1 [n,h],
  * dW2 [n,d,h], db2 [n,d]; dbg, db1, db2 may be NULL when not wanted.
- * All arithmetic is fp32 on the CUDA cores with every sum in a fixed order, so
- * results are bit-reproducible.  ws: a caller-owned, 256-byte aligned
- * workspace of moe_backward_workspace_bytes(shape) bytes (about
- * 4*S*(2h + 2d + 8) + 8*n*d bytes, S = T*k); its first 256 bytes are the
- * error header that moe_check reads.  An idx or routing entry out of range
- * sets MOE_ERR_DEVICE.
+ * Every sum runs in a fixed order, so results are bit-reproducible.  bf16
+ * shapes whose d and h are multiples of 128 run the contractions on the
+ * tensor cores (bf16 operands, fp32
+ * accumulation, the recomputed expert outputs and the intermediate gradient
+ * rows rounded to bf16, as in the forward's expert stage); all other shapes
+ * run in fp32 on the CUDA cores.  ws: a caller-owned, 256-byte aligned
+ * workspace of moe_backward_workspace_bytes(shape) bytes (it grows with
+ * S*(d + h), S = T*k, and with n*d*h on the tensor-core path, which also
+ * holds the experts' weights transposed); its first 256 bytes are the error
+ * header that moe_check reads.  An idx or routing entry out of range sets
+ * MOE_ERR_DEVICE.
  */
 MOE_API size_t moe_backward_workspace_bytes(const moe_shape *shape);
 MOE_API moe_status moe_backward(const moe_shape *shape, const void *x, const float *Wg,

@@ -17,20 +17,32 @@
 //   dWg[:,e] = sum dc x,  dWn[:,e] = sum dr x,  dbg[e] = sum dc
 //   dW2[e] = sum dE a^T,  db2[e] = sum dE,  dW1[e] = sum dz x^T,  db1[e] = sum dz
 //
-// Everything runs in fp32 on the CUDA cores (inputs of either dtype are read
-// exactly), every sum in a fixed order, so results are bit-reproducible.
-// Stages, in launch order:
+// bf16 shapes whose widths are multiples of 128 run the contractions on the
+// tensor cores (launch_backward_tc below: bf16 operands, fp32 accumulation,
+// bf16 intermediates); other shapes run everything in fp32 on the CUDA cores
+// (inputs of either dtype are read exactly).  Every sum has a fixed order, so
+// results are bit-reproducible either way.  CUDA-core stages, in launch order:
 //   dispatch of idx (counts, offsets, perm, inv_perm) and a 64-row tile table
 //   bwd_row_gemm  Z = X W1^T + b1 (pre-activation, kept), E = ReLU(Z) W2^T + b2,
 //                 dZ = (dE W2) * [Z > 0] with dE rows = G dy rows, dXs = dZ W1
 //   bwd_transpose Wg^T, Wn^T;  bwd_gimp  w_imp dCV^2/dimp
 //   bwd_token     dG, dH, dc, dr and dx (one warp per token)
-//   bwd_gate_wgrad  dWg, dWn, dbg (one thread per input column per expert)
-//   bwd_wgrad     dW2, dW1 (per expert, summed over its rows);  bwd_colsum  db2, db1
+//   bwd_gate_part/_fin  dWg, dWn, dbg;  bwd_colsum_part/_fin  db2, db1 (row sums in
+//                 256-row chunks, then the chunks of each expert in order)
+//   bwd_wgrad     dW2, dW1 (per expert, summed over its rows)
+#include "backward_tc.h"
 #include "moe_device.cuh"
 #include "moe_launch.h"
 
 namespace moe {
+
+// The forward's grouped tensor-core GEMM (ffn_tc.cu): out[r, c] = act(sum_k
+// A[r, k] B[e*N + c, k] + bias[e, c]) for the 128-row tiles of each expert, bf16 out.
+cudaError_t launch_grouped_gemm_tc(const moe_shape &s, const __nv_bfloat16 *A, int K,
+                                   const __nv_bfloat16 *B, int N, const float *bias, int relu,
+                                   const int32_t *offsets, const int32_t *tiles,
+                                   __nv_bfloat16 *out, int32_t *err, cudaStream_t st);
+
 namespace {
 
 constexpr int32_t kSiteBwdPerm = 20;
@@ -42,8 +54,15 @@ struct BwdLayout {
     size_t counts = 0, offsets = 0, perm = 0, inv_perm = 0, imp = 0, cv2 = 0, tiles = 0;
     size_t WgT = 0, WnT = 0, gimp = 0, dc = 0, dr = 0;
     size_t Z = 0, dZ = 0, E = 0, dXs = 0;
+    size_t ctiles = 0, pg = 0, pn = 0, pb = 0, pc = 0;  // chunked row sums
     size_t total = 0;
 };
+
+// Rows are summed in chunks of this many rows of one expert (see row_sums).
+constexpr int kRowChunk = 256;
+inline size_t row_chunks(const moe_shape &s) {
+    return static_cast<size_t>((slots(s) + kRowChunk - 1) / kRowChunk + s.n);
+}
 
 BwdLayout bwd_layout(const moe_shape &s) {
     BwdLayout L;
@@ -77,6 +96,12 @@ BwdLayout bwd_layout(const moe_shape &s) {
     L.dZ = take(S * h * 4);
     L.E = take(S * d * 4);
     L.dXs = take(S * d * 4);
+    const size_t C = row_chunks(s);
+    L.ctiles = take((n + 1) * 4);
+    L.pg = take(C * d * 4);
+    L.pn = take(C * d * 4);
+    L.pb = take(C * 4);
+    L.pc = take(C * (d > h ? d : h) * 4);
     L.total = o;
     return L;
 }
@@ -308,30 +333,77 @@ __global__ void __launch_bounds__(256) bwd_wgrad(RowOp P, RowOp Q, int M, int N,
             oe[static_cast<int64_t>(i0 + ty * 4 + i) * N + j0 + tx * 4 + j] = acc[i][j];
 }
 
-// out[e][c] = sum over the rows r of expert e, in order, of P(r, c).
-__global__ void __launch_bounds__(256) bwd_colsum(RowOp P, int M, const int32_t *__restrict__ offsets,
-                                                  int64_t S, float *__restrict__ out, int32_t *err) {
-    const int e = blockIdx.y;
-    const int c = blockIdx.x * 256 + threadIdx.x;
-    if (c >= M) return;
-    float acc = 0.0f;
-    for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+// Sums over an expert's rows run in two passes so that an expert holding most
+// of the rows does not serialise on one block: chunks of kChunkRows rows of one
+// expert (chunk table ctiles, built like a row-tile table) are summed by
+// separate blocks, then each expert adds its chunks' partial sums in order.
+constexpr int kChunkRows = kRowChunk;
+
+__device__ __forceinline__ bool chunk_rows(const int32_t *__restrict__ ctiles,
+                                           const int32_t *__restrict__ offsets, int n, int c,
+                                           int *r0, int *r1) {
+    if (c >= ctiles[n]) return false;
+    const int e = expert_of_tile(ctiles, n, c);
+    *r0 = offsets[e] + (c - ctiles[e]) * kChunkRows;
+    *r1 = min(*r0 + kChunkRows, offsets[e + 1]);
+    return true;
+}
+
+// part[c, col] = sum over the rows r of chunk c, in order, of P(r, col).  The
+// rows' source rows and scales are staged in shared memory first, so the
+// column loop issues only independent loads.
+__global__ void __launch_bounds__(256) bwd_colsum_part(RowOp P, int M,
+                                                       const int32_t *__restrict__ offsets,
+                                                       const int32_t *__restrict__ ctiles, int n,
+                                                       int64_t S, float *__restrict__ part,
+                                                       int32_t *err) {
+    __shared__ int64_t srow[kChunkRows];
+    __shared__ float ssc[kChunkRows];
+    int r0, r1;
+    if (!chunk_rows(ctiles, offsets, n, blockIdx.x, &r0, &r1)) return;
+    const int cnt = r1 - r0;
+    if (threadIdx.x < cnt) {
+        const int r = r0 + threadIdx.x;
         int64_t row = r;
         float sc = 1.0f;
         if (P.perm) {
-            const int32_t s = P.perm[r];
-            if (s < 0 || s >= S) {
+            const int32_t sl = P.perm[r];
+            if (sl < 0 || sl >= S) {
                 report(err, MOE_ERR_DEVICE, kSiteBwdPerm, r);
-                continue;
+                row = -1;
+            } else {
+                row = sl / P.kdiv;
+                if (P.sc) sc = P.sc[sl];
             }
-            row = s / P.kdiv;
-            if (P.sc) sc = P.sc[s];
         }
-        float v = ldf(P.p, row * P.ld + c, P.bf16);
-        if (P.relu) v = fmaxf(v, 0.0f);
-        acc = fmaf(v, sc, acc);
+        srow[threadIdx.x] = row;
+        ssc[threadIdx.x] = sc;
     }
-    out[static_cast<int64_t>(e) * M + c] = acc;
+    __syncthreads();
+    const int col = blockIdx.y * 256 + threadIdx.x;
+    if (col >= M) return;
+    float acc = 0.0f;
+#pragma unroll 8
+    for (int i = 0; i < cnt; ++i) {
+        const int64_t row = srow[i];
+        if (row < 0) continue;
+        float v = ldf(P.p, row * P.ld + col, P.bf16);
+        if (P.relu) v = fmaxf(v, 0.0f);
+        acc = fmaf(v, ssc[i], acc);
+    }
+    part[static_cast<int64_t>(blockIdx.x) * M + col] = acc;
+}
+
+// out[e, col] = sum over e's chunks, in order, of part[c, col] (0 for no rows).
+__global__ void __launch_bounds__(256) bwd_colsum_fin(const float *__restrict__ part, int M,
+                                                      const int32_t *__restrict__ ctiles,
+                                                      float *__restrict__ out) {
+    const int e = blockIdx.y;
+    const int col = blockIdx.x * 256 + threadIdx.x;
+    if (col >= M) return;
+    float acc = 0.0f;
+    for (int c = ctiles[e]; c < ctiles[e + 1]; ++c) acc += part[static_cast<int64_t>(c) * M + col];
+    out[static_cast<int64_t>(e) * M + col] = acc;
 }
 
 // WT[i, j] = W[j, i] for W [rows, cols] fp32.
@@ -397,9 +469,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // One warp per token: dG, dH, dc, dr of its k slots and the whole of dx_t.
+// One pass over the columns forms <dy_t, E_j> and <x_t, Wn[:, e_j]> for all
+// k slots (KM >= k accumulators per lane), then 2k warp reductions.
+template <int KM>
 __global__ void __launch_bounds__(256) bwd_token(
     int64_t T, int d, int n, int k, const void *__restrict__ x, const void *__restrict__ dy,
-    int bf16, const float *__restrict__ E, const float *__restrict__ dXs,
+    int bf16, const void *__restrict__ E, const void *__restrict__ dXs, int ebf16,
     const int32_t *__restrict__ inv_perm, const int32_t *__restrict__ idx,
     const float *__restrict__ G, const float *__restrict__ gimp, const float *__restrict__ WgT,
     const float *__restrict__ WnT, const float *__restrict__ eps, float *__restrict__ dc,
@@ -408,40 +483,51 @@ __global__ void __launch_bounds__(256) bwd_token(
     const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
     if (t >= T) return;
     const int64_t S = T * k;
-    float dG[MOE_MAX_K], dH[MOE_MAX_K], drv[MOE_MAX_K];
-    int ex[MOE_MAX_K], row[MOE_MAX_K];
-    float sGdG = 0.0f;
+    int ex[KM], row[KM];
+    float aE[KM], aR[KM];
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_K; ++j) {
-        if (j >= k) break;
+    for (int j = 0; j < KM; ++j) {
+        ex[j] = 0;
+        row[j] = -1;
+        aE[j] = 0.0f;
+        aR[j] = 0.0f;
+        if (j >= k) continue;
         const int64_t s = t * k + j;
-        int e = idx[s];
-        int r = inv_perm[s];
+        const int e = idx[s];
+        const int r = inv_perm[s];
         if (e < 0 || e >= n || r < 0 || r >= S) {
             if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteBwdPerm, static_cast<int32_t>(s));
-            e = 0;
-            r = -1;
+            continue;
         }
         ex[j] = e;
         row[j] = r;
-        float acc = 0.0f;
-        if (r >= 0)
-            for (int c = lane; c < d; c += 32)
-                acc = fmaf(ldf(dy, t * d + c, bf16), E[static_cast<int64_t>(r) * d + c], acc);
-        dG[j] = warp_sum(acc) + gimp[e];
-        sGdG = fmaf(G[s], dG[j], sGdG);
+    }
+    for (int c = lane; c < d; c += 32) {
+        const float dv = ldf(dy, t * d + c, bf16);
+        const float xv = eps ? ldf(x, t * d + c, bf16) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+            if (j >= k) break;
+            if (row[j] >= 0) aE[j] = fmaf(dv, ldf(E, static_cast<int64_t>(row[j]) * d + c, ebf16), aE[j]);
+            if (eps) aR[j] = fmaf(xv, WnT[static_cast<int64_t>(ex[j]) * d + c], aR[j]);
+        }
+    }
+    float dG[KM], dH[KM], drv[KM];
+    float sGdG = 0.0f;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        if (j >= k) break;
+        dG[j] = warp_sum(aE[j]) + gimp[ex[j]];
+        sGdG = fmaf(G[t * k + j], dG[j], sGdG);
     }
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_K; ++j) {
+    for (int j = 0; j < KM; ++j) {
         if (j >= k) break;
         const int64_t s = t * k + j;
         dH[j] = G[s] * (dG[j] - sGdG);
         float dv = 0.0f;
         if (eps) {
-            float acc = 0.0f;
-            for (int c = lane; c < d; c += 32)
-                acc = fmaf(ldf(x, t * d + c, bf16), WnT[static_cast<int64_t>(ex[j]) * d + c], acc);
-            const float r = warp_sum(acc);
+            const float r = warp_sum(aR[j]);
             dv = dH[j] * eps[t * n + ex[j]] / (1.0f + __expf(-r));
         }
         drv[j] = dv;
@@ -453,46 +539,140 @@ __global__ void __launch_bounds__(256) bwd_token(
     for (int c = lane; c < d; c += 32) {
         float acc = 0.0f;
 #pragma unroll
-        for (int j = 0; j < MOE_MAX_K; ++j) {
+        for (int j = 0; j < KM; ++j) {
             if (j >= k) break;
             const int64_t we = static_cast<int64_t>(ex[j]) * d + c;
             acc = fmaf(dH[j], WgT[we], acc);
             if (eps) acc = fmaf(drv[j], WnT[we], acc);
-            if (row[j] >= 0) acc += dXs[static_cast<int64_t>(row[j]) * d + c];
+            if (row[j] >= 0) acc += ldf(dXs, static_cast<int64_t>(row[j]) * d + c, ebf16);
         }
         dx[t * d + c] = acc;
     }
 }
 
-// dWg[q, e] = sum over e's rows of x[t, q] dc[s]; the same with dr for dWn;
-// dbg[e] = sum of dc.  One thread per input column q, rows in order.
-__global__ void __launch_bounds__(256) bwd_gate_wgrad(
-    int d, int n, int k, int64_t S, const void *__restrict__ x, int bf16,
-    const int32_t *__restrict__ perm, const int32_t *__restrict__ offsets,
-    const float *__restrict__ dc, const float *__restrict__ dr, float *__restrict__ dWg,
-    float *__restrict__ dWn, float *__restrict__ dbg, int32_t *err) {
+// Launches the token kernel with 4 accumulators per lane when k <= 4.
+cudaError_t launch_token(int64_t T, int d, int n, int k, const void *x, const void *dy, int bf16,
+                         const void *E, const void *dXs, int ebf16, const int32_t *inv,
+                         const int32_t *idx, const float *G, const float *gimp, const float *WgT,
+                         const float *WnT, const float *eps, float *dc, float *dr, float *dx,
+                         int32_t *err, cudaStream_t st) {
+    const unsigned grid = static_cast<unsigned>((T + 7) / 8);
+    if (k <= 4)
+        bwd_token<4><<<grid, 256, 0, st>>>(T, d, n, k, x, dy, bf16, E, dXs, ebf16, inv, idx, G, gimp,
+                                           WgT, WnT, eps, dc, dr, dx, err);
+    else
+        bwd_token<MOE_MAX_K><<<grid, 256, 0, st>>>(T, d, n, k, x, dy, bf16, E, dXs, ebf16, inv, idx, G,
+                                                   gimp, WgT, WnT, eps, dc, dr, dx, err);
+    return cudaGetLastError();
+}
+
+
+// Gate weight gradients, in the same two passes: per chunk c of one expert's
+// rows, pg[c, q] = sum of x[t, q] dc[s], pn[c, q] = sum of x[t, q] dr[s] and
+// pb[c] = sum of dc[s] (rows in order; one thread per input column q) ...
+__global__ void __launch_bounds__(256) bwd_gate_part(
+    int d, int k, int64_t S, const void *__restrict__ x, int bf16, const int32_t *__restrict__ perm,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ ctiles, int n,
+    const float *__restrict__ dc, const float *__restrict__ dr, float *__restrict__ pg,
+    float *__restrict__ pn, float *__restrict__ pb, int32_t *err) {
+    __shared__ int64_t trow[kChunkRows];
+    __shared__ float gdc[kChunkRows], gdr[kChunkRows];
+    int r0, r1;
+    if (!chunk_rows(ctiles, offsets, n, blockIdx.x, &r0, &r1)) return;
+    const int cnt = r1 - r0;
+    if (threadIdx.x < cnt) {
+        const int r = r0 + threadIdx.x;
+        const int32_t sl = perm[r];
+        if (sl < 0 || sl >= S) {
+            if (blockIdx.y == 0) report(err, MOE_ERR_DEVICE, kSiteBwdPerm, r);
+            trow[threadIdx.x] = -1;
+            gdc[threadIdx.x] = 0.0f;
+            gdr[threadIdx.x] = 0.0f;
+        } else {
+            trow[threadIdx.x] = sl / k;
+            gdc[threadIdx.x] = dc[sl];
+            gdr[threadIdx.x] = dr[sl];
+        }
+    }
+    __syncthreads();
+    const int64_t c = blockIdx.x;
+    if (blockIdx.y == 0 && threadIdx.x == 0) {
+        float ab = 0.0f;
+        for (int i = 0; i < cnt; ++i) ab += gdc[i];
+        pb[c] = ab;
+    }
+    const int q = blockIdx.y * 256 + threadIdx.x;
+    if (q >= d) return;
+    float ag = 0.0f, an = 0.0f;
+#pragma unroll 8
+    for (int i = 0; i < cnt; ++i) {
+        const int64_t t = trow[i];
+        if (t < 0) continue;
+        const float xv = ldf(x, t * d + q, bf16);
+        ag = fmaf(xv, gdc[i], ag);
+        an = fmaf(xv, gdr[i], an);
+    }
+    pg[c * d + q] = ag;
+    pn[c * d + q] = an;
+}
+
+// ... then dWg[q, e], dWn[q, e], dbg[e] = the sums over e's chunks in order.
+__global__ void __launch_bounds__(256) bwd_gate_fin(int d, int n, const int32_t *__restrict__ ctiles,
+                                                    const float *__restrict__ pg,
+                                                    const float *__restrict__ pn,
+                                                    const float *__restrict__ pb,
+                                                    float *__restrict__ dWg, float *__restrict__ dWn,
+                                                    float *__restrict__ dbg) {
     const int e = blockIdx.y;
     const int q = blockIdx.x * 256 + threadIdx.x;
-    float ag = 0.0f, an = 0.0f, ab = 0.0f;
-    for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
-        const int32_t s = perm[r];
-        if (s < 0 || s >= S) {
-            if (q == 0) report(err, MOE_ERR_DEVICE, kSiteBwdPerm, r);
-            continue;
-        }
-        const float g = dc[s];
-        ab += g;
-        if (q < d) {
-            const float xv = ldf(x, static_cast<int64_t>(s / k) * d + q, bf16);
-            ag = fmaf(xv, g, ag);
-            an = fmaf(xv, dr[s], an);
-        }
+    const int c0 = ctiles[e], c1 = ctiles[e + 1];
+    if (dbg && blockIdx.x == 0 && threadIdx.x == 0) {
+        float ab = 0.0f;
+        for (int c = c0; c < c1; ++c) ab += pb[c];
+        dbg[e] = ab;
     }
-    if (q < d) {
-        dWg[static_cast<int64_t>(q) * n + e] = ag;
-        if (dWn) dWn[static_cast<int64_t>(q) * n + e] = an;
+    if (q >= d) return;
+    float ag = 0.0f, an = 0.0f;
+    for (int c = c0; c < c1; ++c) {
+        ag += pg[static_cast<int64_t>(c) * d + q];
+        an += pn[static_cast<int64_t>(c) * d + q];
     }
-    if (dbg && blockIdx.x == 0 && threadIdx.x == 0) dbg[e] = ab;
+    dWg[static_cast<int64_t>(q) * n + e] = ag;
+    if (dWn) dWn[static_cast<int64_t>(q) * n + e] = an;
+}
+
+// Chunk table, gate gradients and bias sums (both paths): the chunked row
+// sums of dc/dr into dWg, dWn, dbg, of dE into db2 and of dz into db1.
+struct RowSums {
+    int32_t *ctiles;
+    float *pg, *pn, *pb, *pc;
+};
+
+cudaError_t row_sums(const moe_shape &s, const RowSums &R, const int32_t *offsets,
+                     const int32_t *perm, const void *x, int bf16, const float *dc, const float *dr,
+                     float *dWg, float *dWn, float *dbg, const RowOp &dE_op, float *db2,
+                     const RowOp &dz_op, float *db1, int32_t *err, cudaStream_t st) {
+    const int64_t S = slots(s);
+    const int n = s.n, d = s.d, h = s.h;
+    const unsigned chunks = static_cast<unsigned>((S + kChunkRows - 1) / kChunkRows + n);
+    cudaError_t e = launch_row_tiles(offsets, n, kChunkRows, R.ctiles, st);
+    if (e != cudaSuccess) return e;
+    bwd_gate_part<<<dim3(chunks, (d + 255) / 256), 256, 0, st>>>(d, s.k, S, x, bf16, perm, offsets,
+                                                                 R.ctiles, n, dc, dr, R.pg, R.pn,
+                                                                 R.pb, err);
+    bwd_gate_fin<<<dim3((d + 255) / 256, n), 256, 0, st>>>(d, n, R.ctiles, R.pg, R.pn, R.pb, dWg, dWn,
+                                                           dbg);
+    if (db2) {
+        bwd_colsum_part<<<dim3(chunks, (d + 255) / 256), 256, 0, st>>>(dE_op, d, offsets, R.ctiles, n,
+                                                                       S, R.pc, err);
+        bwd_colsum_fin<<<dim3((d + 255) / 256, n), 256, 0, st>>>(R.pc, d, R.ctiles, db2);
+    }
+    if (db1) {
+        bwd_colsum_part<<<dim3(chunks, (h + 255) / 256), 256, 0, st>>>(dz_op, h, offsets, R.ctiles, n,
+                                                                       S, R.pc, err);
+        bwd_colsum_fin<<<dim3((h + 255) / 256, n), 256, 0, st>>>(R.pc, h, R.ctiles, db1);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t row_gemm(const RowGemm &g, int64_t S, int n, cudaStream_t st) {
@@ -503,7 +683,139 @@ cudaError_t row_gemm(const RowGemm &g, int64_t S, int n, cudaStream_t st) {
 
 }  // namespace
 
-size_t backward_workspace_bytes(const moe_shape &s) { return bwd_layout(s).total; }
+// --- tensor-core path (bf16) -------------------------------------------------
+// The forward's workspace comes first (routing, x rows in expert order,
+// hidden activations a = ReLU(z) and expert outputs E, all bf16, from a
+// recompute of the expert stage); then:
+//   W1T, W2T  the experts' weights transposed ([n, d, h] and [n, h, d])
+//   dE        [S, d] rows G dy in expert order;  dA -> dZ [S, h];  dXs [S, d]
+//   kblk      64-row blocks per expert (tile table), the k-blocks of the
+//             weight-gradient contractions
+//   PdE, Pa, PdZ, Px  dE, a, dZ, x rows transposed and padded ([M, Kcap])
+//   WgT, WnT, gimp, dc, dr  as in the CUDA-core path
+struct BtLayout {
+    WsLayout fwd;
+    int64_t Kcap = 0;
+    size_t W1T = 0, W2T = 0, dE = 0, dA = 0, dXs = 0, kblk = 0, PdE = 0, Pa = 0, PdZ = 0, Px = 0;
+    size_t WgT = 0, WnT = 0, gimp = 0, dc = 0, dr = 0;
+    size_t ctiles = 0, pg = 0, pn = 0, pb = 0, pc = 0;
+    size_t total = 0;
+};
+
+bool backward_tc_supported(const moe_shape &s) {
+    return s.dtype == MOE_BF16 && s.groups == 0 && s.d % 128 == 0 && s.h % 128 == 0;
+}
+
+BtLayout bt_layout(const moe_shape &s) {
+    BtLayout L;
+    L.fwd = ws_layout(s);
+    const size_t S = static_cast<size_t>(slots(s));
+    const size_t n = static_cast<size_t>(s.n), d = static_cast<size_t>(s.d),
+                 h = static_cast<size_t>(s.h);
+    L.Kcap = 64 * (static_cast<int64_t>((S + 63) / 64) + s.n);
+    const size_t K = static_cast<size_t>(L.Kcap);
+    size_t o = L.fwd.total;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.W1T = take(n * d * h * 2);
+    L.W2T = take(n * d * h * 2);
+    L.dE = take(S * d * 2);
+    L.dA = take(S * h * 2);
+    L.dXs = take(S * d * 2);
+    L.kblk = take((n + 1) * 4);
+    L.PdE = take(d * K * 2);
+    L.Pa = take(h * K * 2);
+    L.PdZ = take(h * K * 2);
+    L.Px = take(d * K * 2);
+    L.WgT = take(n * d * 4);
+    L.WnT = take(n * d * 4);
+    L.gimp = take(n * 4);
+    L.dc = take(S * 4);
+    L.dr = take(S * 4);
+    const size_t C = row_chunks(s);
+    L.ctiles = take((n + 1) * 4);
+    L.pg = take(C * d * 4);
+    L.pn = take(C * d * 4);
+    L.pb = take(C * 4);
+    L.pc = take(C * (d > h ? d : h) * 4);
+    L.total = o;
+    return L;
+}
+
+cudaError_t launch_backward_tc(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
+                               const float *eps, const void *W1, const float *b1, const void *W2,
+                               const float *b2, const int32_t *idx, const float *G,
+                               const float *importance, const void *dy, float w_imp, float *dx,
+                               float *dWg, float *dWn, float *dbg, float *dW1, float *db1,
+                               float *dW2, float *db2, void *ws, cudaStream_t st) {
+    const BtLayout B = bt_layout(s);
+    const WsLayout &L = B.fwd;
+    const int64_t S = slots(s);
+    const int n = s.n, d = s.d, h = s.h, k = s.k;
+    int32_t *err = ws_ptr<int32_t>(ws, 0);
+    int32_t *offsets = ws_ptr<int32_t>(ws, L.offsets);
+    int32_t *perm = ws_ptr<int32_t>(ws, L.perm);
+    int32_t *inv = ws_ptr<int32_t>(ws, L.inv_perm);
+    const int32_t *tiles = ws_ptr<int32_t>(ws, L.tiles);  // 128-row blocks, from the recompute
+    auto bf = [&](size_t off) { return ws_ptr<__nv_bfloat16>(ws, off); };
+    __nv_bfloat16 *xperm = bf(L.xperm), *hid = bf(L.hidden), *E = bf(L.yslot);
+    __nv_bfloat16 *W1T = bf(B.W1T), *W2T = bf(B.W2T), *dE = bf(B.dE), *dZ = bf(B.dA), *dXs = bf(B.dXs);
+    int32_t *kblk = ws_ptr<int32_t>(ws, B.kblk);
+    float *WgT = ws_ptr<float>(ws, B.WgT), *WnT = ws_ptr<float>(ws, B.WnT);
+    float *gimp = ws_ptr<float>(ws, B.gimp), *dc = ws_ptr<float>(ws, B.dc), *dr = ws_ptr<float>(ws, B.dr);
+    const float *eps_used = s.noisy ? eps : nullptr;
+    float *dWn_used = s.noisy ? dWn : nullptr;
+    if (!s.noisy && dWn) cudaMemsetAsync(dWn, 0, sizeof(float) * d * n, st);
+
+    cudaError_t e = launch_dispatch(s, idx, G, ws_ptr<int32_t>(ws, L.counts), offsets, perm, inv,
+                                    ws_ptr<float>(ws, L.importance), ws_ptr<float>(ws, L.cv2), ws,
+                                    L, st);
+    // recompute x rows, a = ReLU(x W1^T + b1) and E = a W2^T + b2 (bf16, expert order)
+    if (e == cudaSuccess) e = launch_expert_ffn(s, x, perm, offsets, W1, b1, W2, b2, E, ws, L, st);
+    if (e == cudaSuccess)
+        e = launch_transpose_experts(static_cast<const __nv_bfloat16 *>(W2), n, d, h, W2T, st);
+    if (e == cudaSuccess)
+        e = launch_transpose_experts(static_cast<const __nv_bfloat16 *>(W1), n, h, d, W1T, st);
+    if (e == cudaSuccess)
+        e = launch_rows_scaled(static_cast<const __nv_bfloat16 *>(dy), G, perm, S, d, k, dE, err, st);
+    // dA = dE W2 (B = W2^T rows, K = d), then dZ = dA * [a > 0];  dXs = dZ W1 (B = W1^T rows, K = h)
+    if (e == cudaSuccess)
+        e = launch_grouped_gemm_tc(s, dE, d, W2T, h, nullptr, 0, offsets, tiles, dZ, err, st);
+    if (e == cudaSuccess) e = launch_relu_mask(dZ, hid, S * static_cast<int64_t>(h), st);
+    if (e == cudaSuccess)
+        e = launch_grouped_gemm_tc(s, dZ, h, W1T, d, nullptr, 0, offsets, tiles, dXs, err, st);
+    // weight gradients: rows as the contraction axis, transposed and padded per expert
+    if (e == cudaSuccess) e = launch_row_tiles(offsets, n, 64, kblk, st);
+    if (e == cudaSuccess) e = launch_transpose_pad(dE, d, offsets, kblk, n, S, B.Kcap, bf(B.PdE), st);
+    if (e == cudaSuccess) e = launch_transpose_pad(hid, h, offsets, kblk, n, S, B.Kcap, bf(B.Pa), st);
+    if (e == cudaSuccess) e = launch_transpose_pad(dZ, h, offsets, kblk, n, S, B.Kcap, bf(B.PdZ), st);
+    if (e == cudaSuccess) e = launch_transpose_pad(xperm, d, offsets, kblk, n, S, B.Kcap, bf(B.Px), st);
+    if (e == cudaSuccess) e = launch_wgrad_tc(bf(B.PdE), d, bf(B.Pa), h, B.Kcap, kblk, n, dW2, err, st);
+    if (e == cudaSuccess) e = launch_wgrad_tc(bf(B.PdZ), h, bf(B.Px), d, B.Kcap, kblk, n, dW1, err, st);
+    if (e != cudaSuccess) return e;
+
+    // gate side and the sums over rows, on the CUDA cores
+    bwd_transpose<<<dim3((n + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wg, d, n, WgT);
+    if (eps_used)
+        bwd_transpose<<<dim3((n + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wn, d, n, WnT);
+    bwd_gimp<<<1, 256, 0, st>>>(w_imp != 0.0f ? importance : nullptr, n, w_imp, gimp);
+    if ((e = launch_token(s.T, d, n, k, x, dy, 1, E, dXs, 1, inv, idx, G, gimp, WgT, WnT, eps_used,
+                          dc, dr, dx, err, st)) != cudaSuccess)
+        return e;
+    const RowOp dE_op{dy, 1, d, perm, k, G, 0};
+    const RowOp dz_op{dZ, 1, h, nullptr, 1, nullptr, 0};
+    const RowSums R{ws_ptr<int32_t>(ws, B.ctiles), ws_ptr<float>(ws, B.pg), ws_ptr<float>(ws, B.pn),
+                    ws_ptr<float>(ws, B.pb), ws_ptr<float>(ws, B.pc)};
+    return row_sums(s, R, offsets, perm, x, 1, dc, dr, dWg, dWn_used, dbg, dE_op, db2, dz_op, db1, err,
+                    st);
+}
+
+size_t backward_workspace_bytes(const moe_shape &s) {
+    return backward_tc_supported(s) ? bt_layout(s).total : bwd_layout(s).total;
+}
 
 namespace {
 
@@ -597,10 +909,10 @@ cudaError_t launch_backward(const moe_shape &s, const void *x, const float *Wg, 
     if (eps_used)
         bwd_transpose<<<dim3((n + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wn, d, n, WnT);
     bwd_gimp<<<1, 256, 0, st>>>(w_imp != 0.0f ? importance : nullptr, n, w_imp, gimp);
-    bwd_token<<<static_cast<unsigned>((s.T + 7) / 8), 256, 0, st>>>(
-        s.T, d, n, k, x, dy, bf16, E, dXs, inv, idx, G, gimp, WgT, WnT, eps_used, dc, dr, dx, err);
-    bwd_gate_wgrad<<<dim3((d + 255) / 256, n), 256, 0, st>>>(d, n, k, S, x, bf16, perm, offsets, dc,
-                                                             dr, dWg, dWn_used, dbg, err);
+    if ((e = launch_token(s.T, d, n, k, x, dy, bf16, E, dXs, 0, inv, idx, G, gimp, WgT, WnT,
+                          eps_used, dc, dr, dx, err, st)) != cudaSuccess)
+        return e;
+
     // dW2[e] = sum dE a^T  (M = d, N = h),  dW1[e] = sum dz x^T  (M = h, N = d)
     const RowOp dE_op{dy, bf16, d, perm, k, G, 0};
     const RowOp a_op{Z, 0, h, nullptr, 1, nullptr, 1};
@@ -608,9 +920,10 @@ cudaError_t launch_backward(const moe_shape &s, const void *x, const float *Wg, 
     const RowOp x_op{x, bf16, d, perm, k, nullptr, 0};
     bwd_wgrad<<<dim3(h / kBT, d / kBT, n), 256, 0, st>>>(dE_op, a_op, d, h, offsets, S, dW2, err);
     bwd_wgrad<<<dim3(d / kBT, h / kBT, n), 256, 0, st>>>(dz_op, x_op, h, d, offsets, S, dW1, err);
-    if (db2) bwd_colsum<<<dim3((d + 255) / 256, n), 256, 0, st>>>(dE_op, d, offsets, S, db2, err);
-    if (db1) bwd_colsum<<<dim3((h + 255) / 256, n), 256, 0, st>>>(dz_op, h, offsets, S, db1, err);
-    return cudaGetLastError();
+    const RowSums R{ws_ptr<int32_t>(ws, B.ctiles), ws_ptr<float>(ws, B.pg), ws_ptr<float>(ws, B.pn),
+                    ws_ptr<float>(ws, B.pb), ws_ptr<float>(ws, B.pc)};
+    return row_sums(s, R, offsets, perm, x, bf16, dc, dr, dWg, dWn_used, dbg, dE_op, db2, dz_op, db1,
+                    err, st);
 }
 
 }  // namespace
@@ -664,9 +977,9 @@ moe_status moe_backward(const moe_shape *s, const void *x, const float *Wg, cons
         if (db2) cudaMemsetAsync(db2, 0, sizeof(float) * n * d, st);
         return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     }
-    const cudaError_t e = launch_backward(*s, x, Wg, Wnoise, eps, W1, b1, W2, b2, idx, G, importance,
-                                          dy, w_importance, dx, dWg, dWnoise, dbg, dW1, db1, dW2,
-                                          db2, ws, st);
+    const auto run = backward_tc_supported(*s) ? launch_backward_tc : launch_backward;
+    const cudaError_t e = run(*s, x, Wg, Wnoise, eps, W1, b1, W2, b2, idx, G, importance, dy,
+                              w_importance, dx, dWg, dWnoise, dbg, dW1, db1, dW2, db2, ws, st);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
