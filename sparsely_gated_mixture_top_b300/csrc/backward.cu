@@ -502,6 +502,7 @@ __global__ void __launch_bounds__(256) bwd_token(
         ex[j] = e;
         row[j] = r;
     }
+#pragma unroll 4
     for (int c = lane; c < d; c += 32) {
         const float dv = ldf(dy, t * d + c, bf16);
         const float xv = eps ? ldf(x, t * d + c, bf16) : 0.0f;
@@ -536,6 +537,7 @@ __global__ void __launch_bounds__(256) bwd_token(
             dr[s] = dv;
         }
     }
+#pragma unroll 4
     for (int c = lane; c < d; c += 32) {
         float acc = 0.0f;
 #pragma unroll
