@@ -552,6 +552,129 @@ __global__ void __launch_bounds__(256) bwd_token(
     }
 }
 
+// The token kernel for bf16 x, dy, E and dX rows with d a multiple of 256:
+// each lane takes 8 consecutive columns per step (16-byte loads of bf16 rows,
+// 32-byte loads of the fp32 gate columns, two 16-byte stores of dx).
+__device__ __forceinline__ void bf16x8(const __nv_bfloat16 *p, float (&f)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+        f[2 * i] = __low2float(b);
+        f[2 * i + 1] = __high2float(b);
+    }
+}
+
+__device__ __forceinline__ void f32x8(const float *p, float (&f)[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+}
+
+template <int KM>
+__global__ void __launch_bounds__(256) bwd_token_v8(
+    int64_t T, int d, int n, int k, const __nv_bfloat16 *__restrict__ x,
+    const __nv_bfloat16 *__restrict__ dy, const __nv_bfloat16 *__restrict__ E,
+    const __nv_bfloat16 *__restrict__ dXs, const int32_t *__restrict__ inv_perm,
+    const int32_t *__restrict__ idx, const float *__restrict__ G, const float *__restrict__ gimp,
+    const float *__restrict__ WgT, const float *__restrict__ WnT, const float *__restrict__ eps,
+    float *__restrict__ dc, float *__restrict__ dr, float *__restrict__ dx, int32_t *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+    if (t >= T) return;
+    const int64_t S = T * k;
+    int ex[KM], row[KM];
+    float aE[KM], aR[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        ex[j] = 0;
+        row[j] = -1;
+        aE[j] = 0.0f;
+        aR[j] = 0.0f;
+        if (j >= k) continue;
+        const int64_t s = t * k + j;
+        const int e = idx[s];
+        const int r = inv_perm[s];
+        if (e < 0 || e >= n || r < 0 || r >= S) {
+            if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteBwdPerm, static_cast<int32_t>(s));
+            continue;
+        }
+        ex[j] = e;
+        row[j] = r;
+    }
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+        float dv[8], xv[8];
+        bf16x8(dy + t * d + c0, dv);
+        if (eps) bf16x8(x + t * d + c0, xv);
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+            if (j >= k) break;
+            if (row[j] >= 0) {
+                float ev[8];
+                bf16x8(E + static_cast<int64_t>(row[j]) * d + c0, ev);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) aE[j] = fmaf(dv[i], ev[i], aE[j]);
+            }
+            if (eps) {
+                float wv[8];
+                f32x8(WnT + static_cast<int64_t>(ex[j]) * d + c0, wv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) aR[j] = fmaf(xv[i], wv[i], aR[j]);
+            }
+        }
+    }
+    float dG[KM], dH[KM], drv[KM];
+    float sGdG = 0.0f;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        if (j >= k) break;
+        dG[j] = warp_sum(aE[j]) + gimp[ex[j]];
+        sGdG = fmaf(G[t * k + j], dG[j], sGdG);
+    }
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        if (j >= k) break;
+        const int64_t s = t * k + j;
+        dH[j] = G[s] * (dG[j] - sGdG);
+        float dv = 0.0f;
+        if (eps) {
+            const float r = warp_sum(aR[j]);
+            dv = dH[j] * eps[t * n + ex[j]] / (1.0f + __expf(-r));
+        }
+        drv[j] = dv;
+        if (lane == 0) {
+            dc[s] = dH[j];
+            dr[s] = dv;
+        }
+    }
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+        float acc[8] = {};
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+            if (j >= k) break;
+            float wg[8];
+            f32x8(WgT + static_cast<int64_t>(ex[j]) * d + c0, wg);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(dH[j], wg[i], acc[i]);
+            if (eps) {
+                float wn[8];
+                f32x8(WnT + static_cast<int64_t>(ex[j]) * d + c0, wn);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(drv[j], wn[i], acc[i]);
+            }
+            if (row[j] >= 0) {
+                float xr[8];
+                bf16x8(dXs + static_cast<int64_t>(row[j]) * d + c0, xr);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] += xr[i];
+            }
+        }
+        float4 *o = reinterpret_cast<float4 *>(dx + t * d + c0);
+        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+}
+
 // Launches the token kernel with 4 accumulators per lane when k <= 4.
 cudaError_t launch_token(int64_t T, int d, int n, int k, const void *x, const void *dy, int bf16,
                          const void *E, const void *dXs, int ebf16, const int32_t *inv,
@@ -559,6 +682,18 @@ cudaError_t launch_token(int64_t T, int d, int n, int k, const void *x, const vo
                          const float *WnT, const float *eps, float *dc, float *dr, float *dx,
                          int32_t *err, cudaStream_t st) {
     const unsigned grid = static_cast<unsigned>((T + 7) / 8);
+    if (bf16 && ebf16 && d % 256 == 0) {
+        using bf = __nv_bfloat16;
+        const bf *xb = static_cast<const bf *>(x), *dyb = static_cast<const bf *>(dy);
+        const bf *Eb = static_cast<const bf *>(E), *Xb = static_cast<const bf *>(dXs);
+        if (k <= 4)
+            bwd_token_v8<4><<<grid, 256, 0, st>>>(T, d, n, k, xb, dyb, Eb, Xb, inv, idx, G, gimp, WgT,
+                                                  WnT, eps, dc, dr, dx, err);
+        else
+            bwd_token_v8<MOE_MAX_K><<<grid, 256, 0, st>>>(T, d, n, k, xb, dyb, Eb, Xb, inv, idx, G,
+                                                          gimp, WgT, WnT, eps, dc, dr, dx, err);
+        return cudaGetLastError();
+    }
     if (k <= 4)
         bwd_token<4><<<grid, 256, 0, st>>>(T, d, n, k, x, dy, bf16, E, dXs, ebf16, inv, idx, G, gimp,
                                            WgT, WnT, eps, dc, dr, dx, err);

@@ -9,7 +9,9 @@
 //                   earlier slots of its chunk with the same expert (warp
 //                   __match_any + warps taken in order), the chunk's
 //                   per-expert counts and gate-weight sums (each warp's group
-//                   of <= 32 slots in fp32, the groups in fp64, slot order)
+//                   of <= 32 slots in fp32, the groups in fp64, slot order);
+//                   route_rank_warps gives the same for n <= 512 from a
+//                   [warp][expert] table instead of 32 barrier rounds
 //   route_colscan   per expert, an exclusive scan of the counts down the
 //                   chunks (chunk bases), the expert's count and its
 //                   importance (chunk partials summed in chunk order)
@@ -89,6 +91,72 @@ __global__ void __launch_bounds__(1024) route_rank(const int32_t *__restrict__ i
 // Block (32 x 32): 32 experts (x) by 32 chunk segments (y).  Chunk counts
 // become chunk bases (exclusive scan down the chunks); the expert's count
 // and importance (fp64, chunk order) are the column totals.
+// route_rank for n <= kRankWarpsMaxN: the same outputs without the 32
+// barrier rounds.  Each warp's leaders write their group's count and fp32
+// gate-weight sum to a [32 warps][n] table; one thread per expert then walks
+// the warps in order (exclusive scan of the counts, fp64 sum of the groups,
+// the same order as route_rank) and every slot reads its warp's base.
+constexpr int kRankWarpsMaxN = 512;
+
+__global__ void __launch_bounds__(1024) route_rank_warps(const int32_t *__restrict__ idx,
+                                                         const float *__restrict__ G, int64_t S,
+                                                         int n, int32_t *__restrict__ local_rank,
+                                                         int32_t *__restrict__ chunk,
+                                                         double *__restrict__ chunk_imp,
+                                                         int32_t *err) {
+    extern __shared__ __align__(8) unsigned char route_sh[];
+    int32_t *wc = reinterpret_cast<int32_t *>(route_sh);           // [32][n] counts, then bases
+    float *wsum = reinterpret_cast<float *>(route_sh + 128 * n);    // [32][n] group sums
+    for (int i = threadIdx.x; i < 32 * n; i += blockDim.x) {
+        wc[i] = 0;
+        wsum[i] = 0.0f;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t s = static_cast<int64_t>(blockIdx.x) * kRouteChunk + threadIdx.x;
+    int e = -1;
+    float g = 0.0f;
+    if (s < S) {
+        e = idx[s];
+        if (e < 0 || e >= n) {
+            report(err, MOE_ERR_DEVICE, kSiteRouteIdx, static_cast<int32_t>(s));
+            e = -1;
+        } else {
+            g = G[s];
+        }
+    }
+    const unsigned mask = __match_any_sync(0xffffffffu, e);
+    const int leader = __ffs(mask) - 1;
+    const int rank_in_warp = __popc(mask & ((1u << lane) - 1u));
+    float seg = 0.0f;
+#pragma unroll
+    for (int src = 0; src < 32; ++src) {
+        const float v = __shfl_sync(0xffffffffu, g, src);
+        if ((mask >> src) & 1u) seg += v;
+    }
+    if (lane == leader && e >= 0) {
+        wc[warp * n + e] = __popc(mask);
+        wsum[warp * n + e] = seg;
+    }
+    __syncthreads();
+    int32_t *row = chunk + static_cast<int64_t>(blockIdx.x) * n;
+    double *irow = chunk_imp + static_cast<int64_t>(blockIdx.x) * n;
+    for (int ee = threadIdx.x; ee < n; ee += blockDim.x) {
+        int32_t run = 0;
+        double imp = 0.0;
+        for (int w = 0; w < 32; ++w) {
+            const int32_t c = wc[w * n + ee];
+            wc[w * n + ee] = run;
+            run += c;
+            if (c) imp += static_cast<double>(wsum[w * n + ee]);
+        }
+        row[ee] = run;
+        irow[ee] = imp;
+    }
+    __syncthreads();
+    if (e >= 0) local_rank[s] = wc[warp * n + e] + rank_in_warp;
+}
+
 __global__ void __launch_bounds__(1024) route_colscan(int32_t *__restrict__ chunk,
                                                       const double *__restrict__ chunk_imp,
                                                       int chunks, int n, int32_t *__restrict__ counts,
@@ -245,7 +313,20 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
             opted_in = smem;
         }
     }
-    route_rank<<<chunks, 1024, smem, st>>>(idx, G, S, n, local_rank, chunk, chunk_imp, err);
+    if (n <= kRankWarpsMaxN) {
+        // 256 * n bytes of tables (128 KB at most), opted in once
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [] {
+            attr_err = cudaFuncSetAttribute(route_rank_warps, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            256 * kRankWarpsMaxN);
+        });
+        if (attr_err != cudaSuccess) return attr_err;
+        route_rank_warps<<<chunks, 1024, 256 * static_cast<size_t>(n), st>>>(idx, G, S, n, local_rank,
+                                                                           chunk, chunk_imp, err);
+    } else {
+        route_rank<<<chunks, 1024, smem, st>>>(idx, G, S, n, local_rank, chunk, chunk_imp, err);
+    }
     route_colscan<<<(n + 31) / 32, dim3(32, 32), 0, st>>>(chunk, chunk_imp, chunks, n, counts, imp64);
     route_finish<<<1, 256, 0, st>>>(counts, imp64, n, offsets, importance, cv2);
     route_scatter<<<static_cast<unsigned>((S + 255) / 256), 256, 0, st>>>(

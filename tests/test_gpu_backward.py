@@ -47,6 +47,7 @@ CASES = [
     (W("bwd_tc_noise_off", T=300, d=128, h=256, n=6, k=2, noisy=False, seed=53), 0.5),
     (W("bwd_tc_k16", T=200, d=128, h=128, n=20, k=16, seed=54), 0.0),
     (W("bwd_tc_wide_experts", T=700, d=512, h=1024, n=3, k=1, bias_std=0.1, seed=55), 0.4),
+    (W("bwd_tc_k8", T=200, d=256, h=256, n=20, k=8, bias_std=0.1, seed=56), 0.6),
 ]
 
 
