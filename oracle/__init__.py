@@ -56,6 +56,8 @@ def _lib_():
         lib.oracle_combine_rows.restype = i32
         lib.oracle_backward_flat.argtypes = [i64, i32, i32, i32, i32] + [vp] * 10 + [dbl] + [vp] * 10
         lib.oracle_backward_flat.restype = i32
+        lib.oracle_forward_balanced.argtypes = [i64, i32, i32, i32, i32] + [vp] * 13
+        lib.oracle_forward_balanced.restype = i32
         _lib = lib
     return _lib
 
@@ -268,4 +270,22 @@ def backward(x, Wg, Wn, bg, eps, W1, b1, W2, b2, dy, k: int, w_imp: float = 0.0)
         _p(out["dW1"]), _p(out["db1"]), _p(out["dW2"]), _p(out["db2"]), _p(out["idx"]), _p(out["G"]))
     if rc:
         raise ValueError("oracle_backward_flat: bad arguments")
+    return out
+
+
+def forward_balanced(x, Wg, Wn, bg, eps, thr, W1, b1, W2, b2, k: int):
+    """Flat layer with balanced routing: thr None = batchwise mask (every expert
+    keeps the floor(k*T/n) tokens with the largest noisy score), else expert e
+    keeps the tokens whose score exceeds thr[e].  Returns dict(y [T,d],
+    counts [n] int32, W [T,n] the softmax weights over each token's kept
+    experts, 0 elsewhere)."""
+    x, Wg, Wn, bg, eps, thr, W1, b1, W2, b2 = map(_f64, (x, Wg, Wn, bg, eps, thr, W1, b1, W2, b2))
+    T, d = x.shape
+    n, h, _ = W1.shape
+    out = dict(y=np.zeros((T, d)), counts=np.zeros(n, np.int32), W=np.zeros((T, n)))
+    rc = _lib_().oracle_forward_balanced(T, d, h, n, k, _p(x), _p(Wg), _p(Wn), _p(bg), _p(eps),
+                                         _p(thr), _p(W1), _p(b1), _p(W2), _p(b2), _p(out["y"]),
+                                         _p(out["counts"]), _p(out["W"]))
+    if rc:
+        raise ValueError("oracle_forward_balanced: bad arguments")
     return out

@@ -710,3 +710,115 @@ int oracle_backward_flat(int64_t T, int d, int h, int n, int k, const double *x,
     free(gimp);
     return bad ? -1 : 0;
 }
+
+/*
+ * Balanced routing.  "Outrageously Large Neural Networks - 中文验证版", section
+ * 方法适配: in some translation experiments a per-batch mask gives every
+ * expert the same batch size during training, and per-expert thresholds
+ * approximate that behaviour at inference.  The pages give no formula; the
+ * plainest reading, written out here:
+ *   H[t, e]   the noisy score of the flat gate (as in noisy_top_k_gate)
+ *   batchwise (thr == NULL): m = floor(k*T/n); expert e keeps the m tokens
+ *             with the largest H[:, e] (equal scores: the lower token index
+ *             first)
+ *   threshold (thr given):   expert e keeps token t iff H[t, e] > thr[e]
+ *   weights   w[t, e] = softmax of H[t, .] over the experts that kept t
+ *             (KeepTopK replaced by the mask); a token no expert kept has
+ *             y_t = 0
+ *   y[t]      = sum over the kept experts e, in increasing e, of w[t, e] E_e(x_t)
+ * Outputs y [T, d], counts [n] (tokens kept per expert), W [T, n] (the
+ * weights, 0 where not kept; may be NULL).  Returns 0, or -1 on bad arguments.
+ */
+typedef struct {
+    double h;
+    int64_t t;
+} col_entry;
+
+static int by_desc_h_then_token(const void *pa, const void *pb) {
+    const col_entry *a = (const col_entry *)pa, *b = (const col_entry *)pb;
+    if (a->h > b->h) return -1;
+    if (a->h < b->h) return 1;
+    return (a->t > b->t) - (a->t < b->t);
+}
+
+int oracle_forward_balanced(int64_t T, int d, int h, int n, int k, const double *x,
+                            const double *Wg, const double *Wn, const double *bg,
+                            const double *eps, const double *thr, const double *W1,
+                            const double *b1, const double *W2, const double *b2, double *y,
+                            int32_t *counts, double *W) {
+    if (T < 0 || d <= 0 || h <= 0 || n <= 0 || k <= 0 || k > n) return -1;
+    double *H = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * (size_t)n);
+    unsigned char *keep = (unsigned char *)calloc((size_t)(T > 0 ? T : 1) * (size_t)n, 1);
+    if (!H || !keep) return -1;
+    /* noisy scores */
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int e = 0; e < n; ++e) {
+            double c = bg ? bg[e] : 0.0, r = 0.0;
+            for (int j = 0; j < d; ++j) {
+                c += x[t * d + j] * Wg[(int64_t)j * n + e];
+                r += x[t * d + j] * Wn[(int64_t)j * n + e];
+            }
+            H[t * n + e] = eps ? c + eps[t * (int64_t)n + e] * oracle_softplus(r) : c;
+        }
+    }
+    /* the mask */
+    if (thr) {
+        for (int64_t t = 0; t < T; ++t)
+            for (int e = 0; e < n; ++e) keep[t * n + e] = H[t * n + e] > thr[e];
+    } else {
+        const int64_t m = (int64_t)k * T / n;
+        col_entry *col = (col_entry *)malloc(sizeof(col_entry) * (size_t)(T > 0 ? T : 1));
+        if (!col) return -1;
+        for (int e = 0; e < n; ++e) {
+            for (int64_t t = 0; t < T; ++t) {
+                col[t].h = H[t * n + e];
+                col[t].t = t;
+            }
+            qsort(col, (size_t)T, sizeof(col_entry), by_desc_h_then_token);
+            for (int64_t q = 0; q < m; ++q) keep[col[q].t * n + e] = 1;
+        }
+        free(col);
+    }
+    for (int e = 0; e < n; ++e) {
+        int32_t c = 0;
+        for (int64_t t = 0; t < T; ++t) c += keep[t * n + e];
+        counts[e] = c;
+    }
+    /* weights and the experts */
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *a = (double *)malloc(sizeof(double) * (size_t)h);
+        double *E = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!a || !E) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t t = 0; t < T; ++t) {
+                double *yt = y + t * d;
+                for (int o = 0; o < d; ++o) yt[o] = 0.0;
+                double mx = -INFINITY, sum = 0.0;
+                for (int e = 0; e < n; ++e)
+                    if (keep[t * n + e] && H[t * n + e] > mx) mx = H[t * n + e];
+                for (int e = 0; e < n; ++e)
+                    if (keep[t * n + e]) sum += exp(H[t * n + e] - mx);
+                for (int e = 0; e < n; ++e) {
+                    const double w = keep[t * n + e] ? exp(H[t * n + e] - mx) / sum : 0.0;
+                    if (W) W[t * n + e] = w;
+                    if (!keep[t * n + e]) continue;
+                    oracle_expert(d, h, x + t * d, W1 + (int64_t)e * h * d,
+                                  b1 ? b1 + (int64_t)e * h : NULL, W2 + (int64_t)e * d * h,
+                                  b2 ? b2 + (int64_t)e * d : NULL, a, E);
+                    for (int o = 0; o < d; ++o) yt[o] += w * E[o];
+                }
+            }
+        }
+        free(a);
+        free(E);
+    }
+    free(H);
+    free(keep);
+    return bad ? -1 : 0;
+}
