@@ -49,9 +49,11 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target CPU seconds of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--pass", dest="which", choices=["forward", "backward"], default="forward",
+    p.add_argument("--pass", dest="which", choices=["forward", "backward", "balanced"],
+                   default="forward",
                    help="forward: moe_forward (the headline); backward: moe_backward of the flat "
-                        "layer with the forward's selection")
+                        "layer with the forward's selection; balanced: moe_forward_balanced with "
+                        "the batchwise mask")
     p.add_argument("--traffic-summary", nargs=2, metavar=("NCU_CSV", "BENCH_JSON"),
                    help="print the DRAM-traffic record of one expert-FFN stage from an ncu "
                         "--csv log of the stage's launches (TRAFFIC_NCU) and the bench line "
@@ -436,6 +438,66 @@ def backward_arm(args, w: wl.Workload):
     print(json.dumps(line), flush=True)
 
 
+def balanced_arm(args, w: wl.Workload):
+    """Times moe_forward_balanced with the batchwise mask (every expert keeps
+    floor(k*T/n) tokens) on the workload, inputs resident on the device."""
+    from sparsely_gated_mixture_top_b300 import binding as B
+    if w.groups:
+        print(json.dumps({"metric": "MoE-layer balanced-routing tokens/sec", "unavailable":
+                          "balanced routing covers flat gating only"}))
+        return
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    host = wl.make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    s = B.shape_of(w)
+    m = w.k * w.T // w.n
+    cap = w.n * m
+    ws = B.balanced_workspace(s, cap, dev)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    y = torch.empty((w.T, w.d), dtype=dt, device=dev)
+    counts = torch.empty((w.n,), dtype=torch.int32, device=dev)
+
+    def step():
+        B.moe_forward_balanced(s, d["x"], d["Wg"], d["Wn"], d["bg"], d["eps"], None, cap, d["W1"],
+                               d["b1"], d["W2"], d["b2"], y, counts, None, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if B.moe_check(ws, stream) != B.MOE_OK:
+        raise RuntimeError("device error during warm-up")
+    clocks = ClockSampler(0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    status = B.moe_check(ws, stream)
+    if status != B.MOE_OK:
+        raise RuntimeError(f"device error in the timed region: {B.status_string(status)}")
+    ms = e0.elapsed_time(e1) / args.steps
+    alg = algorithmic(w, counts.cpu().numpy())
+    pk = peaks()
+    t_roof = max(alg["layer_bytes"] / (pk["hbm"] * 1e9), alg["flops"] / (pk["bf16"] * 1e12))
+    line = {
+        "metric": "MoE-layer tokens/sec with the batchwise mask (moe_forward_balanced, 1xB300)",
+        "value": w.T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded counter-based normal)",
+        "config": dict(config_of(w), rows_per_expert=m, gate_scores="fp32 CUDA cores"),
+        "layer_roofline": {"t_roof_us": t_roof * 1e6, "t_meas_us": ms * 1e3,
+                           "frac": t_roof / (ms / 1e3), "algorithmic_bytes": alg["layer_bytes"],
+                           "flops": alg["flops"]},
+        "e2e": None, "cpu_baseline": None, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     w = wl.WORKLOADS[args.workload]
@@ -447,6 +509,9 @@ def main():
         return
     if args.which == "backward":
         backward_arm(args, w)
+        return
+    if args.which == "balanced":
+        balanced_arm(args, w)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

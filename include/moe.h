@@ -269,6 +269,34 @@ MOE_API moe_status moe_backward(const moe_shape *shape, const void *x, const flo
                                 float *db2, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * The layer with balanced routing ("Outrageously Large Neural Networks -
+ * 中文验证版", section 方法适配: a per-batch mask gives every expert the same
+ * batch size during training; per-expert thresholds approximate it at
+ * inference).  Flat gating only (MOE_ERR_UNSUPPORTED otherwise).  H = the flat
+ * gate's noisy score, x.Wg (+ bg) + eps * softplus(x.Wnoise), fp32.
+ *   thr == NULL  batchwise mask: expert e keeps the m = floor(k*T/n) tokens
+ *                with the largest H[:, e] (equal scores: the lower token
+ *                index first); rows_cap must be at least n*m.
+ *   thr [n]      thresholds: expert e keeps token t iff H[t, e] > thr[e]; a
+ *                total above rows_cap drops the rows past it and sets
+ *                MOE_ERR_DEVICE.
+ * Weights: softmax of H[t, .] over the experts that kept t.  y[t] = sum over
+ * those experts, in increasing e, of w * E_e(x_t) (0 when none kept t); fp32
+ * accumulation, one rounding to x's dtype.  Outputs: y [T,d], counts [n]
+ * (tokens kept per expert, before any capacity cut), W [T,n] fp32 weights (0
+ * where not kept; may be NULL).  ws: caller-owned, 256-byte aligned, of
+ * moe_balanced_workspace_bytes(shape, rows_cap) bytes; T*n must not exceed
+ * MOE_MAX_SLOTS.
+ */
+MOE_API size_t moe_balanced_workspace_bytes(const moe_shape *shape, int64_t rows_cap);
+MOE_API moe_status moe_forward_balanced(const moe_shape *shape, const void *x, const float *Wg,
+                                        const float *Wnoise, const float *bg, const float *eps,
+                                        const float *thr, int64_t rows_cap, const void *W1,
+                                        const float *b1, const void *W2, const float *b2, void *y,
+                                        int32_t *counts, float *W, void *ws, size_t ws_bytes,
+                                        void *stream);
+
+/*
  * Synchronises `stream`, reads the workspace's device error word, clears it
  * and returns it (MOE_OK when no device error was recorded).  Returns
  * MOE_ERR_CUDA if the stream itself failed.

@@ -30,7 +30,8 @@ MOE_BF16 = 1
 EXPORTS = ("moe_version", "moe_status_string", "moe_validate", "moe_workspace_bytes",
            "moe_workspace_init", "moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine",
            "moe_forward", "moe_check", "moe_dispatch_noalloc", "moe_load_workspace_bytes",
-           "moe_gate_load", "moe_backward_workspace_bytes", "moe_backward")
+           "moe_gate_load", "moe_backward_workspace_bytes", "moe_backward",
+           "moe_balanced_workspace_bytes", "moe_forward_balanced")
 
 
 class MoEShape(ctypes.Structure):
@@ -68,8 +69,12 @@ def _load():
     lib.moe_backward_workspace_bytes.argtypes = [shp]
     lib.moe_backward_workspace_bytes.restype = sz
     lib.moe_backward.argtypes = [shp] + [vp] * 12 + [ctypes.c_float] + [vp] * 9 + [sz, vp]
+    lib.moe_balanced_workspace_bytes.argtypes = [shp, ctypes.c_int64]
+    lib.moe_balanced_workspace_bytes.restype = sz
+    lib.moe_forward_balanced.argtypes = [shp] + [vp] * 6 + [ctypes.c_int64] + [vp] * 8 + [sz, vp]
     for f in ("moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
-              "moe_check", "moe_dispatch_noalloc", "moe_gate_load", "moe_backward"):
+              "moe_check", "moe_dispatch_noalloc", "moe_gate_load", "moe_backward",
+              "moe_forward_balanced"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -235,3 +240,27 @@ def moe_backward(shape, x, Wg, Wn, eps, W1, b1, W2, b2, idx, G, importance, dy, 
         ctypes.byref(shape), _p(x), _p(Wg), _p(Wn), _p(eps), _p(W1), _p(b1), _p(W2), _p(b2),
         _p(idx), _p(G), _p(importance), _p(dy), float(w_importance), _p(dx), _p(dWg), _p(dWn),
         _p(dbg), _p(dW1), _p(db1), _p(dW2), _p(db2), _p(ws), ws.numel(), _stream(stream)))
+
+
+def balanced_workspace_bytes(shape: MoEShape, rows_cap: int) -> int:
+    return lib.moe_balanced_workspace_bytes(ctypes.byref(shape), int(rows_cap))
+
+
+def balanced_workspace(shape: MoEShape, rows_cap: int, device="cuda", stream=None) -> torch.Tensor:
+    """A fresh workspace for moe_forward_balanced with its error word cleared."""
+    nbytes = balanced_workspace_bytes(shape, rows_cap)
+    if nbytes == 0:
+        raise MoEError("moe_balanced_workspace_bytes", validate(shape) or MOE_ERR_UNSUPPORTED)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    _ok("moe_workspace_init", lib.moe_workspace_init(_p(ws), nbytes, _stream(stream)))
+    return ws
+
+
+def moe_forward_balanced(shape, x, Wg, Wn, bg, eps, thr, rows_cap, W1, b1, W2, b2, y, counts, W,
+                         ws, stream=None):
+    """The layer with balanced routing: thr None = batchwise mask (each expert
+    keeps floor(k*T/n) tokens), else per-expert thresholds."""
+    _ok("moe_forward_balanced", lib.moe_forward_balanced(
+        ctypes.byref(shape), _p(x), _p(Wg), _p(Wn), _p(bg), _p(eps), _p(thr), int(rows_cap),
+        _p(W1), _p(b1), _p(W2), _p(b2), _p(y), _p(counts), _p(W), _p(ws), ws.numel(),
+        _stream(stream)))

@@ -130,3 +130,29 @@ def test_backward_rejects_bad_arguments_before_any_launch():
     assert B.backward_workspace_bytes(hier) == 0
     assert call(shape=hier) == B.MOE_ERR_UNSUPPORTED
     assert call(shape=B.make_shape(**dict(GOOD, k=0))) == B.MOE_ERR_INVALID_ARG
+
+
+def test_balanced_rejects_bad_arguments_before_any_launch():
+    s = B.make_shape(**GOOD)                    # T=100, n=16, k=4: m = 25, n*m = 400
+    cap = 400
+    n = B.balanced_workspace_bytes(s, cap)
+    assert n > 0 and n % 256 == 0
+    assert B.balanced_workspace_bytes(s, 2 * cap) > n
+    ok, mis = _fake(1 << 20), _fake((1 << 20) + 8)
+    lib = B.lib
+
+    def call(shape=s, x=ok, Wg=ok, Wn=ok, bg=None, eps=ok, thr=None, rows=cap, W1=ok, W2=ok,
+             y=ok, counts=ok, W=None, ws=ok, nbytes=n):
+        return lib.moe_forward_balanced(ctypes.byref(shape), x, Wg, Wn, bg, eps, thr, rows, W1,
+                                        None, W2, None, y, counts, W, ws, nbytes, None)
+
+    assert call(x=mis) == B.MOE_ERR_INVALID_ARG
+    assert call(counts=None) == B.MOE_ERR_INVALID_ARG
+    assert call(eps=None) == B.MOE_ERR_INVALID_ARG              # noisy shape needs eps
+    assert call(rows=cap - 1, nbytes=B.balanced_workspace_bytes(s, cap - 1)) == B.MOE_ERR_INVALID_ARG
+    assert call(nbytes=n - 256) == B.MOE_ERR_WORKSPACE
+    assert call(ws=mis) == B.MOE_ERR_WORKSPACE
+    assert call(rows=-1) == B.MOE_ERR_UNSUPPORTED
+    hier = B.make_shape(**dict(GOOD, n=16, groups=4, k_groups=2, k=4))
+    assert B.balanced_workspace_bytes(hier, cap) == 0
+    assert call(shape=hier) == B.MOE_ERR_UNSUPPORTED
