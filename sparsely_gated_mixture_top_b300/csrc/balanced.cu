@@ -11,7 +11,10 @@
 //   weights    softmax of H[t, .] over the experts that kept t
 //   y[t]       sum over those experts, in increasing e, of w E_e(x_t); 0 if none
 // Stages, in launch order:
-//   bal_scores        H [T, n] fp32 on the CUDA cores (64 x 64 tiles)
+//   scores            H [T, n]: noisy bf16 shapes from the tensor-core gate's
+//                     load mode (c and softplus(r) per expert, fp32-faithful),
+//                     then bal_noisy_sum; other shapes bal_scores, fp32 on the
+//                     CUDA cores (64 x 64 tiles)
 //   bal_count         per expert: the m-th largest score by a 4-pass 8-bit
 //                     radix select on order-preserving keys, and how many of
 //                     the tied scores to keep (batchwise); or the number of
@@ -39,9 +42,17 @@ struct BalLayout {
     moe_shape ffn;  // the expert stage's shape: one slot per row
     WsLayout fwd;
     size_t H = 0, rowmap = 0, row_token = 0, row_weight = 0, kstar = 0, quota = 0, cnt = 0;
+    size_t sN = 0, gidx = 0, gG = 0, vk = 0;  // tensor-core scores: noise scale, its top-k, k-th
     size_t total = 0;
     int64_t rows = 0;  // row capacity
 };
+
+// Noisy bf16 shapes take the scores from the tensor-core gate, which in its
+// load mode writes the clean score c = x.Wg + bg and the noise scale
+// softplus(x.Wnoise) of every (token, expert), fp32-faithful; H = c + eps * s.
+bool bal_tc_scores(const moe_shape &s) {
+    return s.dtype == MOE_BF16 && s.noisy && s.k < MOE_MAX_K && gate_tc_supported(s);
+}
 
 moe_shape ffn_shape(const moe_shape &s, int64_t rows_cap) {
     moe_shape f = s;
@@ -72,6 +83,12 @@ BalLayout bal_layout(const moe_shape &s, int64_t rows_cap) {
     B.kstar = take(static_cast<size_t>(s.n) * 4);
     B.quota = take(static_cast<size_t>(s.n) * 4);
     B.cnt = take(static_cast<size_t>(s.n) * 4);
+    if (bal_tc_scores(s)) {
+        B.sN = take(Tn * 4);
+        B.gidx = take(static_cast<size_t>(s.T) * s.k * 4);
+        B.gG = take(static_cast<size_t>(s.T) * s.k * 4);
+        B.vk = take(static_cast<size_t>(s.T) * 2 * 4);
+    }
     B.total = o;
     return B;
 }
@@ -140,6 +157,14 @@ __global__ void __launch_bounds__(256) bal_scores(const TX *__restrict__ x, cons
             H[t * n + e] = v;
         }
     }
+}
+
+// H = c + eps * s in place over c (T*n entries).
+__global__ void __launch_bounds__(256) bal_noisy_sum(float *__restrict__ c, const float *__restrict__ sc,
+                                                     const float *__restrict__ eps, int64_t count) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < count;
+         i += static_cast<int64_t>(gridDim.x) * 256)
+        c[i] = fmaf(eps[i], sc[i], c[i]);
 }
 
 // Order-preserving key of a float: larger float, larger key.
@@ -413,7 +438,16 @@ cudaError_t launch_forward_balanced(const moe_shape &s, const void *x, const flo
     int32_t *offsets = ws_ptr<int32_t>(ws, L.offsets);
     const float *eps_used = s.noisy ? eps : nullptr;
     const dim3 sgrid(static_cast<unsigned>((T + kBT - 1) / kBT), static_cast<unsigned>((n + kBT - 1) / kBT));
-    if (s.dtype == MOE_BF16)
+    if (bal_tc_scores(s) && eps_used) {
+        float *sN = ws_ptr<float>(ws, B.sN);
+        cudaError_t ge = launch_gate_tc_load(s, x, Wg, Wn, bg, eps_used, ws_ptr<int32_t>(ws, B.gidx),
+                                             ws_ptr<float>(ws, B.gG), H, sN, ws_ptr<float>(ws, B.vk),
+                                             ws, L, st);
+        if (ge != cudaSuccess) return ge;
+        const int64_t count = T * n;
+        const unsigned g = static_cast<unsigned>(std::min<int64_t>((count + 255) / 256, 148 * 16));
+        bal_noisy_sum<<<g, 256, 0, st>>>(H, sN, eps_used, count);
+    } else if (s.dtype == MOE_BF16)
         bal_scores<__nv_bfloat16><<<sgrid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(x), Wg, Wn,
                                                         bg, eps_used, T, d, n, H);
     else
