@@ -15,6 +15,7 @@
 //                     load mode (c and softplus(r) per expert, fp32-faithful),
 //                     then bal_noisy_sum; other shapes bal_scores, fp32 on the
 //                     CUDA cores (64 x 64 tiles)
+//   bal_transpose     HT [n, T], each expert's scores contiguous
 //   bal_count         per expert: the m-th largest score by a 4-pass 8-bit
 //                     radix select on order-preserving keys, and how many of
 //                     the tied scores to keep (batchwise); or the number of
@@ -41,7 +42,7 @@ constexpr int kBT = 64, kBK = 16;
 struct BalLayout {
     moe_shape ffn;  // the expert stage's shape: one slot per row
     WsLayout fwd;
-    size_t H = 0, rowmap = 0, row_token = 0, row_weight = 0, kstar = 0, quota = 0, cnt = 0;
+    size_t H = 0, HT = 0, rowmap = 0, row_token = 0, row_weight = 0, kstar = 0, quota = 0, cnt = 0;
     size_t sN = 0, gidx = 0, gG = 0, vk = 0;  // tensor-core scores: noise scale, its top-k, k-th
     size_t total = 0;
     int64_t rows = 0;  // row capacity
@@ -77,6 +78,7 @@ BalLayout bal_layout(const moe_shape &s, int64_t rows_cap) {
         return at;
     };
     B.H = take(Tn * 4);
+    B.HT = take(Tn * 4);
     B.rowmap = take(Tn * 4);
     B.row_token = take(R * 4);
     B.row_weight = take(R * 4);
@@ -167,6 +169,25 @@ __global__ void __launch_bounds__(256) bal_noisy_sum(float *__restrict__ c, cons
         c[i] = fmaf(eps[i], sc[i], c[i]);
 }
 
+// HT[e, t] = H[t, e]: each expert's scores contiguous for the per-expert
+// select and compaction (32 x 32 tiles through shared memory).
+__global__ void bal_transpose(const float *__restrict__ H, int64_t T, int n, float *__restrict__ HT) {
+    __shared__ float tile[32][33];
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const int e0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int64_t t = t0 + i;
+        const int e = e0 + threadIdx.x;
+        tile[i][threadIdx.x] = (t < T && e < n) ? H[t * n + e] : 0.0f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int e = e0 + i;
+        const int64_t t = t0 + threadIdx.x;
+        if (e < n && t < T) HT[static_cast<int64_t>(e) * T + t] = tile[threadIdx.x][i];
+    }
+}
+
 // Order-preserving key of a float: larger float, larger key.
 __device__ __forceinline__ uint32_t fkey(float f) {
     const uint32_t u = __float_as_uint(f);
@@ -177,7 +198,7 @@ __device__ __forceinline__ uint32_t fkey(float f) {
 // = key of the m-th largest score, quota[e] = how many scores equal to it are
 // kept (the lowest token indices), cnt[e] = m.  Threshold: cnt[e] = number of
 // scores above thr[e].
-__global__ void __launch_bounds__(1024) bal_count(const float *__restrict__ H, int64_t T, int n,
+__global__ void __launch_bounds__(1024) bal_count(const float *__restrict__ HT, int64_t T, int n,
                                                   int64_t m, const float *__restrict__ thr,
                                                   uint32_t *__restrict__ kstar,
                                                   int32_t *__restrict__ quota,
@@ -191,7 +212,8 @@ __global__ void __launch_bounds__(1024) bal_count(const float *__restrict__ H, i
     if (thr) {
         const float th = thr[e];
         int32_t c = 0;
-        for (int64_t t = tid; t < T; t += 1024) c += H[t * n + e] > th ? 1 : 0;
+        const float *col = HT + static_cast<int64_t>(e) * T;
+        for (int64_t t = tid; t < T; t += 1024) c += col[t] > th ? 1 : 0;
         for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
         if ((tid & 31) == 0) part[tid >> 5] = c;
         __syncthreads();
@@ -218,7 +240,7 @@ __global__ void __launch_bounds__(1024) bal_count(const float *__restrict__ H, i
         for (int i = tid; i < 256; i += 1024) hist[i] = 0;
         __syncthreads();
         for (int64_t t = tid; t < T; t += 1024) {
-            const uint32_t key = fkey(H[t * n + e]);
+            const uint32_t key = fkey(HT[static_cast<int64_t>(e) * T + t]);
             if ((key & pmask) == prefix) atomicAdd(&hist[(key >> (8 * p)) & 255u], 1u);
         }
         __syncthreads();
@@ -304,7 +326,7 @@ __device__ __forceinline__ int32_t block_exscan(int32_t v, int32_t *warp_tot) {
 
 // One block of 1024 threads per expert: its kept tokens in token order into
 // rows offsets[e] .. offsets[e+1]-1 (thread i owns a contiguous token range).
-__global__ void __launch_bounds__(1024) bal_write(const float *__restrict__ H, int64_t T, int n,
+__global__ void __launch_bounds__(1024) bal_write(const float *__restrict__ HT, int64_t T, int n,
                                                   const float *__restrict__ thr,
                                                   const uint32_t *__restrict__ kstar,
                                                   const int32_t *__restrict__ quota,
@@ -318,14 +340,15 @@ __global__ void __launch_bounds__(1024) bal_write(const float *__restrict__ H, i
     const uint32_t ks = kstar[e];
     const int32_t qt = quota[e];
     const float th = thr ? thr[e] : 0.0f;
+    const float *col = HT + static_cast<int64_t>(e) * T;
     // ties at the m-th score before this thread's range
     int32_t eq = 0;
     if (!thr)
-        for (int64_t t = t0; t < t1; ++t) eq += fkey(H[t * n + e]) == ks ? 1 : 0;
+        for (int64_t t = t0; t < t1; ++t) eq += fkey(col[t]) == ks ? 1 : 0;
     const int32_t eq_base = block_exscan(eq, warp_tot);
     auto kept = [&](int64_t t, int32_t &seen) {
-        if (thr) return H[t * n + e] > th;
-        const uint32_t key = fkey(H[t * n + e]);
+        if (thr) return col[t] > th;
+        const uint32_t key = fkey(col[t]);
         if (key > ks) return true;
         if (key == ks) return eq_base + seen++ < qt;
         return false;
@@ -453,12 +476,15 @@ cudaError_t launch_forward_balanced(const moe_shape &s, const void *x, const flo
     else
         bal_scores<float><<<sgrid, 256, 0, st>>>(static_cast<const float *>(x), Wg, Wn, bg, eps_used,
                                                  T, d, n, H);
+    float *HT = ws_ptr<float>(ws, B.HT);
+    bal_transpose<<<dim3(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>((n + 31) / 32)),
+                    dim3(32, 8), 0, st>>>(H, T, n, HT);
     const int64_t m = thr ? 0 : static_cast<int64_t>(s.k) * T / n;
-    bal_count<<<n, 1024, 0, st>>>(H, T, n, m, thr, ws_ptr<uint32_t>(ws, B.kstar),
+    bal_count<<<n, 1024, 0, st>>>(HT, T, n, m, thr, ws_ptr<uint32_t>(ws, B.kstar),
                                   ws_ptr<int32_t>(ws, B.quota), ws_ptr<int32_t>(ws, B.cnt));
     bal_scan<<<1, 1024, 0, st>>>(ws_ptr<int32_t>(ws, B.cnt), n, rows_cap, offsets, counts, err);
     cudaMemsetAsync(rowmap, 0xFF, sizeof(int32_t) * static_cast<size_t>(T) * n, st);  // -1
-    bal_write<<<n, 1024, 0, st>>>(H, T, n, thr, ws_ptr<uint32_t>(ws, B.kstar),
+    bal_write<<<n, 1024, 0, st>>>(HT, T, n, thr, ws_ptr<uint32_t>(ws, B.kstar),
                                   ws_ptr<int32_t>(ws, B.quota), offsets, row_token, rowmap);
     bal_weights<<<static_cast<unsigned>((T + 7) / 8), 256, 0, st>>>(H, rowmap, T, n, row_weight, W);
     cudaError_t e = cudaGetLastError();
