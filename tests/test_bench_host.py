@@ -1,0 +1,50 @@
+"""Host-side pieces of bench.py: the traffic record built from an ncu log,
+the algorithmic bytes of a workload, and the whole-job throughput."""
+import json
+
+import numpy as np
+
+import bench
+from sparsely_gated_mixture_top_b300 import workloads as wl
+
+CSV = '''==PROF== Connected to process 1
+"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"
+"0","1","python","h","unnamed>::ffn_tiles(const int *, int, int, int *)","1","7","(1024, 1, 1)","(1, 1, 1)","0","10.3","m","dram__bytes_read.sum","byte","1,024"
+"0","1","python","h","unnamed>::ffn_tiles(const int *, int, int, int *)","1","7","(1024, 1, 1)","(1, 1, 1)","0","10.3","m","dram__bytes_write.sum","byte","0"
+"0","1","python","h","unnamed>::ffn_tiles(const int *, int, int, int *)","1","7","(1024, 1, 1)","(1, 1, 1)","0","10.3","m","gpu__time_duration.sum","us","4.5"
+"1","1","python","h","void unnamed>::ffn_gemm_tc<256, 4>(x)","1","7","(320, 1, 1)","(148, 1, 1)","0","10.3","m","dram__bytes_read.sum","Mbyte","2.5"
+"1","1","python","h","void unnamed>::ffn_gemm_tc<256, 4>(x)","1","7","(320, 1, 1)","(148, 1, 1)","0","10.3","m","dram__bytes_write.sum","Kbyte","3"
+"1","1","python","h","void unnamed>::ffn_gemm_tc<256, 4>(x)","1","7","(320, 1, 1)","(148, 1, 1)","0","10.3","m","gpu__time_duration.sum","ns","9000"
+'''
+
+
+def test_traffic_summary_sums_the_captured_launches(tmp_path):
+    csv = tmp_path / "t.csv"
+    csv.write_text(CSV)
+    line = tmp_path / "b.json"
+    line.write_text("noise\n" + json.dumps({"roofline": {"algorithmic_per_launch": 123}}) + "\n")
+    rec = bench.traffic_summary(str(csv), str(line), wl.WORKLOADS["flat_n256_k4"])
+    assert rec["ffn_stage_dram_bytes_per_launch"] == 1024 + 2_500_000 + 3_000
+    assert [k["kernel"] for k in rec["kernels"]] == ["unnamed>::ffn_tiles",
+                                                    "void unnamed>::ffn_gemm_tc<256, 4>"]
+    assert rec["kernels"][0]["duration_ns_cold"] == 4500 and rec["kernels"][1]["duration_ns_cold"] == 9000
+    assert rec["algorithmic_bytes_per_launch"] == 123
+    assert rec["source_sha256"] == bench.source_digest() and rec["workload"] == "flat_n256_k4"
+
+
+def test_algorithmic_bytes_and_flops():
+    w = wl.Workload("t", T=10, d=64, h=128, n=4, k=2)            # bf16, flat, noisy
+    counts = np.array([5, 0, 10, 5])                               # 3 experts hit
+    a = bench.algorithmic(w, counts)
+    S = 20
+    weights = 3 * (2 * 64 * 128 * 2 + 4 * (64 + 128))
+    assert a["experts_hit"] == 3
+    assert a["flops"] == 4.0 * S * 64 * 128
+    assert a["ffn_bytes"] == weights + 10 * 64 * 2 + S * 64 * 2
+    assert a["layer_bytes"] == (weights + 2 * 10 * 64 * 2 + 10 * 4 * 4 + 2 * 64 * 4 * 4 +
+                                S * 8 + 4 * 8)
+
+
+def test_job_throughput_single_rank():
+    ms, value = bench.job_throughput(2.0, 1000)
+    assert ms == 2.0 and value == 1000 / 2e-3
