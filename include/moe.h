@@ -297,6 +297,16 @@ MOE_API moe_status moe_forward_balanced(const moe_shape *shape, const void *x, c
                                         void *stream);
 
 /*
+ * Diagnostic: launches one thread that waits, through the same bounded wait
+ * every pipelined kernel of this library uses, on a barrier that nothing
+ * arrives at.  After the 2 s limit it records MOE_ERR_TIMEOUT in the
+ * workspace's error word and returns; moe_check then reports it.  Nothing
+ * faults or traps and the context stays usable.  ws: any workspace of at
+ * least 256 bytes, 256-byte aligned.
+ */
+MOE_API moe_status moe_selftest_timeout(void *ws, size_t ws_bytes, void *stream);
+
+/*
  * Synchronises `stream`, reads the workspace's device error word, clears it
  * and returns it (MOE_OK when no device error was recorded).  Returns
  * MOE_ERR_CUDA if the stream itself failed.

@@ -31,7 +31,7 @@ EXPORTS = ("moe_version", "moe_status_string", "moe_validate", "moe_workspace_by
            "moe_workspace_init", "moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine",
            "moe_forward", "moe_check", "moe_dispatch_noalloc", "moe_load_workspace_bytes",
            "moe_gate_load", "moe_backward_workspace_bytes", "moe_backward",
-           "moe_balanced_workspace_bytes", "moe_forward_balanced")
+           "moe_balanced_workspace_bytes", "moe_forward_balanced", "moe_selftest_timeout")
 
 
 class MoEShape(ctypes.Structure):
@@ -72,9 +72,10 @@ def _load():
     lib.moe_balanced_workspace_bytes.argtypes = [shp, ctypes.c_int64]
     lib.moe_balanced_workspace_bytes.restype = sz
     lib.moe_forward_balanced.argtypes = [shp] + [vp] * 6 + [ctypes.c_int64] + [vp] * 8 + [sz, vp]
+    lib.moe_selftest_timeout.argtypes = [vp, sz, vp]
     for f in ("moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
               "moe_check", "moe_dispatch_noalloc", "moe_gate_load", "moe_backward",
-              "moe_forward_balanced"):
+              "moe_forward_balanced", "moe_selftest_timeout"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -264,3 +265,8 @@ def moe_forward_balanced(shape, x, Wg, Wn, bg, eps, thr, rows_cap, W1, b1, W2, b
         ctypes.byref(shape), _p(x), _p(Wg), _p(Wn), _p(bg), _p(eps), _p(thr), int(rows_cap),
         _p(W1), _p(b1), _p(W2), _p(b2), _p(y), _p(counts), _p(W), _p(ws), ws.numel(),
         _stream(stream)))
+
+
+def moe_selftest_timeout(ws, stream=None):
+    """Diagnostic: a bounded wait that runs out (MOE_ERR_TIMEOUT in ws after ~2 s)."""
+    _ok("moe_selftest_timeout", lib.moe_selftest_timeout(_p(ws), ws.numel(), _stream(stream)))
