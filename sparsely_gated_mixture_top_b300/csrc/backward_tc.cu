@@ -28,6 +28,7 @@ constexpr int kWgRows = 128;
 constexpr int kWgEpiWarps = 8;
 constexpr int kWgThreads = 32 * (2 + kWgEpiWarps);
 constexpr int32_t kSiteWgProducer = 30, kSiteWgMma = 31, kSiteWgEpilogue = 32, kSiteWgDrain = 33;
+constexpr int32_t kSiteRowsPerm = 34;  // a perm entry out of range while building dE rows
 
 template <int BN, int STAGES>
 struct WgCfg {
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(256) bt_rows_scaled(const __nv_bfloat16 *__res
     const int32_t s = perm[r];
     uint4 *dst = reinterpret_cast<uint4 *>(dE + r * d);
     if (s < 0 || s >= S) {
-        if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteWgProducer, static_cast<int32_t>(r));
+        if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteRowsPerm, static_cast<int32_t>(r));
         for (int c = lane; c < d / 8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
         return;
     }
