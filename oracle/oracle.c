@@ -115,12 +115,15 @@ static void noisy_top_k_gate(int d, const double *x, const double *Wg, const dou
                              double *H, scored *order, double *kept, double *margin) {
     for (int i = 0; i < m; ++i) {
         double c = 0.0, r = 0.0;
-        for (int j = 0; j < d; ++j) {
-            c += x[j] * Wg[(int64_t)j * ld + col0 + i];
-            r += x[j] * Wn[(int64_t)j * ld + col0 + i];
-        }
+        for (int j = 0; j < d; ++j) c += x[j] * Wg[(int64_t)j * ld + col0 + i];
         if (bg) c += bg[col0 + i];
-        H[i] = eps_row ? c + eps_row[col0 + i] * oracle_softplus(r) : c;
+        /* Without eps the noise term is absent, and Wn may be absent too. */
+        if (eps_row && Wn) {
+            for (int j = 0; j < d; ++j) r += x[j] * Wn[(int64_t)j * ld + col0 + i];
+            H[i] = c + eps_row[col0 + i] * oracle_softplus(r);
+        } else {
+            H[i] = c;
+        }
     }
     /* KeepTopK: sort (H desc, index asc) and keep the first k. */
     for (int i = 0; i < m; ++i) {
@@ -155,7 +158,7 @@ static void noisy_top_k_gate(int d, const double *x, const double *Wg, const dou
 int oracle_gate_flat(int64_t T, int d, int n, int k, const double *x, const double *Wg,
                      const double *Wn, const double *bg, const double *eps, int32_t *idx,
                      double *G, double *H_out, double *margin) {
-    if (T < 0 || d <= 0 || n <= 0 || k <= 0 || k > n) return -1;
+    if (T < 0 || d <= 0 || n <= 0 || k <= 0 || k > n || (eps && !Wn)) return -1;
     int bad = 0;
 #pragma omp parallel
     {
@@ -285,7 +288,7 @@ int oracle_gate_hier(int64_t T, int d, int groups, int m, int k_groups, int k_in
                      const double *x, const double *Wg, const double *Wn, const double *bg,
                      const double *eps, int32_t *idx, double *G, double *margin) {
     if (T < 0 || d <= 0 || groups <= 0 || m <= 0 || k_groups <= 0 || k_groups > groups ||
-        k_inner <= 0 || k_inner > m)
+        k_inner <= 0 || k_inner > m || (eps && !Wn))
         return -1;
     const int64_t C = (int64_t)groups + (int64_t)groups * m; /* score columns */
     const int k = k_groups * k_inner;

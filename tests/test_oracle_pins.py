@@ -358,3 +358,98 @@ def test_forward_hierarchical_invariants():
     assert np.array_equal(out["idx"], idx_h)
     y = oracle.experts_combine(x, idx_h, G_h, W1, np.zeros((n, h)), W2, np.zeros((n, d)))
     np.testing.assert_array_equal(out["y"], y)
+
+
+# --------------------------------------------------------------------------
+# Combine from expert-order rows ("MoE:稀疏门控混合专家", section 二: y is the
+# gate-weighted sum of the selected experts' outputs; only they contribute).
+# --------------------------------------------------------------------------
+def _combine_case(T=37, k=3, d=5, S_extra=4, drop=4, seed=3):
+    """Expert-order rows Y [S, d], gate weights G [T, k] and an inv_perm that
+    is a random permutation of the slots into rows, a few slots set to -1."""
+    rng = np.random.default_rng(seed)
+    S = T * k + S_extra
+    Y = rng.normal(size=(S, d))
+    G = rng.uniform(0.05, 1.0, size=(T, k))
+    inv = rng.permutation(S)[: T * k].astype(np.int32)
+    inv[rng.choice(T * k, size=drop, replace=False)] = -1
+    return Y, G, inv
+
+
+def _combine_pins(y, Y, G, inv):
+    """Checks of a candidate combine result that do not restate its formula:
+    (1) it equals the product of a scipy sparse [T, S] routing matrix with Y;
+    (2) with Y the identity, row t holds G[t, j] at column inv[t*k+j];
+    (3) with one-hot gate weights, row t is the selected expert row itself."""
+    import scipy.sparse as sp
+    T, k = G.shape
+    S, d = Y.shape
+    t_of = np.repeat(np.arange(T), k)
+    keep = inv >= 0
+    M = sp.csr_matrix((G.reshape(-1)[keep], (t_of[keep], inv[keep])), shape=(T, S))
+    ok = np.allclose(y(Y, inv, G), M @ Y, rtol=1e-13, atol=1e-13)
+    eye = np.eye(S)
+    yi = y(eye, inv, G)
+    want = np.zeros((T, S))
+    for s in np.nonzero(keep)[0]:
+        want[s // k, inv[s]] += G.reshape(-1)[s]
+    ok &= np.array_equal(yi, want)
+    for j in range(k):
+        oh = np.zeros_like(G)
+        oh[:, j] = 1.0
+        rows = inv.reshape(T, k)[:, j]
+        exp = np.where((rows >= 0)[:, None], Y[np.clip(rows, 0, None)], 0.0)
+        ok &= np.array_equal(y(Y, inv, oh), exp)
+    return bool(ok)
+
+
+def test_combine_rows_pins():
+    Y, G, inv = _combine_case()
+    assert _combine_pins(oracle.combine_rows, Y, G, inv)
+
+
+def test_combine_rows_pins_fail_planted_mistakes():
+    # Plausible mistakes, planted in copies of the combine on the CPU: each
+    # must fail the pins above.
+    Y, G, inv = _combine_case(seed=5)
+
+    def weight_dropped(Y_, inv_, G_):
+        return oracle.combine_rows(Y_, inv_, np.ones_like(G_))
+
+    def rows_by_slot(Y_, inv_, G_):
+        T, k = G_.shape
+        slot = np.where(inv_ >= 0, np.arange(T * k), -1).astype(np.int32)
+        return oracle.combine_rows(Y_, slot, G_)
+
+    def weight_of_next_slot(Y_, inv_, G_):
+        return oracle.combine_rows(Y_, inv_, np.roll(G_, 1, axis=1))
+
+    for bad in (weight_dropped, rows_by_slot, weight_of_next_slot):
+        assert not _combine_pins(bad, Y, G, inv), bad.__name__
+
+
+def test_combine_rows_composes_to_the_pinned_forward():
+    # routing, the experts on expert-order rows and the combine give the same
+    # y as the forward pass (itself pinned to torch's dense mixture and linear)
+    rng = np.random.default_rng(9)
+    T, d, h, n, k = 23, 16, 24, 5, 2
+    x = rng.normal(size=(T, d))
+    Wg = rng.normal(size=(d, n)) / math.sqrt(d)
+    W1 = rng.normal(size=(n, h, d)) / math.sqrt(d)
+    b1 = rng.normal(size=(n, h)) * 0.1
+    W2 = rng.normal(size=(n, d, h)) / math.sqrt(h)
+    b2 = rng.normal(size=(n, d)) * 0.1
+    ref = oracle.forward(x, Wg, None, None, None, W1, b1, W2, b2, k)
+    counts, offsets, perm, inv, imp, cv2 = oracle.route(ref["idx"], ref["G"], n)
+    experts = ref["idx"].reshape(-1)[perm]
+    Y = oracle.expert_rows(x[perm // k], experts, W1, b1, W2, b2)
+    y = oracle.combine_rows(Y, inv, ref["G"])
+    np.testing.assert_allclose(y, ref["y"], rtol=1e-12, atol=1e-12)
+
+
+def test_combine_rows_rejects_a_row_out_of_range():
+    Y, G, inv = _combine_case()
+    bad = inv.copy()
+    bad[7] = Y.shape[0]
+    with pytest.raises(ValueError):
+        oracle.combine_rows(Y, bad, G)
