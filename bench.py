@@ -49,6 +49,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target CPU seconds of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-workload", action="store_true",
+                   help="skip the other full-size workloads (per_workload field)")
+    p.add_argument("--per-workload-steps", type=int, default=20)
     p.add_argument("--pass", dest="which", choices=["forward", "backward", "balanced"],
                    default="forward",
                    help="forward: moe_forward (the headline); backward: moe_backward of the flat "
@@ -176,7 +179,9 @@ def algorithmic(w: wl.Workload, counts: np.ndarray) -> dict:
     wg_b = 2 * w.d * gate_cols * 4
     small = S * 8 + w.n * 8
     layer_bytes = weights + x_b + y_b + eps_b + wg_b + small
-    ffn_bytes = weights + x_b + S * w.d * eb     # weights hit, x rows once, expert rows out
+    # expert FFN stage: the hit experts' weights and x read once; the slot
+    # buffer, hidden activations and gathered rows are not algorithmic
+    ffn_bytes = weights + x_b
     flops = 4.0 * S * w.d * w.h
     return dict(layer_bytes=layer_bytes, ffn_bytes=ffn_bytes, flops=flops, experts_hit=hit)
 
@@ -185,55 +190,126 @@ def algorithmic(w: wl.Workload, counts: np.ndarray) -> dict:
 # Clock sampling during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
+    """Samples the SM clock, its maximum, the power draw and the active
+    clock-event (throttle) reasons of one GPU every `period_s` seconds through
+    NVML, read-only, from a background thread; falls back to `nvidia-smi -lms`
+    when NVML is unavailable.  `stop()` summarises the samples taken between
+    construction and the call."""
+    REASONS = (("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+               ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80),
+               ("sw_power_cap", 0x4))
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, device_index: int, period_s: float = 0.001):
+        self.samples = []          # (sm_mhz, max_mhz, power_w or None, reason bits)
+        self.source = None
         self.proc = None
+        self._stop = threading.Event()
+        self.period = period_s
+        try:
+            import pynvml as nv
+            nv.nvmlInit()
+            self.nv = nv
+            self.handle = self._handle(nv, device_index)
+            self.max_mhz = float(nv.nvmlDeviceGetMaxClockInfo(self.handle, nv.NVML_CLOCK_SM))
+            self.source = "nvml"
+            self._take()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+        except Exception:  # NVML missing or refused: one nvidia-smi process instead
+            self.source = None
+            self._start_smi(device_index)
+
+    @staticmethod
+    def _handle(nv, device_index):
+        try:
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id
+            return nv.nvmlDeviceGetHandleByPciBusId(bus)
+        except Exception:
+            return nv.nvmlDeviceGetHandleByIndex(device_index)
+
+    def _take(self):
+        nv = self.nv
+        sm = float(nv.nvmlDeviceGetClockInfo(self.handle, nv.NVML_CLOCK_SM))
+        try:
+            pw = nv.nvmlDeviceGetPowerUsage(self.handle) / 1000.0
+        except Exception:
+            pw = None
+        bits = int(nv.nvmlDeviceGetCurrentClocksEventReasons(self.handle))
+        self.samples.append((sm, self.max_mhz, pw, bits))
+
+    def _poll(self):
+        while not self._stop.wait(self.period):
+            try:
+                self._take()
+            except Exception:
+                return
+
+    def _start_smi(self, gpu_index):
         self.lines = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.source = "nvidia-smi"
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
             self.thread.start()
         except OSError:
             self.proc = None
 
-    def _read(self):
+    def _read_smi(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
-    def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.thread.join(timeout=5)
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) != 7:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-                power.append(float(parts[2]))
+                sm, smax = float(parts[0]), float(parts[1])
+                pw = float(parts[2])
             except ValueError:
                 continue
-            for name, v in zip(names, parts[3:]):
+            bits = 0
+            for (name, bit), v in zip((self.REASONS[0], self.REASONS[2], self.REASONS[1],
+                                       self.REASONS[4]), parts[3:]):
                 if v.lower() == "active":
+                    bits |= bit
+            self.samples.append((sm, smax, pw, bits))
+
+    def stop(self) -> dict:
+        if self.source is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"],
+                    "samples": 0}
+        if self.source == "nvml":
+            self._stop.set()
+            self.thread.join(timeout=5)
+            try:
+                self._take()       # one more at the end of the region
+            except Exception:
+                pass
+        else:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+        sm = [x[0] for x in self.samples]
+        smax = [x[1] for x in self.samples]
+        power = [x[2] for x in self.samples if x[2] is not None]
+        reasons = set()
+        for x in self.samples:
+            for name, bit in self.REASONS:
+                if x[3] & bit:
                     reasons.add(name)
         return {"sm_mhz": float(np.median(sm)) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "sm_mhz_min": min(sm) if sm else None,
                 "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "source": self.source,
+                "period_ms": self.period * 1e3 if self.source == "nvml" else 20.0,
+                "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------------------
@@ -498,6 +574,142 @@ def balanced_arm(args, w: wl.Workload):
     print(json.dumps(line), flush=True)
 
 
+PER_WORKLOAD = ("hier_4096h_16x256", "skewed_zipf_n64", "sparse_n2048_T4096",
+                "sparse_n2048_T32768", "sparse_n2048_T131072")
+
+
+def device_inputs(w: wl.Workload, dev, rank: int = 0, max_sets: int = 8):
+    """The workload's inputs on the device: weights shared by all ranks, x and
+    eps per rank, plus rotating copies of (x, eps) so that, together with the
+    weights, one step's inputs are out of L2 before they are read again."""
+    wr = w.with_(seed=w.seed + 7919 * rank) if rank else w   # each rank its own batch
+    host = wl.make_inputs(w)
+    if rank:
+        part = wl.make_inputs(wr, experts=False)
+        host["x"], host["eps"] = part["x"], part["eps"]
+    dinp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    per_set = host["x"].numel() * host["x"].element_size() + (
+        host["eps"].numel() * 4 if host["eps"] is not None else 0)
+    nsets = max(2, min(max_sets, math.ceil(256e6 / max(per_set, 1))))
+    sets = [(dinp["x"], dinp["eps"])]
+    for i in range(1, nsets):
+        p = wl.make_inputs(wr.with_(seed=wr.seed + 104729 * i), experts=False)
+        sets.append((p["x"].to(dev), p["eps"].to(dev) if p["eps"] is not None else None))
+    return host, dinp, sets, per_set
+
+
+def ffn_stage_ms(B, w, s, dinp, sets, out, ws, stream, dev, steps):
+    """Mean CUDA-event time of the expert FFN stage (moe_expert_ffn) with the
+    same inputs, between the component calls of the forward pass."""
+    S = w.T * w.k
+    comp = dict(idx=out["idx"], G=out["G"], counts=out["counts"],
+                offsets=torch.empty(w.n + 1, dtype=torch.int32, device=dev),
+                perm=torch.empty(S, dtype=torch.int32, device=dev),
+                inv_perm=torch.empty(S, dtype=torch.int32, device=dev),
+                Y=torch.empty((S, w.d), dtype=out["y"].dtype, device=dev))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        x, eps = sets[i % len(sets)]
+        B.moe_gate(s, x, dinp["Wg"], dinp["Wn"], dinp["bg"], eps, comp["idx"], comp["G"], ws,
+                   stream)
+        B.moe_dispatch(s, comp["idx"], comp["G"], comp["counts"], comp["offsets"], comp["perm"],
+                       comp["inv_perm"], out["importance"], out["cv2"], ws, stream)
+        ev[i][0].record(stream)
+        B.moe_expert_ffn(s, x, comp["perm"], comp["offsets"], dinp["W1"], dinp["b1"], dinp["W2"],
+                         dinp["b2"], comp["Y"], ws, stream)
+        ev[i][1].record(stream)
+        B.moe_combine(s, comp["Y"], comp["inv_perm"], comp["G"], out["y"], ws, stream)
+    torch.cuda.synchronize(dev)
+    status = B.moe_check(ws, stream)
+    if status != B.MOE_OK:
+        raise RuntimeError(f"device error in the stage timing: {B.status_string(status)}")
+    return float(np.mean([a.elapsed_time(b) for a, b in ev]))
+
+
+def rooflines(w, counts, ms_step, ffn_ms, long_run):
+    """Layer roofline and the expert FFN stage's roofline record."""
+    alg = algorithmic(w, counts)
+    pk = peaks()
+    # A contraction timed inside a loop of more than a second runs under the
+    # power cap: its peak is the sustained one, else the burst one.
+    tc_peak = pk["bf16_sustained"] if long_run else pk["bf16"]
+    tc_label = "sustained" if long_run else "burst"
+    ffn_bound_hbm = alg["ffn_bytes"] / (pk["hbm"] * 1e9) >= alg["flops"] / (tc_peak * 1e12)
+    if ffn_bound_hbm:
+        achieved = alg["ffn_bytes"] / (ffn_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s"}
+        roof["peak_source"] = pk["source"] + " copy bandwidth"
+    else:
+        achieved = alg["flops"] / (ffn_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s"}
+        roof["peak_source"] = f"{pk['source']} bf16 ({tc_label})"
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = stage_traffic(w)
+    roof["kernel"] = "expert FFN stage (moe_expert_ffn)"
+    roof["algorithmic_per_launch"] = alg["ffn_bytes"] if ffn_bound_hbm else alg["flops"]
+    roof["algorithmic_accounting"] = ("weights of the experts hit + x read once (slot buffer, "
+                                      "hidden activations and gathered rows excluded)"
+                                      if ffn_bound_hbm else "4*S*d*h FLOPs")
+    roof["ms_per_launch"] = ffn_ms
+    t_hbm = alg["layer_bytes"] / (pk["hbm"] * 1e9)
+    t_tc = alg["flops"] / (tc_peak * 1e12)
+    t_roof = max(t_hbm, t_tc)
+    layer_roof = {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+                  "tensor_peak": f"{tc_label} {tc_peak} TFLOP/s",
+                  "t_roof_us": t_roof * 1e6, "t_meas_us": ms_step * 1e3,
+                  "frac": t_roof / (ms_step / 1e3), "algorithmic_bytes": alg["layer_bytes"],
+                  "flops": alg["flops"], "experts_hit": alg["experts_hit"]}
+    return alg, roof, layer_roof
+
+
+def time_workload(B, w: wl.Workload, dev, stream, steps: int, warmup: int) -> dict:
+    """One workload's forward pass, device-resident inputs: ms per step, its
+    layer roofline fraction, the expert FFN stage's fraction and the clocks."""
+    host, dinp, sets, per_set = device_inputs(w, dev, max_sets=3)
+    del host
+    s = B.shape_of(w)
+    ws = B.workspace(s, dev)
+    out = B.outputs(s, dev)
+
+    def fwd(i):
+        x, eps = sets[i % len(sets)]
+        B.moe_forward(s, x, dinp["Wg"], dinp["Wn"], dinp["bg"], eps, dinp["W1"], dinp["b1"],
+                      dinp["W2"], dinp["b2"], out["y"], out["G"], out["idx"], out["importance"],
+                      out["cv2"], out["counts"], ws, stream)
+
+    for i in range(warmup):
+        fwd(i)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index or 0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        fwd(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    status = B.moe_check(ws, stream)
+    if status != B.MOE_OK:
+        raise RuntimeError(f"{w.name}: device error: {B.status_string(status)}")
+    ms = e0.elapsed_time(e1)
+    ms_step = ms / steps
+    ffn_ms = ffn_stage_ms(B, w, s, dinp, sets, out, ws, stream, dev, max(3, steps // 2))
+    alg, roof, layer_roof = rooflines(w, out["counts"].cpu().numpy(), ms_step, ffn_ms,
+                                      ms > 1000.0)
+    rec = {"config": config_of(w), "steps": steps, "warmup": warmup, "ms_per_step": ms_step,
+           "tokens_per_s": w.T / (ms_step / 1e3), "tflops": alg["flops"] / (ms_step / 1e3) / 1e12,
+           "layer_roofline_frac": layer_roof["frac"], "layer_bound": layer_roof["bound"],
+           "t_roof_us": layer_roof["t_roof_us"],
+           "ffn_stage": {"ms": ffn_ms, "bound": roof["bound"], "achieved": roof["achieved"],
+                         "unit": roof["unit"], "frac": roof["frac"]},
+           "clocks": clk}
+    del dinp, sets, ws, out
+    torch.cuda.empty_cache()
+    return rec
+
+
 def main():
     args = parse()
     w = wl.WORKLOADS[args.workload]
@@ -526,23 +738,8 @@ def main():
 
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    wr = w.with_(seed=w.seed + 7919 * rank) if rank else w   # each rank its own batch
-    host = wl.make_inputs(w)                                   # weights shared by all ranks
-    if rank:
-        part = wl.make_inputs(wr, experts=False)
-        host["x"], host["eps"] = part["x"], part["eps"]
-    dinp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
-
-    # rotating copies of the per-step inputs (x, eps): together with the
-    # weights they exceed L2, so no step reads another step's inputs from L2
-    per_set = host["x"].numel() * host["x"].element_size() + (
-        host["eps"].numel() * 4 if host["eps"] is not None else 0)
-    nsets = max(2, min(8, math.ceil(256e6 / max(per_set, 1))))
-    sets = [(dinp["x"], dinp["eps"])]
-    for i in range(1, nsets):
-        p = wl.make_inputs(wr.with_(seed=wr.seed + 104729 * i), experts=False)
-        sets.append((p["x"].to(dev), p["eps"].to(dev) if p["eps"] is not None else None))
-
+    host, dinp, sets, per_set = device_inputs(w, dev, rank)
+    nsets = len(sets)
     s = B.shape_of(w)
     ws = B.workspace(s, dev)
     out = B.outputs(s, dev)
@@ -578,64 +775,14 @@ def main():
     status = B.moe_check(ws, stream)
     if status != B.MOE_OK:
         raise RuntimeError(f"device error in the timed region: {B.status_string(status)}")
+    long_run = ms > 1000.0
     ms, value = job_throughput(ms, w.T * args.steps, dist, dev)
     ms_step = ms / args.steps
-    counts = out["counts"].cpu().numpy()
-    alg = algorithmic(w, counts)
-    pk = peaks()
 
     # ---- stage timing: the expert FFN stage, same inputs, component calls ---
-    S = w.T * w.k
-    comp = dict(idx=out["idx"], G=out["G"], counts=out["counts"],
-                offsets=torch.empty(w.n + 1, dtype=torch.int32, device=dev),
-                perm=torch.empty(S, dtype=torch.int32, device=dev),
-                inv_perm=torch.empty(S, dtype=torch.int32, device=dev),
-                Y=torch.empty((S, w.d), dtype=out["y"].dtype, device=dev))
-    ksteps = max(1, args.steps // 2)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(ksteps)]
-    torch.cuda.synchronize(dev)
-    for i in range(ksteps):
-        x, eps = sets[i % nsets]
-        B.moe_gate(s, x, dinp["Wg"], dinp["Wn"], dinp["bg"], eps, comp["idx"], comp["G"], ws,
-                   stream)
-        B.moe_dispatch(s, comp["idx"], comp["G"], comp["counts"], comp["offsets"], comp["perm"],
-                       comp["inv_perm"], out["importance"], out["cv2"], ws, stream)
-        ev[i][0].record(stream)
-        B.moe_expert_ffn(s, x, comp["perm"], comp["offsets"], dinp["W1"], dinp["b1"], dinp["W2"],
-                         dinp["b2"], comp["Y"], ws, stream)
-        ev[i][1].record(stream)
-        B.moe_combine(s, comp["Y"], comp["inv_perm"], comp["G"], out["y"], ws, stream)
-    torch.cuda.synchronize(dev)
-    ffn_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
-    # A contraction timed inside a loop of more than a second runs under the
-    # power cap: its peak is the sustained one, else the burst one.
-    long_run = ms > 1000.0
-    tc_peak = pk["bf16_sustained"] if long_run else pk["bf16"]
-    tc_label = "sustained" if long_run else "burst"
-    ffn_bound_hbm = alg["ffn_bytes"] / (pk["hbm"] * 1e9) >= alg["flops"] / (tc_peak * 1e12)
-    if ffn_bound_hbm:
-        achieved = alg["ffn_bytes"] / (ffn_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s"}
-        roof["peak_source"] = pk["source"] + " copy bandwidth"
-    else:
-        achieved = alg["flops"] / (ffn_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s"}
-        roof["peak_source"] = f"{pk['source']} bf16 ({tc_label})"
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = stage_traffic(w)
-    roof["kernel"] = "expert FFN stage (moe_expert_ffn: tile table, gather, 2 grouped tcgen05 GEMMs)"
-    roof["algorithmic_per_launch"] = alg["ffn_bytes"] if ffn_bound_hbm else alg["flops"]
-    roof["ms_per_launch"] = ffn_ms
+    ffn_ms = ffn_stage_ms(B, w, s, dinp, sets, out, ws, stream, dev, max(1, args.steps // 2))
+    alg, roof, layer_roof = rooflines(w, out["counts"].cpu().numpy(), ms_step, ffn_ms, long_run)
 
-    t_roof = max(alg["layer_bytes"] / (pk["hbm"] * 1e9), alg["flops"] / (tc_peak * 1e12))
-    layer_roof = {"bound": "hbm" if alg["layer_bytes"] / (pk["hbm"] * 1e9) >= alg["flops"] / (
-                      tc_peak * 1e12) else "tensor", "tensor_peak": f"{tc_label} {tc_peak} TFLOP/s",
-                  "t_roof_us": t_roof * 1e6, "t_meas_us": ms_step * 1e3,
-                  "frac": t_roof / (ms_step / 1e3), "algorithmic_bytes": alg["layer_bytes"],
-                  "flops": alg["flops"], "experts_hit": alg["experts_hit"]}
-
-    # ---- end to end: host buffers in, results out, through moe_forward ------
     # ---- end to end: host buffers in, results out, through moe_forward ------
     # Every step copies its x and eps in from pinned host memory and its y, G,
     # idx, importance, cv2 and counts back.  As a serving loop would, the
@@ -711,6 +858,18 @@ def main():
                "sample": f"first {ntok} tokens of the workload, one fp64 oracle forward "
                          f"({dt:.1f} s; weights converted to fp64 before timing)"}
 
+    # ---- the other full-size workloads, one GPU (rank 0 of a 1-rank run) ----
+    per_workload = None
+    if rank == 0 and world == 1 and not args.no_per_workload:
+        del dinp, sets, ws, out, host
+        torch.cuda.empty_cache()
+        per_workload = {}
+        for name in PER_WORKLOAD:
+            if name == w.name:
+                continue
+            per_workload[name] = time_workload(B, wl.WORKLOADS[name], dev, stream,
+                                               steps=args.per_workload_steps, warmup=3)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -726,6 +885,7 @@ def main():
             "e2e": e2e,
             "gpu_launches": launches_per_step(w) * args.steps,
             "clocks": clk,
+            "per_workload": per_workload,
         }
         print(json.dumps(line), flush=True)
     if dist:

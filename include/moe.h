@@ -119,8 +119,13 @@ MOE_API const char *moe_status_string(moe_status s);
 MOE_API moe_status moe_validate(const moe_shape *shape);
 
 /* Workspace bytes every call below needs for this shape (0 if the shape is
- * invalid).  One workspace serves all calls of one shape; its first 256 bytes
- * hold the device error word.  The workspace must be 256-byte aligned. */
+ * invalid).  The pages have no counterpart (their layer ran inside a training
+ * framework that owned memory); the workspace holds what the stages pass to
+ * each other: the packed gate matrices of section 三/四 of
+ * "MoE:稀疏门控混合专家", the routing scratch, and the expert-ordered rows of
+ * "Outrageously Large Neural Networks - 中文验证版" section 瓶颈.  One
+ * workspace serves all calls of one shape; its first 256 bytes hold the
+ * device error word.  The workspace must be 256-byte aligned. */
 MOE_API size_t moe_workspace_bytes(const moe_shape *shape);
 
 /* Clears the device error word of a workspace (enqueued on `stream`).  Call it
@@ -141,7 +146,13 @@ MOE_API moe_status moe_gate(const moe_shape *shape, const void *x, const float *
                     size_t ws_bytes, void *stream);
 
 /*
- * Dispatch (routing): per-expert counts, their exclusive scan, the stable
+ * Dispatch (routing).  "Outrageously Large Neural Networks - 中文验证版",
+ * section 瓶颈: each expert receives only the rows routed to it (about k*b/n
+ * of a batch of b), so those rows are gathered together; "MoE:稀疏门控混合专家"
+ * section 二: experts with weight 0 are not computed; section 方法适配 of the
+ * first page and the wudongming97 note (section 方法怎么做): the importance of
+ * an expert is the batch sum of its gate weights.
+ * Outputs: per-expert counts, their exclusive scan, the stable
  * permutation of the slots into expert-contiguous rows and its inverse, the
  * importance vector (gate weight summed per expert in row order, fp64
  * accumulation) and its CV^2.  An idx entry outside [0, n) sets
@@ -164,9 +175,10 @@ MOE_API moe_status moe_dispatch(const moe_shape *shape, const int32_t *idx, cons
  *   - Limit: the scratch needed is 256 B + 4*S + 12*ceil(S/1024)*n + 8*n
  *     bytes (each term rounded up to 256 B); a shape that needs more than
  *     8 MiB returns MOE_ERR_UNSUPPORTED and enqueues nothing.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress)
+ *     with the caller's current device, so the address stays right after a
+ *     device reset.  The first call on a device may load the library's
+ *     module there: make that first call before any stream capture.
  *   - Every call on a device shares the one array, which keeps the previous
  *     call's contents (each call clears the part that must start at zero).
  *     Calls whose work overlaps on the GPU (different streams, or different
@@ -192,7 +204,9 @@ MOE_API moe_status moe_expert_ffn(const moe_shape *shape, const void *x, const i
                           const float *b2, void *Y_slot, void *ws, size_t ws_bytes, void *stream);
 
 /*
- * Combine: y[t] = sum_{j=0..k-1} G[t,j] * Y_slot[inv_perm[t*k+j]], summed in
+ * Combine ("MoE:稀疏门控混合专家", section 二: y = sum_i G(x)_i E_i(x), only
+ * the selected experts contributing):
+ * y[t] = sum_{j=0..k-1} G[t,j] * Y_slot[inv_perm[t*k+j]], summed in
  * fp32 in that fixed j order and rounded once to the output type.  A slot
  * with inv_perm = -1 contributes nothing; an entry >= S sets MOE_ERR_DEVICE.
  */
@@ -200,8 +214,9 @@ MOE_API moe_status moe_combine(const moe_shape *shape, const void *Y_slot, const
                        const float *G, void *y, void *ws, size_t ws_bytes, void *stream);
 
 /*
- * The whole forward pass on one stream: gate, dispatch, expert FFNs and
- * combine.  Outputs y [T,d], G [T,k], idx [T,k], importance [n], cv2 [1],
+ * The whole forward pass on one stream ("MoE:稀疏门控混合专家", sections 二,
+ * 三 and 四: noisy score, KeepTopK, softmax, the selected experts, their
+ * weighted sum): gate, dispatch, expert FFNs and combine.  Outputs y [T,d], G [T,k], idx [T,k], importance [n], cv2 [1],
  * counts [n]; the permutation and the expert outputs live in the workspace.
  */
 MOE_API moe_status moe_forward(const moe_shape *shape, const void *x, const float *Wg, const float *Wn,
@@ -309,7 +324,11 @@ MOE_API moe_status moe_selftest_timeout(void *ws, size_t ws_bytes, void *stream)
 /*
  * Synchronises `stream`, reads the workspace's device error word, clears it
  * and returns it (MOE_OK when no device error was recorded).  Returns
- * MOE_ERR_CUDA if the stream itself failed.
+ * MOE_ERR_CUDA if the stream itself failed.  The pages have no counterpart:
+ * this is how device-side checks of the steps above (an expert index outside
+ * the n experts of "MoE:稀疏门控混合专家" section 三, a routing entry outside
+ * the S = T*k slots, a bounded wait that ran out) reach the caller without a
+ * fault.
  */
 MOE_API moe_status moe_check(void *ws, void *stream);
 

@@ -49,3 +49,55 @@ def enforce_margin(w: wl.Workload, inp: dict, rows=None, min_margin: float = 1e-
         inp["eps"][todo] = wl.eps_rows(w, todo.tolist(), [attempts[t] for t in todo.tolist()])
         redraws += int(todo.size)
     raise RuntimeError(f"{todo.size} tokens still below the margin after {max_rounds} rounds")
+
+
+def column_cut_gaps(H: np.ndarray, ranks) -> np.ndarray:
+    """For each column e of the oracle scores H [T, n], the gap between its
+    ranks[e]-th and (ranks[e]+1)-th largest value (+inf when the rank is 0 or T)."""
+    T, n = H.shape
+    gaps = np.full(n, np.inf)
+    for e in range(n):
+        r = int(ranks[e])
+        if 0 < r < T:
+            part = -np.partition(-H[:, e], (r - 1, r))
+            gaps[e] = part[r - 1] - part[r]
+    return gaps
+
+
+def enforce_cut_margin(w: wl.Workload, inp: dict, ranks, min_margin: float = 1e-3,
+                       max_redraws: int = 200000) -> int:
+    """Balanced routing keeps, in column e, the ranks[e] tokens with the largest
+    noisy score H[:, e].  Redraw single eps cells (in place) until every
+    column's ranks[e]-th and (ranks[e]+1)-th oracle scores differ by at least
+    `min_margin`, so that the kept set has one right answer under rounding.
+
+    Only the cell eps[t, e] of the token t at rank ranks[e] + 1 of a failing
+    column is redrawn: that moves H[t, e] alone and leaves every other column
+    as it was.  Returns the number of redraws.  Needs noisy flat inputs."""
+    if inp["eps"] is None or w.groups:
+        raise ValueError("the cut margin redraws eps cells of a flat noisy workload")
+    _, _, H, _ = gate_flat(inp["x"], inp["Wg"], inp["Wn"], inp["bg"], inp["eps"], 1)
+    T, n = H.shape
+    attempts = {}
+    redraws = 0
+    for e in range(n):
+        r = int(ranks[e])
+        if not 0 < r < T:
+            continue
+        while True:
+            col = H[:, e]
+            order = np.argsort(-col, kind="stable")
+            if col[order[r - 1]] - col[order[r]] >= min_margin:
+                break
+            if redraws >= max_redraws:
+                raise RuntimeError(f"column {e}: cut margin not reached after {redraws} redraws")
+            t = int(order[r])
+            a = attempts.get((t, e), 0) + 1
+            attempts[(t, e)] = a
+            inp["eps"][t, e] = wl.eps_cell(w, t, e, a)
+            # the oracle's noisy score of this one token again (its other columns are unchanged)
+            _, _, Ht, _ = gate_flat(inp["x"][t:t + 1], inp["Wg"], inp["Wn"], inp["bg"],
+                                    inp["eps"][t:t + 1], 1)
+            H[t, e] = Ht[0, e]
+            redraws += 1
+    return redraws

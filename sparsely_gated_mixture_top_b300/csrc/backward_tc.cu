@@ -409,12 +409,9 @@ template <int BN, int STAGES>
 cudaError_t launch_wg(const CUtensorMap &mP, const CUtensorMap &mQ, const int32_t *kblk, int n,
                       int M, int N, float *out, int32_t *err, cudaStream_t st) {
     using Cfg = WgCfg<BN, STAGES>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(wgrad_gemm_tc<BN, STAGES>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
-    });
+    // Per-context opt-in above 48 KB, set before every launch (cheap).
+    const cudaError_t attr_err = cudaFuncSetAttribute(
+        wgrad_gemm_tc<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t total = static_cast<int64_t>(n) * (M / kWgRows) * (N / BN);
     const int grid = static_cast<int>(total < sm_count() ? total : sm_count());

@@ -13,8 +13,6 @@
 #include "moe_device.cuh"
 #include "moe_launch.h"
 
-#include <mutex>
-
 namespace moe {
 
 namespace {
@@ -44,26 +42,18 @@ WsLayout noalloc_layout(const moe_shape &s) {
     return L;
 }
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};
-std::once_flag g_scratch_once[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices] = {};
-
-// Device address of the static array on the current device (host code only
-// sees a host-side stand-in for the symbol, so the address must be queried).
+// Device address of the static array on the current device.  Host code only
+// sees a host-side stand-in for the symbol, so the address is queried, with
+// the device current, on every call: the lookup is a cheap host operation
+// once the module is loaded, and a fresh lookup stays right after a device
+// reset (which reloads the module, possibly at another address).  The first
+// call on a device may load the module there.
 cudaError_t scratch_address(void **out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::call_once(g_scratch_once[dev], [dev] {
-        void *p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        g_scratch_addr[dev] = p;
-    });
-    if (g_scratch_err[dev] != cudaSuccess) return g_scratch_err[dev];
-    *out = g_scratch_addr[dev];
-    return *out ? cudaSuccess : cudaErrorInvalidSymbol;
+    *out = p;
+    return p ? cudaSuccess : cudaErrorInvalidSymbol;
 }
 
 }  // namespace

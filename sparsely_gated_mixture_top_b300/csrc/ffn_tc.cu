@@ -354,12 +354,10 @@ cudaError_t launch_bn(const CUtensorMap &mA, const CUtensorMap &mB, const int32_
                       __nv_bfloat16 *out, int32_t *err, int grid, cudaStream_t st) {
     const int out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
     using Cfg = TcCfg<BN, STAGES>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(ffn_gemm_tc<BN, STAGES>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
-    });
+    // The opt-in above 48 KB of dynamic shared memory belongs to the current
+    // device's context, so it is set before every launch (a cheap host call).
+    cudaError_t attr_err = cudaFuncSetAttribute(
+        ffn_gemm_tc<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (attr_err != cudaSuccess) return attr_err;
     ffn_gemm_tc<BN, STAGES><<<grid, kFfnThreads, Cfg::kSmem, st>>>(mA, mB, offsets, tiles, n, K, N, bias,
                                                            relu, out, out_v8, err);

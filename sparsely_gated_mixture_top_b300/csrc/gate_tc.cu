@@ -674,12 +674,9 @@ template <bool kResident, bool kGrouped, int KM>
 cudaError_t launch_gate_tc_t(const CUtensorMap &mx, const uint8_t *wpack, const GateArgs &ga,
                              int grid, cudaStream_t st) {
     using Cfg = GateCfg<kResident, KM>;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(gate_tc<kResident, kGrouped, KM>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
-    });
+    // Per-context opt-in above 48 KB, set before every launch (cheap).
+    const cudaError_t attr = cudaFuncSetAttribute(
+        gate_tc<kResident, kGrouped, KM>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (attr != cudaSuccess) return attr;
     gate_tc<kResident, kGrouped, KM><<<grid, kGateThreads, Cfg::kSmem, st>>>(mx, wpack, ga);
     return cudaGetLastError();

@@ -25,8 +25,6 @@
 #include "moe_device.cuh"
 #include "moe_launch.h"
 
-#include <mutex>
-
 namespace moe {
 
 namespace {
@@ -299,32 +297,24 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
     int32_t *chunk = ws_ptr<int32_t>(ws, L.chunk);
     double *chunk_imp = ws_ptr<double>(ws, L.chunk_imp);
     double *imp64 = ws_ptr<double>(ws, L.imp64);
-    // Dynamic shared memory: n doubles and n ints (plus 4 KB static); the
-    // opt-in above the default 48 KB is raised once to the largest size seen.
-    const size_t smem = 12 * static_cast<size_t>(n);
-    static size_t opted_in = 0;
-    static std::mutex opt_mu;
-    if (smem + 4096 > 48 * 1024) {
-        std::lock_guard<std::mutex> lock(opt_mu);
-        if (smem > opted_in) {
+    // Dynamic shared memory above the default 48 KB needs an opt-in, which
+    // belongs to the current device's context: it is set before each launch.
+    if (n <= kRankWarpsMaxN) {
+        const size_t smem = 256 * static_cast<size_t>(n);  // [32][n] counts and sums
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(
+                route_rank_warps, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+        }
+        route_rank_warps<<<chunks, 1024, smem, st>>>(idx, G, S, n, local_rank, chunk, chunk_imp,
+                                                     err);
+    } else {
+        const size_t smem = 12 * static_cast<size_t>(n);  // n doubles and n ints (+4 KB static)
+        if (smem + 4096 > 48 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(
                 route_rank, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
             if (e != cudaSuccess) return e;
-            opted_in = smem;
         }
-    }
-    if (n <= kRankWarpsMaxN) {
-        // 256 * n bytes of tables (128 KB at most), opted in once
-        static std::once_flag once;
-        static cudaError_t attr_err = cudaSuccess;
-        std::call_once(once, [] {
-            attr_err = cudaFuncSetAttribute(route_rank_warps, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            256 * kRankWarpsMaxN);
-        });
-        if (attr_err != cudaSuccess) return attr_err;
-        route_rank_warps<<<chunks, 1024, 256 * static_cast<size_t>(n), st>>>(idx, G, S, n, local_rank,
-                                                                           chunk, chunk_imp, err);
-    } else {
         route_rank<<<chunks, 1024, smem, st>>>(idx, G, S, n, local_rank, chunk, chunk_imp, err);
     }
     route_colscan<<<(n + 31) / 32, dim3(32, 32), 0, st>>>(chunk, chunk_imp, chunks, n, counts, imp64);

@@ -25,6 +25,7 @@ from . import synth
 
 # Tensor ids of the generator streams (part of the input definition).
 TID_X, TID_WG, TID_WN, TID_EPS, TID_W1, TID_B1, TID_W2, TID_B2 = 1, 2, 3, 5, 6, 7, 8, 9
+TID_EPS_CELL = 10   # single eps cells redrawn one at a time (attempt >= 1)
 
 
 @dataclass(frozen=True)
@@ -125,6 +126,14 @@ def eps_rows(w: Workload, rows, attempts) -> torch.Tensor:
     for i, (t, a) in enumerate(zip(rows, attempts)):
         synth.fill_normal(out[i], w.seed, TID_EPS, int(a), int(t) * w.cols, 1.0)
     return out
+
+
+def eps_cell(w: Workload, t: int, e: int, attempt: int) -> float:
+    """A fresh N(0,1) draw for the single cell eps[t, e] (stream TID_EPS_CELL,
+    its own attempt counter), for redraws that must move one score only."""
+    out = torch.empty((1,), dtype=torch.float32)
+    synth.fill_normal(out, w.seed, TID_EPS_CELL, int(attempt), int(t) * w.cols + int(e), 1.0)
+    return float(out[0])
 
 
 def make_inputs(w: Workload, pin: bool = False, experts: bool = True,

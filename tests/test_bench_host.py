@@ -40,7 +40,8 @@ def test_algorithmic_bytes_and_flops():
     weights = 3 * (2 * 64 * 128 * 2 + 4 * (64 + 128))
     assert a["experts_hit"] == 3
     assert a["flops"] == 4.0 * S * 64 * 128
-    assert a["ffn_bytes"] == weights + 10 * 64 * 2 + S * 64 * 2
+    # the FFN stage: hit weights and x once; the slot buffer is not algorithmic
+    assert a["ffn_bytes"] == weights + 10 * 64 * 2
     assert a["layer_bytes"] == (weights + 2 * 10 * 64 * 2 + 10 * 4 * 4 + 2 * 64 * 4 * 4 +
                                 S * 8 + 4 * 8)
 
@@ -48,3 +49,20 @@ def test_algorithmic_bytes_and_flops():
 def test_job_throughput_single_rank():
     ms, value = bench.job_throughput(2.0, 1000)
     assert ms == 2.0 and value == 1000 / 2e-3
+
+
+def test_clock_sampler_summary_without_a_gpu():
+    # On a machine without NVML or nvidia-smi the sampler reports no source and
+    # no numbers instead of failing; with samples injected it reports the
+    # median, the minimum, the maximum and every active reason.
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    c.samples, c.source, c.period = [], "nvml", 0.001
+    c._stop = bench.threading.Event()
+    c.thread = bench.threading.Thread(target=lambda: None)
+    c.thread.start()
+    c._take = lambda: None
+    c.samples = [(2032.0, 2032.0, 500.0, 0x0), (1900.0, 2032.0, 900.0, 0x4),
+                 (2000.0, 2032.0, 800.0, 0x0)]
+    r = c.stop()
+    assert r["sm_mhz"] == 2000.0 and r["sm_mhz_min"] == 1900.0 and r["sm_max_mhz"] == 2032.0
+    assert r["samples"] == 3 and r["reasons"] == ["sw_power_cap"] and r["power_w_max"] == 900.0

@@ -65,3 +65,27 @@ def test_zipf_gate_bias():
     assert b.shape == (64,)
     assert b[0].item() == 0.0 and b[1].item() == pytest.approx(2 * math.log(0.5), rel=1e-6)
     assert torch.all(b[1:] < b[:-1])
+
+
+def test_cut_margin_redraws_single_cells():
+    """The balanced-routing cut margin redraws single eps cells: afterwards
+    every column's cut clears the margin, and a changed cell never moves the
+    scores of another column."""
+    import oracle
+    from oracle.margin import column_cut_gaps, enforce_cut_margin
+    w = wl.Workload("cut", T=500, d=32, h=64, n=6, k=2, seed=3)
+    inp = wl.make_inputs(w, experts=False)
+    before = inp["eps"].clone()
+    _, _, H0, _ = oracle.gate_flat(inp["x"], inp["Wg"], inp["Wn"], inp["bg"], inp["eps"], 1)
+    ranks = [w.k * w.T // w.n] * w.n
+    redraws = enforce_cut_margin(w, inp, ranks, min_margin=5e-3)
+    assert redraws > 0
+    _, _, H1, _ = oracle.gate_flat(inp["x"], inp["Wg"], inp["Wn"], inp["bg"], inp["eps"], 1)
+    assert column_cut_gaps(H1, ranks).min() >= 5e-3
+    changed = (inp["eps"] != before).numpy()
+    assert changed.sum() >= 1
+    np.testing.assert_array_equal(H1[~changed], H0[~changed])
+    # the same redraw sequence again gives the same tensor (counter-based draws)
+    again = wl.make_inputs(w, experts=False)
+    enforce_cut_margin(w, again, ranks, min_margin=5e-3)
+    assert torch.equal(again["eps"], inp["eps"])
