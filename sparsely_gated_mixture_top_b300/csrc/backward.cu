@@ -896,7 +896,9 @@ cudaError_t launch_backward_tc(const moe_shape &s, const void *x, const float *W
     int32_t *offsets = ws_ptr<int32_t>(ws, L.offsets);
     int32_t *perm = ws_ptr<int32_t>(ws, L.perm);
     int32_t *inv = ws_ptr<int32_t>(ws, L.inv_perm);
-    const int32_t *tiles = ws_ptr<int32_t>(ws, L.tiles);  // 128-row blocks, from the recompute
+    int32_t *tiles = ws_ptr<int32_t>(ws, L.tiles);     // 128-row blocks (single-SM GEMM)
+    int32_t *ptiles = ws_ptr<int32_t>(ws, L.ptiles);   // token tiles (pair GEMM)
+    int4 *plist = ws_ptr<int4>(ws, L.plist);
     auto bf = [&](size_t off) { return ws_ptr<__nv_bfloat16>(ws, off); };
     __nv_bfloat16 *xperm = bf(L.xperm), *hid = bf(L.hidden), *E = bf(L.yslot);
     __nv_bfloat16 *W1T = bf(B.W1T), *W2T = bf(B.W2T), *dE = bf(B.dE), *dZ = bf(B.dA), *dXs = bf(B.dXs);
@@ -919,11 +921,22 @@ cudaError_t launch_backward_tc(const moe_shape &s, const void *x, const float *W
     if (e == cudaSuccess)
         e = launch_rows_scaled(static_cast<const __nv_bfloat16 *>(dy), G, perm, S, d, k, dE, err, st);
     // dA = dE W2 (B = W2^T rows, K = d), then dZ = dA * [a > 0];  dXs = dZ W1 (B = W1^T rows, K = h)
-    if (e == cudaSuccess)
-        e = launch_grouped_gemm_tc(s, dE, d, W2T, h, nullptr, 0, offsets, tiles, dZ, err, st);
+    // Each GEMM runs on an SM pair when its output width allows (the tile
+    // tables of both kernels are built here from the routing).
+    if (e == cudaSuccess) e = launch_row_tiles(offsets, n, kTcRows, tiles, st);
+    if (e == cudaSuccess && (pair_gemm_supported(h) || pair_gemm_supported(d)))
+        e = launch_pair_tiles(offsets, n, ptiles, plist, st);
+    auto row_gemm = [&](const __nv_bfloat16 *X, int K, const __nv_bfloat16 *Wt, int Nout,
+                        __nv_bfloat16 *out) {
+        return pair_gemm_supported(Nout)
+                   ? launch_grouped_gemm_pair(s, X, K, Wt, Nout, nullptr, 0, ptiles, plist, out,
+                                              err, st)
+                   : launch_grouped_gemm_tc(s, X, K, Wt, Nout, nullptr, 0, offsets, tiles, out,
+                                            err, st);
+    };
+    if (e == cudaSuccess) e = row_gemm(dE, d, W2T, h, dZ);
     if (e == cudaSuccess) e = launch_relu_mask(dZ, hid, S * static_cast<int64_t>(h), st);
-    if (e == cudaSuccess)
-        e = launch_grouped_gemm_tc(s, dZ, h, W1T, d, nullptr, 0, offsets, tiles, dXs, err, st);
+    if (e == cudaSuccess) e = row_gemm(dZ, h, W1T, d, dXs);
     // weight gradients: rows as the contraction axis, transposed and padded per expert
     if (e == cudaSuccess) e = launch_row_tiles(offsets, n, 64, kblk, st);
     if (e == cudaSuccess) e = launch_transpose_pad(dE, d, offsets, kblk, n, S, B.Kcap, bf(B.PdE), st);

@@ -373,38 +373,6 @@ __global__ void __launch_bounds__(256) bt_transpose_pad(const __nv_bfloat16 *__r
                       out + static_cast<int64_t>(c0) * Kcap + static_cast<int64_t>(rt) * 64, Kcap, t);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// bf16 [rows, K] (K contiguous) as a 3-D tensor {64, rows, K/64}, box {64, box_rows, 1}.
-bool make_kmajor_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {64, rows, K / 64};
-    cuuint64_t strides[2] = {K * 2, 128};
-    cuuint32_t box[3] = {64, box_rows, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int BN, int STAGES>
 cudaError_t launch_wg(const CUtensorMap &mP, const CUtensorMap &mQ, const int32_t *kblk, int n,
                       int M, int N, float *out, int32_t *err, cudaStream_t st) {

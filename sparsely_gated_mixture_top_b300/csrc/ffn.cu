@@ -196,17 +196,32 @@ cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *
     int32_t *err = ws_ptr<int32_t>(ws, 0);
     int32_t *tiles = ws_ptr<int32_t>(ws, L.tiles);
     if (s.dtype == MOE_BF16) {
-        ffn_tiles<<<1, 1024, 0, st>>>(offsets, s.n, kTcRows, tiles);
+        // Each layer runs on a pair of SMs when its output width is a
+        // multiple of 256 (ffn_pair.cu), else on the single-SM kernel.
+        const bool pair1 = pair_gemm_supported(s.h), pair2 = pair_gemm_supported(s.d);
+        int32_t *ptiles = ws_ptr<int32_t>(ws, L.ptiles);
+        int4 *plist = ws_ptr<int4>(ws, L.plist);
+        if (pair1 || pair2) {
+            cudaError_t e = launch_pair_tiles(offsets, s.n, ptiles, plist, st);
+            if (e != cudaSuccess) return e;
+        }
+        if (!pair1 || !pair2) ffn_tiles<<<1, 1024, 0, st>>>(offsets, s.n, kTcRows, tiles);
         __nv_bfloat16 *xperm = ws_ptr<__nv_bfloat16>(ws, L.xperm);
         __nv_bfloat16 *hid = ws_ptr<__nv_bfloat16>(ws, L.hidden);
         ffn_gather<<<static_cast<unsigned>((S + 8 * kGatherRows - 1) / (8 * kGatherRows)), 256, 0, st>>>(
             static_cast<const __nv_bfloat16 *>(x), perm, offsets, s.n, S, s.d, s.k, xperm, err);
-        cudaError_t e = launch_grouped_gemm_tc(s, xperm, s.d, static_cast<const __nv_bfloat16 *>(W1),
-                                               s.h, b1, 1, offsets, tiles, hid, err, st);
+        const auto *W1b = static_cast<const __nv_bfloat16 *>(W1);
+        const auto *W2b = static_cast<const __nv_bfloat16 *>(W2);
+        cudaError_t e = pair1 ? launch_grouped_gemm_pair(s, xperm, s.d, W1b, s.h, b1, 1, ptiles,
+                                                         plist, hid, err, st)
+                              : launch_grouped_gemm_tc(s, xperm, s.d, W1b, s.h, b1, 1, offsets,
+                                                       tiles, hid, err, st);
         if (e != cudaSuccess) return e;
-        return launch_grouped_gemm_tc(s, hid, s.h, static_cast<const __nv_bfloat16 *>(W2), s.d, b2,
-                                      0, offsets, tiles, static_cast<__nv_bfloat16 *>(Y_slot), err,
-                                      st);
+        auto *Y = static_cast<__nv_bfloat16 *>(Y_slot);
+        return pair2 ? launch_grouped_gemm_pair(s, hid, s.h, W2b, s.d, b2, 0, ptiles, plist, Y,
+                                                err, st)
+                     : launch_grouped_gemm_tc(s, hid, s.h, W2b, s.d, b2, 0, offsets, tiles, Y, err,
+                                              st);
     }
     ffn_tiles<<<1, 1024, 0, st>>>(offsets, s.n, kSimtRows, tiles);
     float *hid = ws_ptr<float>(ws, L.hidden);

@@ -312,42 +312,6 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
 }
 
-// --- host side: tensor maps -------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// bf16 matrix [rows, K] (K contiguous) seen as a 3-D tensor {64, rows, K/64}
-// (strides K*2 and 128 bytes), box {64, box_rows, kKB}: one copy brings kKB
-// 64-wide k-blocks of box_rows rows, each landing as a 128-byte-swizzled
-// K-major tile; a k-block past K/64 reads as zeros.
-bool make_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {64, rows, K / 64};
-    cuuint64_t strides[2] = {K * 2, 128};
-    cuuint32_t box[3] = {64, box_rows, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int BN, int STAGES>
 cudaError_t launch_bn(const CUtensorMap &mA, const CUtensorMap &mB, const int32_t *offsets,
                       const int32_t *tiles, int n, int K, int N, const float *bias, int relu,
@@ -366,6 +330,43 @@ cudaError_t launch_bn(const CUtensorMap &mA, const CUtensorMap &mB, const int32_
 
 }  // namespace
 
+// --- host side: tensor maps -------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// bf16 matrix [rows, K] (K contiguous) seen as a 3-D tensor {64, rows, K/64}
+// (strides K*2 and 128 bytes), box {64, box_rows, box_kblocks}: one copy
+// brings box_kblocks 64-wide k-blocks of box_rows rows, each landing as a
+// 128-byte-swizzled K-major tile; a k-block past K/64 reads as zeros.
+bool make_kmajor_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows,
+                     uint32_t box_kblocks) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {64, rows, K / 64};
+    cuuint64_t strides[2] = {K * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, box_kblocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int tc_block_n(int N) {
     if (N % 256 == 0) return 256;
     if (N % 128 == 0) return 128;
@@ -379,8 +380,8 @@ cudaError_t launch_grouped_gemm_tc(const moe_shape &s, const __nv_bfloat16 *A, i
     const int64_t S = slots(s);
     CUtensorMap mA, mB;
     const int BN = tc_block_n(N);
-    if (!make_map(&mA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(S), kTcRows) ||
-        !make_map(&mB, B, static_cast<uint64_t>(K), static_cast<uint64_t>(s.n) * N,
+    if (!make_kmajor_map(&mA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(S), kTcRows) ||
+        !make_kmajor_map(&mB, B, static_cast<uint64_t>(K), static_cast<uint64_t>(s.n) * N,
                   static_cast<uint32_t>(BN)))
         return cudaErrorInvalidValue;
     const int64_t max_tiles = ((S + kTcRows - 1) / kTcRows + s.n) * (N / BN);

@@ -381,6 +381,12 @@ __device__ __forceinline__ float softplus_fast(float z) {
     return fmaxf(z, 0.0f) + __logf(1.0f + __expf(-fabsf(z)));
 }
 
+// Asynchronous bulk prefetch of `bytes` (multiple of 16, 16-byte aligned
+// address) of global memory into L2; nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Hint that a global line will be read soon (into L2).
 __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

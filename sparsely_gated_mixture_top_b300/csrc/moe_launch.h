@@ -2,6 +2,7 @@
 // workspace layout and the launchers of each stage.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -26,6 +27,10 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool gate_tc_supported(const moe_shape &s);
 size_t gate_tc_pack_bytes(const moe_shape &s);
 
+// Entries of the pair FFN's token-tile table: an expert of R rows has at most
+// ceil(R / 256) tiles.
+inline size_t pair_tile_capacity(int64_t S, int n) { return static_cast<size_t>(S / 256 + n + 1); }
+
 // Byte offsets of every region of a workspace (all 256-byte aligned).
 struct WsLayout {
     size_t header = 0;
@@ -44,6 +49,8 @@ struct WsLayout {
     size_t importance = 0;  // [n] fp32
     size_t cv2 = 0;         // [1] fp32
     size_t tiles = 0;       // [n + 1] int32 row-tile starts of the FFN schedule
+    size_t ptiles = 0;      // [n + 1] int32 token-tile starts of the pair FFN schedule
+    size_t plist = 0;       // [S/256 + n + 1] int4 token tiles of the pair FFN schedule
     size_t xperm = 0;       // [S, d] dtype, x rows in expert order
     size_t hidden = 0;      // [S, h] dtype, hidden activations in expert order
     size_t yslot = 0;       // [S, d] dtype, expert outputs in expert order
@@ -78,6 +85,8 @@ inline WsLayout ws_layout(const moe_shape &s) {
     L.importance = take(n * 4);
     L.cv2 = take(4);
     L.tiles = take((n + 1) * 4);
+    L.ptiles = take((n + 1) * 4);
+    L.plist = take(pair_tile_capacity(static_cast<int64_t>(S), s.n) * 16);
     L.xperm = take(S * static_cast<size_t>(s.d) * eb);
     L.hidden = take(S * static_cast<size_t>(s.h) * eb);
     L.yslot = take(S * static_cast<size_t>(s.d) * eb);
@@ -142,5 +151,26 @@ cudaError_t launch_load(const moe_shape &s, const int32_t *idx, void *lws, const
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Pair (cta_group::2) grouped GEMM with the tokens on the MMA's N side
+// (ffn_pair.cu): whether an output width suits it, its token-tile table
+// (tiles[e] = token tiles of the experts before e, tiles[n] = total) and the
+// GEMM  out[r, c] = act(X[r] . W[e*Nout + c] + bias[e*Nout + c]).
+// tlist: one int4 per token tile {expert, first row, rows, rows rounded up to
+// 16}, at most pair_tile_capacity(S, n) entries.
+bool pair_gemm_supported(int Nout);
+cudaError_t launch_pair_tiles(const int32_t *offsets, int n, int32_t *tiles, int4 *tlist,
+                              cudaStream_t st);
+cudaError_t launch_grouped_gemm_pair(const moe_shape &s, const __nv_bfloat16 *X, int K,
+                                     const __nv_bfloat16 *W, int Nout, const float *bias, int relu,
+                                     const int32_t *tiles, const int4 *tlist,
+                                     __nv_bfloat16 *out, int32_t *err, cudaStream_t st);
+
+// Tensor map of a bf16 matrix [rows, K] (K contiguous, K % 64 == 0) seen as a
+// 3-D tensor {64, rows, K/64}: a box of box_rows rows and box_kblocks 64-wide
+// k-blocks lands as that many 128-byte-swizzled K-major tiles back to back;
+// rows or k-blocks past the end read as zeros.
+bool make_kmajor_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows,
+                     uint32_t box_rows, uint32_t box_kblocks = 1);
 
 }  // namespace moe
