@@ -189,6 +189,57 @@ def algorithmic(w: wl.Workload, counts: np.ndarray) -> dict:
 # ---------------------------------------------------------------------------
 # Clock sampling during the timed region
 # ---------------------------------------------------------------------------
+class _Nvml:
+    """The few read-only NVML queries the clock sampler needs, through ctypes
+    on the driver's libnvidia-ml (no Python binding required)."""
+    CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+
+    def handle(self, device_index):
+        ct = self.ct
+        h = ct.c_void_p()
+        try:
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id
+            if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ct.byref(h)) == 0:
+                return h
+        except Exception:
+            pass
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ct.c_uint(device_index), ct.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return h
+
+    def _uint(self, fn, h, *args):
+        v = self.ct.c_uint()
+        if fn(h, *args, self.ct.byref(v)) != 0:
+            raise RuntimeError(fn.__name__)
+        return v.value
+
+    def sm_clock(self, h):
+        return self._uint(self.lib.nvmlDeviceGetClockInfo, h, self.ct.c_int(self.CLOCK_SM))
+
+    def max_sm_clock(self, h):
+        return self._uint(self.lib.nvmlDeviceGetMaxClockInfo, h, self.ct.c_int(self.CLOCK_SM))
+
+    def power_w(self, h):
+        try:
+            return self._uint(self.lib.nvmlDeviceGetPowerUsage, h) / 1000.0
+        except RuntimeError:
+            return None
+
+    def reasons(self, h):
+        v = self.ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetCurrentClocksEventReasons(h, self.ct.byref(v)) != 0:
+            if self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, self.ct.byref(v)) != 0:
+                raise RuntimeError("clock event reasons")
+        return int(v.value)
+
+
 class ClockSampler:
     """Samples the SM clock, its maximum, the power draw and the active
     clock-event (throttle) reasons of one GPU every `period_s` seconds through
@@ -209,35 +260,23 @@ class ClockSampler:
         self._stop = threading.Event()
         self.period = period_s
         try:
-            import pynvml as nv
-            nv.nvmlInit()
-            self.nv = nv
-            self.handle = self._handle(nv, device_index)
-            self.max_mhz = float(nv.nvmlDeviceGetMaxClockInfo(self.handle, nv.NVML_CLOCK_SM))
+            self.nv = _Nvml()
+            self.handle = self.nv.handle(device_index)
+            self.max_mhz = float(self.nv.max_sm_clock(self.handle))
             self.source = "nvml"
             self._take()
             self.thread = threading.Thread(target=self._poll, daemon=True)
             self.thread.start()
-        except Exception:  # NVML missing or refused: one nvidia-smi process instead
+        except Exception as exc:  # NVML missing or refused: one nvidia-smi process instead
+            self.nvml_error = repr(exc)
             self.source = None
             self._start_smi(device_index)
 
-    @staticmethod
-    def _handle(nv, device_index):
-        try:
-            bus = torch.cuda.get_device_properties(device_index).pci_bus_id
-            return nv.nvmlDeviceGetHandleByPciBusId(bus)
-        except Exception:
-            return nv.nvmlDeviceGetHandleByIndex(device_index)
-
     def _take(self):
         nv = self.nv
-        sm = float(nv.nvmlDeviceGetClockInfo(self.handle, nv.NVML_CLOCK_SM))
-        try:
-            pw = nv.nvmlDeviceGetPowerUsage(self.handle) / 1000.0
-        except Exception:
-            pw = None
-        bits = int(nv.nvmlDeviceGetCurrentClocksEventReasons(self.handle))
+        sm = float(nv.sm_clock(self.handle))
+        pw = nv.power_w(self.handle)
+        bits = nv.reasons(self.handle)
         self.samples.append((sm, self.max_mhz, pw, bits))
 
     def _poll(self):
@@ -303,7 +342,8 @@ class ClockSampler:
             for name, bit in self.REASONS:
                 if x[3] & bit:
                     reasons.add(name)
-        return {"sm_mhz": float(np.median(sm)) if sm else None,
+        extra = {"nvml_error": self.nvml_error} if getattr(self, "nvml_error", None) else {}
+        return {**extra, "sm_mhz": float(np.median(sm)) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "sm_mhz_min": min(sm) if sm else None,
                 "power_w_max": max(power) if power else None,
