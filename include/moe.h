@@ -154,8 +154,9 @@ MOE_API moe_status moe_gate(const moe_shape *shape, const void *x, const float *
  * an expert is the batch sum of its gate weights.
  * Outputs: per-expert counts, their exclusive scan, the stable
  * permutation of the slots into expert-contiguous rows and its inverse, the
- * importance vector (gate weight summed per expert in row order, fp64
- * accumulation) and its CV^2.  An idx entry outside [0, n) sets
+ * importance vector (gate weight summed per expert in a fixed order: slots
+ * of a 32-slot group, the groups of a 1024-slot chunk, then the chunks; fp32)
+ * and its CV^2.  An idx entry outside [0, n) sets
  * MOE_ERR_DEVICE in the error word; that slot is left out of every output
  * (inv_perm[s] = -1) and the rest stays consistent.
  */
@@ -172,7 +173,7 @@ MOE_API moe_status moe_dispatch(const moe_shape *shape, const int32_t *idx, cons
  * kernels, but keeps their scratch in one array of static device storage
  * inside this library (8 MiB, resident on every device that loads the
  * library until the process exits).  It calls no allocation routine.
- *   - Limit: the scratch needed is 256 B + 4*S + 12*ceil(S/1024)*n + 8*n
+ *   - Limit: the scratch needed is 256 B + 4*S + 8*ceil(S/1024)*n + 4*n
  *     bytes (each term rounded up to 256 B); a shape that needs more than
  *     8 MiB returns MOE_ERR_UNSUPPORTED and enqueues nothing.
  *   - Every call looks up the array's device address (cudaGetSymbolAddress)

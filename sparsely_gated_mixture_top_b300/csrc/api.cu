@@ -178,8 +178,13 @@ moe_status moe_forward(const moe_shape *s, const void *x, const float *Wg, const
     if (s->T > 0)
         e = launch_gate(*s, x, Wg, s->noisy ? Wn : nullptr, bg, s->noisy ? eps : nullptr, idx, G,
                         ws, L, st);
-    if (e == cudaSuccess) e = launch_dispatch(*s, idx, G, cnt, off, perm, inv, imp, c2, ws, L, st);
-    if (e == cudaSuccess) e = launch_expert_ffn(*s, x, perm, off, W1, b1, W2, b2, yslot, ws, L, st);
+    // The dispatch also gathers the x rows and builds the expert stage's
+    // schedules, so the expert stage starts with its GEMMs.
+    const DispatchExtras ex = dispatch_extras_for_ffn(*s, x, ws, L);
+    if (e == cudaSuccess)
+        e = launch_dispatch(*s, idx, G, cnt, off, perm, inv, imp, c2, ws, L, st, &ex);
+    if (e == cudaSuccess)
+        e = launch_expert_ffn(*s, x, perm, off, W1, b1, W2, b2, yslot, ws, L, st, true);
     if (e == cudaSuccess) e = launch_combine(*s, yslot, inv, G, y, ws_ptr<int32_t>(ws, 0), st);
     return cuda_status(e);
 }

@@ -50,7 +50,7 @@ constexpr int kBT = 64;  // rows and columns of a SIMT tile
 constexpr int kBK = 16;  // k per shared-memory step
 
 struct BwdLayout {
-    size_t local_rank = 0, chunk = 0, chunk_imp = 0, imp64 = 0;
+    size_t local_rank = 0, chunk = 0, chunk_imp = 0, imp_acc = 0;
     size_t counts = 0, offsets = 0, perm = 0, inv_perm = 0, imp = 0, cv2 = 0, tiles = 0;
     size_t WgT = 0, WnT = 0, gimp = 0, dc = 0, dr = 0;
     size_t Z = 0, dZ = 0, E = 0, dXs = 0;
@@ -78,8 +78,8 @@ BwdLayout bwd_layout(const moe_shape &s) {
     };
     L.local_rank = take(S * 4);
     L.chunk = take(chunks * n * 4);
-    L.chunk_imp = take(chunks * n * 8);
-    L.imp64 = take(n * 8);
+    L.chunk_imp = take(chunks * n * 4);
+    L.imp_acc = take(n * 4);
     L.counts = take(n * 4);
     L.offsets = take((n + 1) * 4);
     L.perm = take(S * 4);
@@ -997,7 +997,7 @@ cudaError_t launch_backward(const moe_shape &s, const void *x, const float *Wg, 
     RL.local_rank = B.local_rank;
     RL.chunk = B.chunk;
     RL.chunk_imp = B.chunk_imp;
-    RL.imp64 = B.imp64;
+    RL.imp_acc = B.imp_acc;
     cudaError_t e = launch_dispatch(s, idx, G, ws_ptr<int32_t>(ws, B.counts), offsets, perm, inv,
                                     ws_ptr<float>(ws, B.imp), ws_ptr<float>(ws, B.cv2), ws, RL, st);
     if (e == cudaSuccess) e = launch_row_tiles(offsets, n, kBT, tiles, st);

@@ -1,8 +1,8 @@
 // combine.cu -- y[t] = sum_j G[t,j] * Y_slot[inv_perm[t*k+j]]
 // ("MoE:稀疏门控混合专家", section 二: y = sum_i G(x)_i E_i(x), only the selected
 // experts contributing).  One warp per token, 16-byte vector loads of the
-// expert rows (four in flight), fp32 accumulation in the fixed slot order
-// j = 0..k-1 and one rounding to the output type.
+// expert rows (eight in flight per lane), fp32 accumulation in the fixed slot
+// order j = 0..k-1 and one rounding to the output type.
 #include "moe_device.cuh"
 #include "moe_launch.h"
 
@@ -10,13 +10,13 @@ namespace moe {
 
 namespace {
 
+// 16-byte pieces of a row and their conversion to fp32.
 template <typename T>
 struct Vec;
 template <>
 struct Vec<__nv_bfloat16> {
-    static constexpr int N = 8;
-    __device__ static void load(const __nv_bfloat16 *p, float (&v)[8]) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    static constexpr int N = 8;  // elements per 16-byte piece
+    __device__ static void to_f(const uint4 &u, float (&v)[8]) {
         const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -25,35 +25,37 @@ struct Vec<__nv_bfloat16> {
             v[2 * i + 1] = f.y;
         }
     }
-    __device__ static void store(__nv_bfloat16 *p, const float (&v)[8]) {
+    __device__ static uint4 from_f(const float (&v)[8]) {
         uint4 u;
         u.x = pack_bf16x2(v[0], v[1]);
         u.y = pack_bf16x2(v[2], v[3]);
         u.z = pack_bf16x2(v[4], v[5]);
         u.w = pack_bf16x2(v[6], v[7]);
-        *reinterpret_cast<uint4 *>(p) = u;
+        return u;
     }
 };
 template <>
 struct Vec<float> {
     static constexpr int N = 4;
-    __device__ static void load(const float *p, float (&v)[4]) {
-        const float4 u = *reinterpret_cast<const float4 *>(p);
-        v[0] = u.x;
-        v[1] = u.y;
-        v[2] = u.z;
-        v[3] = u.w;
+    __device__ static void to_f(const uint4 &u, float (&v)[4]) {
+        v[0] = __uint_as_float(u.x);
+        v[1] = __uint_as_float(u.y);
+        v[2] = __uint_as_float(u.z);
+        v[3] = __uint_as_float(u.w);
     }
-    __device__ static void store(float *p, const float (&v)[4]) {
-        *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    __device__ static uint4 from_f(const float (&v)[4]) {
+        return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                          __float_as_uint(v[3]));
     }
 };
 
-// One warp per token.  The token's k rows and weights are read once; for each
-// 32*V-wide column span, four expert rows are loaded before any is summed,
-// then the sum runs in the fixed slot order j = 0..k-1.
+// One warp per token.  The token's k rows and weights are read once; for
+// every pair of 32-piece column spans, all of the (up to four at a time)
+// expert rows' pieces are requested before any is summed, so each lane keeps
+// eight 16-byte loads in flight; the sum runs in the fixed slot order
+// j = 0..k-1 in fp32 and is rounded once.
 template <typename T, int KM>
-__global__ void __launch_bounds__(256, KM <= 4 ? 3 : 2) combine_kernel(const T *__restrict__ Y,
+__global__ void __launch_bounds__(256) combine_kernel(const T *__restrict__ Y,
                                                       const int32_t *__restrict__ inv_perm,
                                                       const float *__restrict__ G, int64_t T_,
                                                       int d, int k, int64_t S,
@@ -78,30 +80,45 @@ __global__ void __launch_bounds__(256, KM <= 4 ? 3 : 2) combine_kernel(const T *
             w[j] = G[t * k + j];
         }
     }
-    for (int c = lane * V; c < d; c += 32 * V) {
-        float acc[V];
+    const int pieces = d / V;  // 16-byte pieces per row
+    for (int p0 = lane; p0 < pieces; p0 += 64) {
+        const int p1 = p0 + 32;
+        const bool two = p1 < pieces;
+        float acc0[V], acc1[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < V; ++i) acc0[i] = acc1[i] = 0.0f;
 #pragma unroll
         for (int j0 = 0; j0 < KM; j0 += 4) {
             if (j0 >= k) break;
-            float v[4][V];
+            uint4 u[4][2];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 const int j = j0 + jj;
-                if (j < k && rows[j] >= 0)
-                    Vec<T>::load(Y + static_cast<int64_t>(rows[j]) * d + c, v[jj]);
+                u[jj][0] = u[jj][1] = make_uint4(0, 0, 0, 0);
+                if (j < k && rows[j] >= 0) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(Y + static_cast<int64_t>(rows[j]) * d);
+                    u[jj][0] = __ldg(src + p0);
+                    if (two) u[jj][1] = __ldg(src + p1);
+                }
             }
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 const int j = j0 + jj;
                 if (j < k && rows[j] >= 0) {
+                    float a[V], b[V];
+                    Vec<T>::to_f(u[jj][0], a);
+                    Vec<T>::to_f(u[jj][1], b);
 #pragma unroll
-                    for (int i = 0; i < V; ++i) acc[i] = fmaf(w[j], v[jj][i], acc[i]);
+                    for (int i = 0; i < V; ++i) {
+                        acc0[i] = fmaf(w[j], a[i], acc0[i]);
+                        acc1[i] = fmaf(w[j], b[i], acc1[i]);
+                    }
                 }
             }
         }
-        Vec<T>::store(y + t * d + c, acc);
+        uint4 *dst = reinterpret_cast<uint4 *>(y + t * d);
+        dst[p0] = Vec<T>::from_f(acc0);
+        if (two) dst[p1] = Vec<T>::from_f(acc1);
     }
 }
 

@@ -6,7 +6,7 @@
 // fixed budget, plug-ins loaded into a host that owns every device
 // allocation, or a real-time path where an allocation could block or fail.
 // This entry point runs the same routing kernels as moe_dispatch, but their
-// scratch (slot ranks, per-chunk counts, fp64 importance and an error word)
+// scratch (slot ranks, per-chunk counts and importance sums, an error word)
 // lives in one array with static storage in this library's device image.
 // The array is created when the library's module is loaded on a device and
 // stays resident on every device that loads it until the process exits.
@@ -35,9 +35,9 @@ WsLayout noalloc_layout(const moe_shape &s) {
     L.chunk = o;
     o = align_up(o + chunks * n * 4, 256);
     L.chunk_imp = o;
-    o = align_up(o + chunks * n * 8, 256);
-    L.imp64 = o;
-    o = align_up(o + n * 8, 256);
+    o = align_up(o + chunks * n * 4, 256);
+    L.imp_acc = o;
+    o = align_up(o + n * 4, 256);
     L.total = o;
     return L;
 }

@@ -187,10 +187,32 @@ cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, cons
     return cudaGetLastError();
 }
 
+DispatchExtras dispatch_extras_for_ffn(const moe_shape &s, const void *x, void *ws,
+                                       const WsLayout &L) {
+    DispatchExtras ex;
+    if (s.dtype == MOE_BF16) {
+        const bool pair1 = pair_gemm_supported(s.h), pair2 = pair_gemm_supported(s.d);
+        ex.x = static_cast<const __nv_bfloat16 *>(x);
+        ex.xperm = ws_ptr<__nv_bfloat16>(ws, L.xperm);
+        if (pair1 || pair2) {
+            ex.ptiles = ws_ptr<int32_t>(ws, L.ptiles);
+            ex.plist = ws_ptr<int4>(ws, L.plist);
+        }
+        if (!pair1 || !pair2) {
+            ex.rtiles = ws_ptr<int32_t>(ws, L.tiles);
+            ex.bm = kTcRows;
+        }
+    } else {
+        ex.rtiles = ws_ptr<int32_t>(ws, L.tiles);
+        ex.bm = kSimtRows;
+    }
+    return ex;
+}
+
 cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *perm,
                               const int32_t *offsets, const void *W1, const float *b1,
                               const void *W2, const float *b2, void *Y_slot, void *ws,
-                              const WsLayout &L, cudaStream_t st) {
+                              const WsLayout &L, cudaStream_t st, bool prepared) {
     const int64_t S = slots(s);
     if (S == 0) return cudaSuccess;
     int32_t *err = ws_ptr<int32_t>(ws, 0);
@@ -201,15 +223,18 @@ cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *
         const bool pair1 = pair_gemm_supported(s.h), pair2 = pair_gemm_supported(s.d);
         int32_t *ptiles = ws_ptr<int32_t>(ws, L.ptiles);
         int4 *plist = ws_ptr<int4>(ws, L.plist);
-        if (pair1 || pair2) {
-            cudaError_t e = launch_pair_tiles(offsets, s.n, ptiles, plist, st);
-            if (e != cudaSuccess) return e;
-        }
-        if (!pair1 || !pair2) ffn_tiles<<<1, 1024, 0, st>>>(offsets, s.n, kTcRows, tiles);
         __nv_bfloat16 *xperm = ws_ptr<__nv_bfloat16>(ws, L.xperm);
         __nv_bfloat16 *hid = ws_ptr<__nv_bfloat16>(ws, L.hidden);
-        ffn_gather<<<static_cast<unsigned>((S + 8 * kGatherRows - 1) / (8 * kGatherRows)), 256, 0, st>>>(
-            static_cast<const __nv_bfloat16 *>(x), perm, offsets, s.n, S, s.d, s.k, xperm, err);
+        if (!prepared) {
+            if (pair1 || pair2) {
+                cudaError_t e = launch_pair_tiles(offsets, s.n, ptiles, plist, st);
+                if (e != cudaSuccess) return e;
+            }
+            if (!pair1 || !pair2) ffn_tiles<<<1, 1024, 0, st>>>(offsets, s.n, kTcRows, tiles);
+            ffn_gather<<<static_cast<unsigned>((S + 8 * kGatherRows - 1) / (8 * kGatherRows)), 256,
+                         0, st>>>(static_cast<const __nv_bfloat16 *>(x), perm, offsets, s.n, S, s.d,
+                                  s.k, xperm, err);
+        }
         const auto *W1b = static_cast<const __nv_bfloat16 *>(W1);
         const auto *W2b = static_cast<const __nv_bfloat16 *>(W2);
         cudaError_t e = pair1 ? launch_grouped_gemm_pair(s, xperm, s.d, W1b, s.h, b1, 1, ptiles,
@@ -223,7 +248,7 @@ cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *
                      : launch_grouped_gemm_tc(s, hid, s.h, W2b, s.d, b2, 0, offsets, tiles, Y, err,
                                               st);
     }
-    ffn_tiles<<<1, 1024, 0, st>>>(offsets, s.n, kSimtRows, tiles);
+    if (!prepared) ffn_tiles<<<1, 1024, 0, st>>>(offsets, s.n, kSimtRows, tiles);
     float *hid = ws_ptr<float>(ws, L.hidden);
     const unsigned max_rt = static_cast<unsigned>((S + kSB - 1) / kSB + s.n);
     grouped_gemm_simt<<<dim3(max_rt, s.h / kSB), 256, 0, st>>>(

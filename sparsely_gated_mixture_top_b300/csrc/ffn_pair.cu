@@ -60,20 +60,6 @@ constexpr int kPairThreads = 32 * (2 + kPairEpiWarps);
 constexpr int kPairKB = 2;          // 64-wide k-blocks per copy (one 3-D box)
 constexpr int kPairStages = 3;
 
-__host__ __device__ __forceinline__ void token_tiling(int R, int &tn, int &ntile) {
-    if (R <= 0) {
-        tn = 0;
-        ntile = 0;
-        return;
-    }
-    const int n0 = (R + kPairTok - 1) / kPairTok;
-    int t = (R + n0 - 1) / n0;
-    t = (t + 15) & ~15;
-    if (t > kPairTok) t = kPairTok;
-    tn = t;
-    ntile = (R + t - 1) / t;
-}
-
 struct PairCfg {
     static constexpr int kKBlockBytes = 128 * 64 * 2;           // 128 rows x one 64-wide k-block
     static constexpr int kABytes = kPairKB * kKBlockBytes;      // this CTA's 128 weight rows

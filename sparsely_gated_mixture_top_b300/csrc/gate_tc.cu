@@ -62,24 +62,27 @@ constexpr int kKBytes = 128 * 64 * 2;  // one 128 x 64 bf16 block: 16 KB
 // ---------------------------------------------------------------------------
 // Packing
 // ---------------------------------------------------------------------------
-// Block: 64 d-rows (k-block kb = blockIdx.z) x 64 chunk columns of one matrix
-// (clean or noise).  Chunk column lc of chunk `chunk` takes W column
+// Block: 16 d-rows (quarter blockIdx.z % 4 of k-block kb = blockIdx.z / 4)
+// x 64 chunk columns of one matrix (clean or noise).  Chunk column lc of
+// chunk `chunk` takes W column
 //   group_m == 0: col_base + chunk*64 + lc            (if < ncols columns)
 //   group_m  > 0: col_base + g*group_m + cl, with g = chunk / mchunks and
 //                 cl = (chunk % mchunks)*64 + lc      (if cl < group_m)
 // and zero elsewhere.  Output: for every (chunk, k-block) a 32 KB unit
 // [hi | lo], each a 128-row x 64-element bf16 tile already in the
 // 128-byte-swizzled K-major order a TMA copy would produce (16-byte group g
-// of row r stored at group g ^ (r % 8)), so that one bulk copy moves it.
-__global__ void __launch_bounds__(256) gate_pack(const float *__restrict__ Wg,
+// of row r stored at group g ^ (r % 8)), so that one bulk copy moves it; this
+// block writes the groups 2*quarter and 2*quarter + 1 of its 64 rows.
+__global__ void __launch_bounds__(128) gate_pack(const float *__restrict__ Wg,
                                                  const float *__restrict__ Wn, int d, int ldw,
                                                  int col_base, int ncols, int group_m,
                                                  int mchunks, int noisy,
                                                  uint8_t *__restrict__ pack) {
-    __shared__ float tile[64][65];
+    __shared__ float tile[16][65];
     const int chunk = blockIdx.x;
     const int which = blockIdx.y;  // 0 clean, 1 noise
-    const int d0 = blockIdx.z * 64;
+    const int kb = blockIdx.z >> 2, quarter = blockIdx.z & 3;
+    const int d0 = kb * 64 + quarter * 16;
     const float *W = which ? Wn : Wg;
     const int tx = threadIdx.x % 64, ty = threadIdx.x / 64;
     int src;
@@ -91,34 +94,33 @@ __global__ void __launch_bounds__(256) gate_pack(const float *__restrict__ Wg,
         const int cl = (chunk - g * mchunks) * kGateChunk + tx;
         src = cl < group_m ? col_base + g * group_m + cl : -1;
     }
-    for (int r = ty; r < 64; r += 4) {
+    for (int r = ty; r < 16; r += 2) {
         float v = 0.0f;
         if (src >= 0 && (which == 0 || noisy)) v = W[static_cast<int64_t>(d0 + r) * ldw + src];
         tile[r][tx] = v;  // tile[d][col]
     }
     __syncthreads();
-    // Output: 64 rows (one per column) x 8 groups of 8 d-values; each thread
-    // writes whole 16-byte groups of hi and of lo.
-    const int64_t unit = (static_cast<int64_t>(chunk) * (d / 64) + blockIdx.z) * 2 * kKBytes;
-    for (int o = threadIdx.x; o < 64 * 8; o += 256) {
-        const int cc = o >> 3, g = o & 7;
-        uint32_t hi[4], lo[4];
+    // Output: this thread's row (one per column) and one 16-byte group of 8
+    // d-values, written for hi and for lo.
+    const int64_t unit = (static_cast<int64_t>(chunk) * (d / 64) + kb) * 2 * kKBytes;
+    const int cc = threadIdx.x >> 1, gl = threadIdx.x & 1;
+    const int g = 2 * quarter + gl;
+    uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float v0 = tile[g * 8 + 2 * e][cc], v1 = tile[g * 8 + 2 * e + 1][cc];
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
-            const __nv_bfloat16 l0 = __float2bfloat16_rn(v0 - __bfloat162float(h0));
-            const __nv_bfloat16 l1 = __float2bfloat16_rn(v1 - __bfloat162float(h1));
-            hi[e] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-                    (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-            lo[e] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
-                    (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
-        }
-        const int rr = which * 64 + cc;
-        const int off = rr * 128 + ((g ^ (rr & 7)) << 4);
-        *reinterpret_cast<uint4 *>(pack + unit + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(pack + unit + kKBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    for (int e = 0; e < 4; ++e) {
+        const float v0 = tile[gl * 8 + 2 * e][cc], v1 = tile[gl * 8 + 2 * e + 1][cc];
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(v0 - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(v1 - __bfloat162float(h1));
+        hi[e] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+        lo[e] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+                (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
     }
+    const int rr = which * 64 + cc;
+    const int off = rr * 128 + ((g ^ (rr & 7)) << 4);
+    *reinterpret_cast<uint4 *>(pack + unit + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4 *>(pack + unit + kKBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -738,7 +740,7 @@ cudaError_t launch_gate_tc_load(const moe_shape &s, const void *x, const float *
     ga.c_out = c_out;
     ga.s_out = s_out;
     ga.vk_out = vk_out;
-    gate_pack<<<dim3(ga.chunks, 2, kblocks), 256, 0, st>>>(Wg, Wn, s.d, s.n, 0, s.n, 0, 1, 1, pack);
+    gate_pack<<<dim3(ga.chunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wn, s.d, s.n, 0, s.n, 0, 1, 1, pack);
     CUtensorMap mx;
     if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
         return cudaErrorInvalidValue;
@@ -773,7 +775,7 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
         ga.k = ga.kk = ga.kf = s.k;
         ga.ncols = s.n;
         ga.chunks = chunks_of(s.n);
-        gate_pack<<<dim3(ga.chunks, 2, kblocks), 256, 0, st>>>(Wg, Wnp, s.d, C, 0, s.n, 0, 1,
+        gate_pack<<<dim3(ga.chunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wnp, s.d, C, 0, s.n, 0, 1,
                                                              noisy, pack);
         CUtensorMap mx;
         if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
@@ -795,7 +797,7 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
     gp.k = gp.kk = gp.kf = kg;
     gp.ncols = Gn;
     gp.chunks = pchunks;
-    gate_pack<<<dim3(pchunks, 2, kblocks), 256, 0, st>>>(Wg, Wnp, s.d, C, 0, Gn, 0, 1, noisy, pack);
+    gate_pack<<<dim3(pchunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wnp, s.d, C, 0, Gn, 0, 1, noisy, pack);
     CUtensorMap mx;
     if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
         return cudaErrorInvalidValue;
@@ -823,7 +825,7 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
     e = launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), perm_g, offsets_g, Gn, P, s.d, kg,
                            xg, err, st);
     if (e != cudaSuccess) return e;
-    gate_pack<<<dim3(Gn * mchunks, 2, kblocks), 256, 0, st>>>(Wg, Wnp, s.d, C, Gn, s.n, m, mchunks,
+    gate_pack<<<dim3(Gn * mchunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wnp, s.d, C, Gn, s.n, m, mchunks,
                                                             noisy, pack_i);
     CUtensorMap mg;
     if (!gate_map(&mg, xg, s.d, static_cast<uint64_t>(P), resident ? kblocks : 1))

@@ -23,6 +23,9 @@ struct WsHeader {
     int32_t aux1;
 };
 constexpr size_t kWsHeaderBytes = 256;
+// int32 in the header counting the blocks of a launch that have finished
+// (the last one does the launch's serial tail and resets it to 0).
+constexpr size_t kWsDoneCounterOffset = 64;
 
 __device__ __forceinline__ void report(int32_t *err_word, int32_t code, int32_t site,
                                        int32_t aux = 0) {

@@ -27,6 +27,23 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool gate_tc_supported(const moe_shape &s);
 size_t gate_tc_pack_bytes(const moe_shape &s);
 
+// Token tiling of the pair FFN for an expert with R rows: ceil(R / 256) tiles
+// of tn rows, tn = ceil(R / tiles) rounded up to 16 (at most 256); the tile
+// count is then ceil(R / tn), so no tile is empty.
+__host__ __device__ inline void token_tiling(int R, int &tn, int &ntile) {
+    if (R <= 0) {
+        tn = 0;
+        ntile = 0;
+        return;
+    }
+    const int n0 = (R + 255) / 256;
+    int t = (R + n0 - 1) / n0;
+    t = (t + 15) & ~15;
+    if (t > 256) t = 256;
+    tn = t;
+    ntile = (R + t - 1) / t;
+}
+
 // Entries of the pair FFN's token-tile table: an expert of R rows has at most
 // ceil(R / 256) tiles.
 inline size_t pair_tile_capacity(int64_t S, int n) { return static_cast<size_t>(S / 256 + n + 1); }
@@ -40,8 +57,8 @@ struct WsLayout {
                             // their weights (hierarchical tensor-core gate only)
     size_t local_rank = 0;  // [S] int32, rank of a slot among same-expert slots of its chunk
     size_t chunk = 0;       // [chunks, n] int32, per-chunk expert counts, then bases
-    size_t chunk_imp = 0;   // [chunks, n] double, per-chunk gate-weight sums
-    size_t imp64 = 0;       // [n] double, importance accumulated in fp64
+    size_t chunk_imp = 0;   // [chunks, n] float, per-chunk gate-weight sums
+    size_t imp_acc = 0;     // [n] float, importance summed over the chunks
     size_t counts = 0;      // [n] int32 (used when the caller does not pass counts)
     size_t offsets = 0;     // [n + 1] int32
     size_t perm = 0;        // [S] int32
@@ -76,8 +93,8 @@ inline WsLayout ws_layout(const moe_shape &s) {
     L.gsel = take(tc_gate && s.groups > 0 ? static_cast<size_t>(s.T) * s.k_groups * 8 : 0);
     L.local_rank = take(S * 4);
     L.chunk = take(chunks * n * 4);
-    L.chunk_imp = take(chunks * n * 8);
-    L.imp64 = take(n * 8);
+    L.chunk_imp = take(chunks * n * 4);
+    L.imp_acc = take(n * 4);
     L.counts = take(n * 4);
     L.offsets = take((n + 1) * 4);
     L.perm = take(S * 4);
@@ -109,15 +126,33 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
                            const float *bg, const float *eps, int32_t *idx, float *G, void *ws,
                            const WsLayout &L, cudaStream_t st);
 
+// Extra outputs the forward pass takes from its dispatch: the x rows in
+// expert order (bf16) and the schedules of the expert stage's GEMMs, built in
+// the same launches instead of launches of their own.
+struct DispatchExtras {
+    const __nv_bfloat16 *x = nullptr;   // gather x[perm[r] / k] into xperm[r] when set
+    __nv_bfloat16 *xperm = nullptr;
+    int32_t *rtiles = nullptr;          // row-tile starts for bm-row tiles (when set)
+    int bm = 0;
+    int32_t *ptiles = nullptr;          // pair token-tile starts and table (when set)
+    int4 *plist = nullptr;
+};
+
 cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float *G,
                             int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
                             float *importance, float *cv2, void *ws, const WsLayout &L,
-                            cudaStream_t st);
+                            cudaStream_t st, const DispatchExtras *ex = nullptr);
 
+// prepared: the dispatch already built the stage's schedules and (bf16) the x
+// rows in expert order (dispatch_extras_for_ffn), so they are not rebuilt.
 cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *perm,
                               const int32_t *offsets, const void *W1, const float *b1,
                               const void *W2, const float *b2, void *Y_slot, void *ws,
-                              const WsLayout &L, cudaStream_t st);
+                              const WsLayout &L, cudaStream_t st, bool prepared = false);
+
+// The DispatchExtras that prepare the expert stage of shape s (ffn.cu).
+DispatchExtras dispatch_extras_for_ffn(const moe_shape &s, const void *x, void *ws,
+                                       const WsLayout &L);
 
 cudaError_t launch_combine(const moe_shape &s, const void *Y_slot, const int32_t *inv_perm,
                            const float *G, void *y, int32_t *err, cudaStream_t st);

@@ -9,16 +9,20 @@
 //                   earlier slots of its chunk with the same expert (warp
 //                   __match_any + warps taken in order), the chunk's
 //                   per-expert counts and gate-weight sums (each warp's group
-//                   of <= 32 slots in fp32, the groups in fp64, slot order);
+//                   of <= 32 slots, then the groups in warp order; fp32);
 //                   route_rank_warps gives the same for n <= 512 from a
 //                   [warp][expert] table instead of 32 barrier rounds
-//   route_colscan   per expert, an exclusive scan of the counts down the
+//   route_scan      per expert, an exclusive scan of the counts down the
 //                   chunks (chunk bases), the expert's count and its
-//                   importance (chunk partials summed in chunk order)
-//   route_finish    one block: exclusive scan of the counts over the experts
-//                   (offsets), importance in fp32, population variance /
-//                   mean^2 of the importance vector (CV^2)
+//                   importance (chunk partials summed in chunk order, fp32); the
+//                   last block to finish then scans the counts over the
+//                   experts (offsets), writes importance in fp32 and the
+//                   population variance / mean^2 of the importance vector
+//                   (CV^2), and, for the forward pass, the expert stage's
+//                   tile schedules
 //   route_scatter   row = offsets[e] + chunk base + local rank: perm, inv_perm
+//                   (route_scatter_gather also copies each slot's x row to
+//                   its expert-order row for the expert stage)
 //
 // The permutation is stable and every sum has a fixed order, so the same idx
 // and G always give the same outputs bit for bit.
@@ -33,14 +37,14 @@ __global__ void __launch_bounds__(1024) route_rank(const int32_t *__restrict__ i
                                                    const float *__restrict__ G, int64_t S, int n,
                                                    int32_t *__restrict__ local_rank,
                                                    int32_t *__restrict__ chunk,
-                                                   double *__restrict__ chunk_imp, int32_t *err) {
+                                                   float *__restrict__ chunk_imp, int32_t *err) {
     extern __shared__ __align__(8) unsigned char route_sh[];
-    double *imp = reinterpret_cast<double *>(route_sh);              // [n]
-    int32_t *cnt = reinterpret_cast<int32_t *>(route_sh + 8 * n);     // [n]
+    float *imp = reinterpret_cast<float *>(route_sh);                // [n]
+    int32_t *cnt = reinterpret_cast<int32_t *>(route_sh + 4 * n);     // [n]
     __shared__ int32_t base_sh[32][32];
     for (int e = threadIdx.x; e < n; e += blockDim.x) {
         cnt[e] = 0;
-        imp[e] = 0.0;
+        imp[e] = 0.0f;
     }
     __syncthreads();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -60,7 +64,7 @@ __global__ void __launch_bounds__(1024) route_rank(const int32_t *__restrict__ i
     const int leader = __ffs(mask) - 1;
     const int rank_in_warp = __popc(mask & ((1u << lane) - 1u));
     // Gate weight of this lane's expert group (at most 32 slots) summed in
-    // lane order in fp32; the groups are then accumulated in fp64.
+    // lane order in fp32; the groups are then accumulated in fp32 in warp order.
     float seg = 0.0f;
 #pragma unroll
     for (int src = 0; src < 32; ++src) {
@@ -73,13 +77,13 @@ __global__ void __launch_bounds__(1024) route_rank(const int32_t *__restrict__ i
         if (warp == w && lane == leader && e >= 0) {
             base_sh[w][lane] = cnt[e];
             cnt[e] += __popc(mask);
-            imp[e] += static_cast<double>(seg);
+            imp[e] += seg;
         }
         __syncthreads();
     }
     if (e >= 0) local_rank[s] = base_sh[warp][leader] + rank_in_warp;
     int32_t *row = chunk + static_cast<int64_t>(blockIdx.x) * n;
-    double *irow = chunk_imp + static_cast<int64_t>(blockIdx.x) * n;
+    float *irow = chunk_imp + static_cast<int64_t>(blockIdx.x) * n;
     for (int ee = threadIdx.x; ee < n; ee += blockDim.x) {
         row[ee] = cnt[ee];
         irow[ee] = imp[ee];
@@ -88,11 +92,11 @@ __global__ void __launch_bounds__(1024) route_rank(const int32_t *__restrict__ i
 
 // Block (32 x 32): 32 experts (x) by 32 chunk segments (y).  Chunk counts
 // become chunk bases (exclusive scan down the chunks); the expert's count
-// and importance (fp64, chunk order) are the column totals.
+// and importance (fp32, chunk order) are the column totals.
 // route_rank for n <= kRankWarpsMaxN: the same outputs without the 32
 // barrier rounds.  Each warp's leaders write their group's count and fp32
 // gate-weight sum to a [32 warps][n] table; one thread per expert then walks
-// the warps in order (exclusive scan of the counts, fp64 sum of the groups,
+// the warps in order (exclusive scan of the counts, fp32 sum of the groups,
 // the same order as route_rank) and every slot reads its warp's base.
 constexpr int kRankWarpsMaxN = 512;
 
@@ -100,7 +104,7 @@ __global__ void __launch_bounds__(1024) route_rank_warps(const int32_t *__restri
                                                          const float *__restrict__ G, int64_t S,
                                                          int n, int32_t *__restrict__ local_rank,
                                                          int32_t *__restrict__ chunk,
-                                                         double *__restrict__ chunk_imp,
+                                                         float *__restrict__ chunk_imp,
                                                          int32_t *err) {
     extern __shared__ __align__(8) unsigned char route_sh[];
     int32_t *wc = reinterpret_cast<int32_t *>(route_sh);           // [32][n] counts, then bases
@@ -138,15 +142,15 @@ __global__ void __launch_bounds__(1024) route_rank_warps(const int32_t *__restri
     }
     __syncthreads();
     int32_t *row = chunk + static_cast<int64_t>(blockIdx.x) * n;
-    double *irow = chunk_imp + static_cast<int64_t>(blockIdx.x) * n;
+    float *irow = chunk_imp + static_cast<int64_t>(blockIdx.x) * n;
     for (int ee = threadIdx.x; ee < n; ee += blockDim.x) {
         int32_t run = 0;
-        double imp = 0.0;
+        float imp = 0.0f;
         for (int w = 0; w < 32; ++w) {
             const int32_t c = wc[w * n + ee];
             wc[w * n + ee] = run;
             run += c;
-            if (c) imp += static_cast<double>(wsum[w * n + ee]);
+            if (c) imp += wsum[w * n + ee];
         }
         row[ee] = run;
         irow[ee] = imp;
@@ -155,18 +159,147 @@ __global__ void __launch_bounds__(1024) route_rank_warps(const int32_t *__restri
     if (e >= 0) local_rank[s] = wc[warp * n + e] + rank_in_warp;
 }
 
-__global__ void __launch_bounds__(1024) route_colscan(int32_t *__restrict__ chunk,
-                                                      const double *__restrict__ chunk_imp,
-                                                      int chunks, int n, int32_t *__restrict__ counts,
-                                                      double *__restrict__ imp64) {
+// Exclusive scan of one int per thread over a block of 1024 threads (in
+// thread order); returns this thread's prefix, *total the block's sum.
+__device__ int32_t block_exclusive_scan_1024(int32_t v, int32_t *sh, int32_t *total) {
+    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    int32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+    }
+    if (lane == 31) sh[warp] = inc;
+    __syncthreads();
+    int32_t base = 0, all = 0;
+    for (int w = 0; w < 32; ++w) {
+        if (w < warp) base += sh[w];
+        all += sh[w];
+    }
+    __syncthreads();
+    *total = all;
+    return base + inc - v;
+}
+
+// Sum of one float per thread over a block of 1024 threads in a fixed order:
+// a shuffle tree in each warp, then a shuffle tree over the 32 warp sums in
+// warp 0; every thread gets the result.  (fp32: on this GPU a dependent fp64
+// add costs ~15x an fp32 add; a tree keeps the error near log2(1024) ulps.)
+__device__ float block_sum_1024(float v, float *sh) {
+    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) sh[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float r = sh[lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+        if (lane == 0) sh[32] = r;
+    }
+    __syncthreads();
+    const float r = sh[32];
+    __syncthreads();
+    return r;
+}
+
+struct ScanOut {
+    int32_t *counts;
+    float *imp;
+    int32_t *offsets;
+    float *importance;
+    float *cv2;
+    int32_t *rtiles;    // optional: starts of bm-row tiles per expert
+    int bm;
+    int32_t *ptiles;    // optional: pair token tiles per expert, and their table
+    int4 *plist;
+};
+
+// The serial tail of the dispatch, run by one block of 1024 threads once every
+// expert's count and importance are known: offsets = exclusive scan of the
+// counts (offsets[n] = total), importance in fp32, CV^2 = population variance
+// / mean^2 (fp32 tree sums, fixed order), and the expert stage's schedules.
+__device__ void dispatch_finish(int n, const ScanOut &o) {
+    __shared__ int32_t ish[32];
+    __shared__ float fsh[33];
+    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+    const int per = (n + 1023) / 1024;
+    const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+    int32_t sum = 0, rt = 0, pt = 0;
+    for (int i = i0; i < i1; ++i) {
+        const int32_t c = __ldcg(o.counts + i);
+        sum += c;
+        if (o.rtiles) rt += (c + o.bm - 1) / o.bm;
+        if (o.ptiles) {
+            int tn, nt;
+            token_tiling(c, tn, nt);
+            pt += nt;
+        }
+    }
+    int32_t total;
+    int32_t run = block_exclusive_scan_1024(sum, ish, &total);
+    int32_t rrun = 0, prun = 0, rtotal = 0, ptotal = 0;
+    if (o.rtiles) rrun = block_exclusive_scan_1024(rt, ish, &rtotal);
+    if (o.ptiles) prun = block_exclusive_scan_1024(pt, ish, &ptotal);
+    for (int i = i0; i < i1; ++i) {
+        const int32_t c = __ldcg(o.counts + i);
+        o.offsets[i] = run;
+        if (o.rtiles) {
+            o.rtiles[i] = rrun;
+            rrun += (c + o.bm - 1) / o.bm;
+        }
+        if (o.ptiles) {
+            o.ptiles[i] = prun;
+            int tn, nt;
+            token_tiling(c, tn, nt);
+            for (int j = 0; j < nt; ++j) {
+                const int rows = min(tn, c - j * tn);
+                o.plist[prun + j] = make_int4(i, run + j * tn, rows, (rows + 15) & ~15);
+            }
+            prun += nt;
+        }
+        run += c;
+    }
+    if (tid == 0) {
+        o.offsets[n] = total;
+        if (o.rtiles) o.rtiles[n] = rtotal;
+        if (o.ptiles) o.ptiles[n] = ptotal;
+    }
+    float sacc = 0.0f;
+    for (int e = tid; e < n; e += 1024) {
+        const float v = __ldcg(o.imp + e);
+        sacc += v;
+        o.importance[e] = v;
+    }
+    const float mean = block_sum_1024(sacc, fsh) / static_cast<float>(n);
+    float q = 0.0f;
+    for (int e = tid; e < n; e += 1024) {
+        const float v = __ldcg(o.imp + e) - mean;
+        q = fmaf(v, v, q);
+    }
+    const float var = block_sum_1024(q, fsh) / static_cast<float>(n);
+    if (tid == 0) o.cv2[0] = mean != 0.0f ? var / (mean * mean) : 0.0f;
+}
+
+// Block (32 x 32): 32 experts (x) by 32 chunk segments (y).  Chunk counts
+// become chunk bases (exclusive scan down the chunks); the expert's count
+// and importance (fp32, chunk order) are the column totals.  The last block
+// to finish (a counter in the workspace header, reset by that block) then
+// runs dispatch_finish.
+__global__ void __launch_bounds__(1024) route_scan(int32_t *__restrict__ chunk,
+                                                   const float *__restrict__ chunk_imp, int chunks,
+                                                   int n, ScanOut o, int32_t *done) {
     __shared__ int32_t part[32][33];
-    __shared__ double ipart[32][33];
+    __shared__ float ipart[32][33];
+    __shared__ int is_last;
     const int tx = threadIdx.x, ty = threadIdx.y;
     const int e = blockIdx.x * 32 + tx;
     const int seg = (chunks + 31) / 32;
     const int b0 = ty * seg, b1 = min(chunks, b0 + seg);
     int32_t sum = 0;
-    double isum = 0.0;
+    float isum = 0.0f;
     if (e < n)
         for (int b = b0; b < b1; ++b) {
             sum += chunk[static_cast<int64_t>(b) * n + e];
@@ -177,7 +310,7 @@ __global__ void __launch_bounds__(1024) route_colscan(int32_t *__restrict__ chun
     __syncthreads();
     if (ty == 0) {
         int32_t run = 0;
-        double irun = 0.0;
+        float irun = 0.0f;
         for (int y = 0; y < 32; ++y) {
             const int32_t v = part[y][tx];
             part[y][tx] = run;
@@ -185,8 +318,8 @@ __global__ void __launch_bounds__(1024) route_colscan(int32_t *__restrict__ chun
             irun += ipart[y][tx];
         }
         if (e < n) {
-            counts[e] = run;
-            imp64[e] = irun;
+            o.counts[e] = run;
+            o.imp[e] = irun;
         }
     }
     __syncthreads();
@@ -199,63 +332,15 @@ __global__ void __launch_bounds__(1024) route_colscan(int32_t *__restrict__ chun
             run += v;
         }
     }
-}
-
-// Sum over the 256 threads of the block in a fixed order (warp shuffle tree,
-// then the 8 warp sums in warp order); every thread gets the result.
-__device__ double block_sum_256(double v, double *sh) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+    // Publish this block's results, then count it; the last block sees all.
+    __threadfence();
     __syncthreads();
-    double r = 0.0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) r += sh[w];
+    if (tx == 0 && ty == 0) is_last = atomicAdd(done, 1) == static_cast<int>(gridDim.x) - 1;
     __syncthreads();
-    return r;
-}
-
-// One block of 256 threads: offsets = exclusive scan of counts (offsets[n] =
-// total), importance in fp32, and CV^2 = population variance / mean^2.
-__global__ void __launch_bounds__(256) route_finish(const int32_t *__restrict__ counts,
-                                                    const double *__restrict__ imp64, int n,
-                                                    int32_t *__restrict__ offsets,
-                                                    float *__restrict__ importance,
-                                                    float *__restrict__ cv2) {
-    __shared__ int32_t wsum[8];
-    __shared__ double sh[8];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int per = (n + 255) / 256;
-    const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
-    int32_t sum = 0;
-    for (int i = i0; i < i1; ++i) sum += counts[i];
-    // exclusive scan of the per-thread sums: warp shuffles, then the warps
-    int32_t inc = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += v;
-    }
-    if (lane == 31) wsum[warp] = inc;
-    __syncthreads();
-    int32_t base = 0;
-    for (int w = 0; w < warp; ++w) base += wsum[w];
-    int32_t run = base + inc - sum;
-    for (int i = i0; i < i1; ++i) {
-        offsets[i] = run;
-        run += counts[i];
-    }
-    if (threadIdx.x == 255) offsets[n] = base + inc;
-    double s = 0.0;
-    for (int e = threadIdx.x; e < n; e += 256) {
-        s += imp64[e];
-        importance[e] = static_cast<float>(imp64[e]);
-    }
-    const double mean = block_sum_256(s, sh) / n;
-    double q = 0.0;
-    for (int e = threadIdx.x; e < n; e += 256) q += (imp64[e] - mean) * (imp64[e] - mean);
-    const double var = block_sum_256(q, sh) / n;
-    if (threadIdx.x == 0) cv2[0] = mean != 0.0 ? static_cast<float>(var / (mean * mean)) : 0.0f;
+    if (!is_last) return;
+    __threadfence();
+    dispatch_finish(n, o);
+    if (tx == 0 && ty == 0) *done = 0;
 }
 
 __global__ void route_scatter(const int32_t *__restrict__ idx, int64_t S, int n,
@@ -276,12 +361,51 @@ __global__ void route_scatter(const int32_t *__restrict__ idx, int64_t S, int n,
     if (s >= offsets[n]) perm[s] = -1;  // rows left empty by invalid slots
 }
 
+// route_scatter with each token's x row copied to the expert-order rows of
+// its k slots (xperm[row] = x[t]): one warp per token, lane j < k handles
+// slot t*k + j, and the row is read once (16-byte loads) and stored k times.
+constexpr int kScatterTokensPerBlock = 8;
+
+__global__ void __launch_bounds__(256) route_scatter_gather(
+    const int32_t *__restrict__ idx, int64_t T, int n, int k, int d,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ chunk,
+    const int32_t *__restrict__ local_rank, int32_t *__restrict__ perm,
+    int32_t *__restrict__ inv_perm, const __nv_bfloat16 *__restrict__ x,
+    __nv_bfloat16 *__restrict__ xperm) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kScatterTokensPerBlock + threadIdx.x / 32;
+    if (t >= T) return;
+    const int total = offsets[n];
+    // the x row's first pieces are requested before the routing lookups
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + t * static_cast<int64_t>(d));
+    const int nv = d / 8;
+    uint4 v0 = lane < nv ? __ldg(src + lane) : make_uint4(0, 0, 0, 0);
+    uint4 v1 = lane + 32 < nv ? __ldg(src + lane + 32) : make_uint4(0, 0, 0, 0);
+    int32_t row = -1;
+    if (lane < k) {
+        const int64_t s = t * k + lane;
+        const int e = idx[s];
+        if (e >= 0 && e < n) row = offsets[e] + chunk[(s / kRouteChunk) * n + e] + local_rank[s];
+        if (row >= 0) perm[row] = static_cast<int32_t>(s);
+        inv_perm[s] = row;
+        if (s >= total) perm[s] = -1;  // rows left empty by invalid slots
+    }
+    for (int j = 0; j < k; ++j) {
+        const int32_t r = __shfl_sync(0xffffffffu, row, j);
+        if (r < 0) continue;
+        uint4 *dst = reinterpret_cast<uint4 *>(xperm + static_cast<int64_t>(r) * d);
+        if (lane < nv) dst[lane] = v0;
+        if (lane + 32 < nv) dst[lane + 32] = v1;
+        for (int c = lane + 64; c < nv; c += 32) dst[c] = __ldg(src + c);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float *G,
                             int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
                             float *importance, float *cv2, void *ws, const WsLayout &L,
-                            cudaStream_t st) {
+                            cudaStream_t st, const DispatchExtras *ex) {
     const int64_t S = slots(s);
     const int n = s.n;
     int32_t *err = ws_ptr<int32_t>(ws, 0);
@@ -295,8 +419,8 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
     const int chunks = static_cast<int>((S + kRouteChunk - 1) / kRouteChunk);
     int32_t *local_rank = ws_ptr<int32_t>(ws, L.local_rank);
     int32_t *chunk = ws_ptr<int32_t>(ws, L.chunk);
-    double *chunk_imp = ws_ptr<double>(ws, L.chunk_imp);
-    double *imp64 = ws_ptr<double>(ws, L.imp64);
+    float *chunk_imp = ws_ptr<float>(ws, L.chunk_imp);
+    float *imp_acc = ws_ptr<float>(ws, L.imp_acc);
     // Dynamic shared memory above the default 48 KB needs an opt-in, which
     // belongs to the current device's context: it is set before each launch.
     if (n <= kRankWarpsMaxN) {
@@ -309,7 +433,7 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
         route_rank_warps<<<chunks, 1024, smem, st>>>(idx, G, S, n, local_rank, chunk, chunk_imp,
                                                      err);
     } else {
-        const size_t smem = 12 * static_cast<size_t>(n);  // n doubles and n ints (+4 KB static)
+        const size_t smem = 8 * static_cast<size_t>(n);  // n floats and n ints (+4 KB static)
         if (smem + 4096 > 48 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(
                 route_rank, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -317,10 +441,24 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
         }
         route_rank<<<chunks, 1024, smem, st>>>(idx, G, S, n, local_rank, chunk, chunk_imp, err);
     }
-    route_colscan<<<(n + 31) / 32, dim3(32, 32), 0, st>>>(chunk, chunk_imp, chunks, n, counts, imp64);
-    route_finish<<<1, 256, 0, st>>>(counts, imp64, n, offsets, importance, cv2);
-    route_scatter<<<static_cast<unsigned>((S + 255) / 256), 256, 0, st>>>(
-        idx, S, n, offsets, chunk, local_rank, perm, inv_perm);
+    ScanOut o{counts, imp_acc, offsets, importance, cv2, nullptr, 0, nullptr, nullptr};
+    if (ex) {
+        o.rtiles = ex->rtiles;
+        o.bm = ex->bm;
+        o.ptiles = ex->ptiles;
+        o.plist = ex->plist;
+    }
+    int32_t *done = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kWsDoneCounterOffset);
+    route_scan<<<(n + 31) / 32, dim3(32, 32), 0, st>>>(chunk, chunk_imp, chunks, n, o, done);
+    if (ex && ex->x) {
+        route_scatter_gather<<<static_cast<unsigned>((s.T + kScatterTokensPerBlock - 1) /
+                                                     kScatterTokensPerBlock),
+                               256, 0, st>>>(idx, s.T, n, s.k, s.d, offsets, chunk, local_rank,
+                                             perm, inv_perm, ex->x, ex->xperm);
+    } else {
+        route_scatter<<<static_cast<unsigned>((S + 255) / 256), 256, 0, st>>>(
+            idx, S, n, offsets, chunk, local_rank, perm, inv_perm);
+    }
     return cudaGetLastError();
 }
 

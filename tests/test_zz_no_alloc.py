@@ -81,14 +81,14 @@ def test_noalloc_dispatch_matches_numpy_and_workspace_dispatch_twice():
         assert abs(got["cv2"].item() - ref["cv2"].item()) <= TOL_CV2 * abs(ref["cv2"].item())
 
 
-# n = 800 experts and S = 612 full chunks of 1024 slots: 256 + 4*S + 12*612*n
-# + 8*n bytes, every term a multiple of 256, is exactly 8 MiB.
-_AT_LIMIT = (626688 // 4, 800, 4)
+# n = 704 experts and S = 862 full chunks of 1024 slots: 256 + 4*S + 8*862*n
+# + 4*n bytes, every term a multiple of 256, is exactly 8 MiB.
+_AT_LIMIT = (882688 // 4, 704, 4)
 
 
 def test_noalloc_dispatch_at_its_scratch_limit():
     T, n, k = _AT_LIMIT
-    assert 256 + 4 * T * k + 12 * (T * k // 1024) * n + 8 * n == 8 << 20
+    assert 256 + 4 * T * k + 8 * (T * k // 1024) * n + 4 * n == 8 << 20
     s = B.make_shape(T, 64, 64, n, k)
     idx, G = _routing_inputs(T, n, k, 3)
     got = _noalloc(s, idx, G, T, n, k)
