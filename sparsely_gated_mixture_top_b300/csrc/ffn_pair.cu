@@ -245,8 +245,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 const PairUnit u = unit_of(tcur, q % nmt);
                 if (q + ncl < total) tcur = __ldg(tlist + (q + ncl) / nmt);
                 const uint32_t idesc = idesc_bf16_f32(kPairM, u.N);
-                if (!mbar_wait_cluster_bounded(tempty(acc), acc_phase ^ 1u, abort_flag, err,
-                                               kSiteTcMma))
+                if (!mbar_wait_bounded(tempty(acc), acc_phase ^ 1u, abort_flag, err, kSiteTcMma))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kPairTok);
@@ -296,12 +295,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         int acc = 0;
         uint32_t acc_phase = 0;
+        // the unit's table entry and bias value are loaded one unit ahead
+        const int fq = static_cast<int>(rank) * 128 + quad * 32 + lane;   // feature in the block
+        auto bias_of = [&](int4 t, int q) {
+            return bias ? __ldg(bias + static_cast<int64_t>(t.x) * Nout + (q % nmt) * kPairM + fq)
+                        : 0.0f;
+        };
         int4 tcur = cl < total ? __ldg(tlist + cl / nmt) : make_int4(0, 0, 0, 0);
+        float bnext = cl < total ? bias_of(tcur, cl) : 0.0f;
         for (int q = cl; q < total; q += ncl) {
             const PairUnit u = unit_of(tcur, q % nmt);
-            if (q + ncl < total) tcur = __ldg(tlist + (q + ncl) / nmt);
+            const float bv = bnext;
+            if (q + ncl < total) {
+                tcur = __ldg(tlist + (q + ncl) / nmt);
+                bnext = bias_of(tcur, q + ncl);
+            }
             const int col0 = u.mt * kPairM + static_cast<int>(rank) * 128 + quad * 32;
-            const float bv = bias ? __ldg(bias + static_cast<int64_t>(u.e) * Nout + col0 + lane) : 0.0f;
             if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, err, kSiteTcEpilogue)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + lane_addr + static_cast<uint32_t>(acc * kPairTok);
@@ -330,7 +339,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
+            if (lane == 0) mbar_arrive_remote(mapa_shared(tempty(acc), 0));
             // Phase 2: per chunk, a 32 x 32 transpose through shared memory
             // (element (t, lane) of rows of 64 bytes whose four 16-byte pieces
             // are permuted by (t >> 1) & 3), then 64-byte row stores.

@@ -76,7 +76,7 @@ constexpr int kKBytes = 128 * 64 * 2;  // one 128 x 64 bf16 block: 16 KB
 __global__ void __launch_bounds__(128) gate_pack(const float *__restrict__ Wg,
                                                  const float *__restrict__ Wn, int d, int ldw,
                                                  int col_base, int ncols, int group_m,
-                                                 int mchunks, int noisy,
+                                                 int mchunks, int noisy, int pair,
                                                  uint8_t *__restrict__ pack) {
     __shared__ float tile[16][65];
     const int chunk = blockIdx.x;
@@ -118,9 +118,21 @@ __global__ void __launch_bounds__(128) gate_pack(const float *__restrict__ Wg,
                 (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
     }
     const int rr = which * 64 + cc;
-    const int off = rr * 128 + ((g ^ (rr & 7)) << 4);
-    *reinterpret_cast<uint4 *>(pack + unit + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4 *>(pack + unit + kKBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    if (!pair) {
+        const int off = rr * 128 + ((g ^ (rr & 7)) << 4);
+        *reinterpret_cast<uint4 *>(pack + unit + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(pack + unit + kKBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    } else {
+        // CTA-pair layout: per (chunk, half) the k-blocks in order, each
+        // [hi 64 rows | lo 64 rows] (16 KB), so that one SM of a pair copies
+        // its half (clean or noise columns) of two k-blocks in one 32 KB box.
+        const int64_t hunit =
+            ((static_cast<int64_t>(chunk) * 2 + which) * (d / 64) + kb) * kKBytes;
+        const int off = cc * 128 + ((g ^ (cc & 7)) << 4);
+        *reinterpret_cast<uint4 *>(pack + hunit + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(pack + hunit + kKBytes / 2 + off) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -190,12 +202,13 @@ __device__ __forceinline__ void softmax_top(const TopK<KM> &t, int kk, float (&w
 constexpr int kGateEpiWarps = 8;  // two per tensor-memory lane quarter
 constexpr int kGateThreads = 32 * (2 + kGateEpiWarps);
 
-template <bool kResident, int KM>
+template <bool kResident, int KM, bool kPair = false>
 struct GateCfg {
     // Stage: the hi and lo W tiles of one (chunk, k-block) unit (plus, when x
-    // is not resident, that k-block of x).
+    // is not resident, that k-block of x).  CTA pair: this SM's half (64
+    // columns) of the hi and lo tiles of two k-blocks, 32 KB.
     static constexpr int kStages = kResident ? 2 : 3;
-    static constexpr int kStageBytes = kResident ? 2 * kKBytes : 3 * kKBytes;
+    static constexpr int kStageBytes = kPair ? 2 * kKBytes : (kResident ? 2 * kKBytes : 3 * kKBytes);
     static constexpr int kXBytes = kResident ? 8 * kKBytes : 0;  // d <= 512
     // Exchange of the final lists of half 1, [slot][row] order.
     static constexpr int kXchBytes = KM * kGateRows * 8;
@@ -262,12 +275,12 @@ struct GateTile {
     int g, row0, rows;
 };
 
-template <bool kGrouped>
-__device__ __forceinline__ GateTile gate_tile(int tile, const GateArgs &a) {
+template <bool kGrouped, bool kPair = false>
+__device__ __forceinline__ GateTile gate_tile(int tile, const GateArgs &a, uint32_t rank = 0) {
     GateTile ti;
     if (!kGrouped) {
         ti.g = 0;
-        ti.row0 = tile * kGateRows;
+        ti.row0 = tile * (kPair ? 2 : 1) * kGateRows + static_cast<int>(rank) * kGateRows;
         const int64_t left = a.T - ti.row0;
         ti.rows = left < kGateRows ? static_cast<int>(left) : kGateRows;
     } else {
@@ -288,11 +301,20 @@ __device__ __forceinline__ GateTile gate_tile(int tile, const GateArgs &a) {
 
 // KM: list size (>= kk).  kGrouped: rows are (token, rank) pairs of one group
 // per tile, scored against that group's columns.
-template <bool kResident, bool kGrouped, int KM>
+// kPair (flat, resident x only): a cluster of two CTAs scores 256 rows, 128
+// per CTA, with one M = 256 MMA whose N = 128 columns are split over the two
+// SMs: the even CTA supplies the 64 clean-score columns of each W tile, the
+// odd one the 64 noise-score columns.  Each SM so streams half of W, two
+// k-blocks per copy (mapW: the packed W viewed as rows of 128 bytes); both
+// CTAs' copies complete on the even CTA's barriers, which issues the MMAs and
+// commits to the barriers of both.  Each CTA's accumulator holds its 128
+// rows x all 128 columns, so the epilogue is the same.
+template <bool kResident, bool kGrouped, int KM, bool kPair = false>
 __global__ void __launch_bounds__(kGateThreads, 1)
     gate_tc(const __grid_constant__ CUtensorMap mapX, const uint8_t *__restrict__ wpack,
-            const GateArgs a) {
-    using Cfg = GateCfg<kResident, KM>;
+            const GateArgs a, const __grid_constant__ CUtensorMap mapW) {
+    static_assert(!kPair || (kResident && !kGrouped), "pair gate: flat, resident x");
+    using Cfg = GateCfg<kResident, KM, kPair>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -323,7 +345,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         }
         for (int b = 0; b < NA; ++b) {
             mbar_init(tfull(b), 1);
-            mbar_init(tempty(b), 32 * kGateEpiWarps);
+            mbar_init(tempty(b), (kPair ? 2 : 1) * kGateEpiWarps);   // one arrival per epilogue warp
         }
         mbar_init(xfull, 1);
         mbar_init(xempty, 1);
@@ -331,17 +353,39 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) tma_prefetch_map(&mapX);
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
-        tmem_relinquish();
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&mapX);
+        if (kPair) tma_prefetch_map(&mapW);
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    uint32_t rank = 0;
+    if constexpr (kPair) {
+        rank = cluster_ctarank();
+        // the pair allocation needs both CTAs running (first barrier) and is
+        // published to both before any copy, MMA or remote arrival (second)
+        cluster_sync();
+        if (warp == 1) {
+            tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
+            tmem_relinquish_pair();
+        }
+        tc_fence_before();
+        cluster_sync();
+        tc_fence_after();
+    } else {
+        if (warp == 1) {
+            tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
     const uint32_t tmem_base = *tmem_slot;
+    // tiles of 128 rows (single CTA) or 256 rows (pair: 128 per CTA)
     const int tiles = kGrouped ? a.tiles_g[a.groups]
-                               : static_cast<int>((a.T + kGateRows - 1) / kGateRows);
+                               : static_cast<int>((a.T + (kPair ? 2 : 1) * kGateRows - 1) /
+                                                  ((kPair ? 2 : 1) * kGateRows));
+    const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int tstep = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     const int kblocks = a.d / kGateBK;
 
     if (warp == 0) {
@@ -351,8 +395,8 @@ __global__ void __launch_bounds__(kGateThreads, 1)
             uint32_t phase = 0, xphase = 0;
             bool ok = true;
             int64_t issued = 0;
-            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-                const GateTile ti = gate_tile<kGrouped>(tile, a);
+            for (int tile = tile0; tile < tiles && ok; tile += tstep) {
+                const GateTile ti = gate_tile<kGrouped, kPair>(tile, a, rank);
                 if (kResident) {
                     if (!mbar_wait_bounded(xempty, xphase ^ 1u, abort_flag, a.err, kSiteTcProducer)) {
                         ok = false;
@@ -360,10 +404,39 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                     }
                     xphase ^= 1u;
                     // the whole x tile (all k-blocks) in one 3-D copy
-                    mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(kblocks * kKBytes));
-                    tma_load_3d(smem_u32(sX), &mapX, xfull, 0, ti.row0, 0);
+                    if constexpr (kPair) {
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(2 * kblocks * kKBytes));
+                        tma_load_3d_pair(smem_u32(sX), &mapX, mapa_shared(xfull, 0), 0, ti.row0, 0);
+                    } else {
+                        mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(kblocks * kKBytes));
+                        tma_load_3d(smem_u32(sX), &mapX, xfull, 0, ti.row0, 0);
+                    }
                 }
                 const int64_t unit0 = static_cast<int64_t>(ti.g) * a.chunks;
+                if constexpr (kPair) {
+                    // this SM's half of two k-blocks of each chunk per stage
+                    for (int c = 0; c < a.chunks && ok; ++c) {
+                        for (int kb = 0; kb < kblocks && ok; kb += 2) {
+                            if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, a.err,
+                                                   kSiteTcProducer)) {
+                                ok = false;
+                                break;
+                            }
+                            if (rank == 0) mbar_arrive_expect_tx(full(stage), 2 * Cfg::kStageBytes);
+                            const int wrow = static_cast<int>(
+                                (((unit0 + c) * 2 + rank) * kblocks + kb) * (kKBytes / 128));
+                            tma_load_2d_pair(smem_u32(sS + stage * Cfg::kStageBytes), &mapW,
+                                             mapa_shared(full(stage), 0), 0, wrow);
+                            ++issued;
+                            if (++stage == S) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                    }
+                    continue;
+                }
                 for (int c = 0; c < a.chunks && ok; ++c) {
                     for (int kb = 0; kb < kblocks && ok; ++kb) {
                         if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, a.err,
@@ -389,7 +462,11 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                     }
                 }
             }
-            if (!ok) {  // let issued copies land before the CTA exits
+            if (!ok && kPair) {  // copies complete on the even CTA's barriers: give them time
+                const uint64_t t0 = global_ns();
+                while (global_ns() - t0 < 200000ull) {
+                }
+            } else if (!ok) {  // let issued copies land before the CTA exits
                 const int outstanding = static_cast<int>(issued < S ? issued : S);
                 int s = stage;
                 uint32_t p = phase;
@@ -411,14 +488,75 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ----------------------------
-        if (lane == 0) {
+        if (kPair && lane == 0 && rank == 0) {
+            // pair MMAs M = 256 (128 rows of each CTA) x N = 128 (64 columns
+            // from each CTA), hi then lo, two k-blocks per stage
+            constexpr uint32_t idesc = idesc_bf16_f32(256, 128);
+            int stage = 0;
+            uint32_t phase = 0, xphase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = tile0; tile < tiles && ok; tile += tstep) {
+                if (!mbar_wait_bounded(xfull, xphase, abort_flag, a.err, kSiteTcMma)) break;
+                xphase ^= 1u;
+                for (int c = 0; c < a.chunks && ok; ++c) {
+                    if (!mbar_wait_bounded(tempty(acc), acc_phase ^ 1u, abort_flag, a.err,
+                                           kSiteTcMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 128);
+                    for (int kb = 0; kb < kblocks && ok; kb += 2) {
+                        if (!mbar_wait_bounded(full(stage), phase, abort_flag, a.err, kSiteTcMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t st = smem_u32(sS + stage * Cfg::kStageBytes);
+                        const int nkb = min(2, kblocks - kb);
+                        for (int j = 0; j < nkb; ++j) {
+                            const uint32_t xa = smem_u32(sX + (kb + j) * kKBytes);
+                            const uint32_t wb = st + j * kKBytes;   // [hi 8 KB | lo 8 KB]
+#pragma unroll
+                            for (int kk = 0; kk < kGateBK / 16; ++kk)  // x . W_hi
+                                tc_mma_f16_pair(d_tmem, sdesc_kmajor_sw128(xa + kk * 32),
+                                                sdesc_kmajor_sw128(wb + kk * 32), idesc,
+                                                (kb | j | kk) != 0 ? 1u : 0u);
+#pragma unroll
+                            for (int kk = 0; kk < kGateBK / 16; ++kk)  // + x . W_lo
+                                tc_mma_f16_pair(d_tmem, sdesc_kmajor_sw128(xa + kk * 32),
+                                                sdesc_kmajor_sw128(wb + kKBytes / 2 + kk * 32),
+                                                idesc, 1u);
+                        }
+                        tc_commit_pair_both(empty(stage));
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    tc_commit_pair_both(tfull(acc));
+                    if (++acc == NA) {
+                        acc = 0;
+                        acc_phase ^= 1u;
+                    }
+                }
+                if (ok) tc_commit_pair_both(xempty);
+            }
+            tc_commit_pair_both(drain_bar);
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(drain_bar, 0) && global_ns() - t0 < kWaitLimitNs) {
+            }
+        } else if (!kPair && lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
             int stage = 0;
             uint32_t phase = 0, xphase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            for (int tile = tile0; tile < tiles && ok; tile += tstep) {
                 if (kResident) {
                     if (!mbar_wait_bounded(xfull, xphase, abort_flag, a.err, kSiteTcMma)) break;
                     xphase ^= 1u;
@@ -484,8 +622,8 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-            const GateTile ti = gate_tile<kGrouped>(tile, a);
+        for (int tile = tile0; tile < tiles; tile += tstep) {
+            const GateTile ti = gate_tile<kGrouped, kPair>(tile, a, rank);
             const bool valid = r < ti.rows;
             // The row's token, its output slots and the score columns it reads.
             int64_t t = ti.row0 + r;
@@ -536,9 +674,15 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                         tmem_ld_32x32b_x16(tmem_base + lane_addr + col, cv);
                         tmem_ld_32x32b_x16(tmem_base + lane_addr + col + 64, nv);
                         tmem_ld_wait();
-                        if (piece == 1) {
+                        if (piece == 1) {  // this warp's part of the accumulator is read
                             tc_fence_before();
-                            mbar_arrive(tempty(acc));  // this half of the accumulator is read
+                            __syncwarp();
+                            if (lane == 0) {
+                                if (kPair)
+                                    mbar_arrive_remote(mapa_shared(tempty(acc), 0));
+                                else
+                                    mbar_arrive(tempty(acc));
+                            }
                         }
                         // Pass 1 (branch-free): the noisy score of every column and
                         // which ones beat the k-th entry of the list.  Within a
@@ -632,10 +776,18 @@ __global__ void __launch_bounds__(kGateThreads, 1)
             }
         }
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    if constexpr (kPair) {
+        __syncwarp();
+        tc_fence_before();
+        cluster_sync();   // no pair MMA, remote arrival or tensor-memory read is left
+        tc_fence_after();
+        if (warp == 1) tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    } else {
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
 }
 
 // --- host side --------------------------------------------------------------
@@ -680,8 +832,60 @@ cudaError_t launch_gate_tc_t(const CUtensorMap &mx, const uint8_t *wpack, const 
     const cudaError_t attr = cudaFuncSetAttribute(
         gate_tc<kResident, kGrouped, KM>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (attr != cudaSuccess) return attr;
-    gate_tc<kResident, kGrouped, KM><<<grid, kGateThreads, Cfg::kSmem, st>>>(mx, wpack, ga);
+    gate_tc<kResident, kGrouped, KM><<<grid, kGateThreads, Cfg::kSmem, st>>>(mx, wpack, ga, mx);
     return cudaGetLastError();
+}
+
+// Packed W in the pair layout viewed as rows of 128 bytes (64 bf16, no
+// swizzle: the bytes are already in the order the MMA reads), boxes of 256
+// rows = 32 KB = one SM's half of two k-blocks.
+bool gate_pair_wmap(CUtensorMap *m, const void *pack, size_t bytes) {
+    EncodeTiledFn enc = gate_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(bytes / 128)};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {64, 256};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pack), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KM>
+cudaError_t launch_gate_pair_t(const CUtensorMap &mx, const CUtensorMap &mw, const uint8_t *wpack,
+                               const GateArgs &ga, int pairs, cudaStream_t st) {
+    using Cfg = GateCfg<true, KM, true>;
+    auto kern = gate_tc<true, false, KM, true>;
+    const cudaError_t attr =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (attr != cudaSuccess) return attr;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(kGateThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mx, wpack, ga, mw);
+}
+
+// The CTA-pair gate serves flat gating with x resident (d <= 512).
+cudaError_t launch_gate_pair(int km, const CUtensorMap &mx, const uint8_t *wpack, size_t pack_bytes,
+                             const GateArgs &ga, cudaStream_t st) {
+    CUtensorMap mw;
+    if (!gate_pair_wmap(&mw, wpack, pack_bytes)) return cudaErrorInvalidValue;
+    const int64_t tiles = (ga.T + 2 * kGateRows - 1) / (2 * kGateRows);
+    const int64_t maxp = sm_count() / 2;
+    const int pairs = static_cast<int>(tiles < maxp ? tiles : maxp);
+    if (km <= 2) return launch_gate_pair_t<2>(mx, mw, wpack, ga, pairs, st);
+    if (km <= 4) return launch_gate_pair_t<4>(mx, mw, wpack, ga, pairs, st);
+    if (km <= 8) return launch_gate_pair_t<8>(mx, mw, wpack, ga, pairs, st);
+    return launch_gate_pair_t<16>(mx, mw, wpack, ga, pairs, st);
 }
 
 template <bool kGrouped>
@@ -740,7 +944,7 @@ cudaError_t launch_gate_tc_load(const moe_shape &s, const void *x, const float *
     ga.c_out = c_out;
     ga.s_out = s_out;
     ga.vk_out = vk_out;
-    gate_pack<<<dim3(ga.chunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wn, s.d, s.n, 0, s.n, 0, 1, 1, pack);
+    gate_pack<<<dim3(ga.chunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wn, s.d, s.n, 0, s.n, 0, 1, 1, 0, pack);
     CUtensorMap mx;
     if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
         return cudaErrorInvalidValue;
@@ -775,11 +979,15 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
         ga.k = ga.kk = ga.kf = s.k;
         ga.ncols = s.n;
         ga.chunks = chunks_of(s.n);
+        const bool pair = resident;
         gate_pack<<<dim3(ga.chunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wnp, s.d, C, 0, s.n, 0, 1,
-                                                             noisy, pack);
+                                                             noisy, pair ? 1 : 0, pack);
         CUtensorMap mx;
         if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
             return cudaErrorInvalidValue;
+        if (pair)
+            return launch_gate_pair(s.k, mx, pack,
+                                    static_cast<size_t>(ga.chunks) * kblocks * 2 * kKBytes, ga, st);
         const int tiles = static_cast<int>((s.T + kGateRows - 1) / kGateRows);
         return launch_gate_tc_km<false>(resident, s.k, mx, pack, ga, tiles < sms ? tiles : sms, st);
     }
@@ -797,12 +1005,17 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
     gp.k = gp.kk = gp.kf = kg;
     gp.ncols = Gn;
     gp.chunks = pchunks;
-    gate_pack<<<dim3(pchunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wnp, s.d, C, 0, Gn, 0, 1, noisy, pack);
+    const bool gpair = resident;
+    gate_pack<<<dim3(pchunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wnp, s.d, C, 0, Gn, 0, 1, noisy,
+                                                          gpair ? 1 : 0, pack);
     CUtensorMap mx;
     if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
         return cudaErrorInvalidValue;
     const int ttiles = static_cast<int>((s.T + kGateRows - 1) / kGateRows);
-    cudaError_t e = launch_gate_tc_km<false>(resident, kg, mx, pack, gp, ttiles < sms ? ttiles : sms, st);
+    cudaError_t e =
+        gpair ? launch_gate_pair(kg, mx, pack, static_cast<size_t>(pchunks) * kblocks * 2 * kKBytes,
+                                 gp, st)
+              : launch_gate_tc_km<false>(resident, kg, mx, pack, gp, ttiles < sms ? ttiles : sms, st);
     if (e != cudaSuccess) return e;
 
     // pass 2: route the pairs by group, gather their x rows, score each group's columns
@@ -826,7 +1039,7 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
                            xg, err, st);
     if (e != cudaSuccess) return e;
     gate_pack<<<dim3(Gn * mchunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wnp, s.d, C, Gn, s.n, m, mchunks,
-                                                            noisy, pack_i);
+                                                            noisy, 0, pack_i);
     CUtensorMap mg;
     if (!gate_map(&mg, xg, s.d, static_cast<uint64_t>(P), resident ? kblocks : 1))
         return cudaErrorInvalidValue;

@@ -286,9 +286,20 @@ __device__ __forceinline__ void cluster_sync() {
 
 // Arrive once, with release semantics at cluster scope, on an mbarrier given
 // by its shared::cluster address (possibly in another CTA of the cluster).
+// The release waits until this thread's earlier memory operations (global
+// stores included) are visible cluster-wide.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
+}
+
+// Arrive once on an mbarrier given by its shared::cluster address with the
+// default (CTA-scope release) semantics: used to hand tensor memory back to
+// the pair's MMA issuer after tcgen05.fence::before_thread_sync, where only
+// the tensor-memory reads must be ordered, so the arrive does not wait for
+// this thread's global stores.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -331,6 +342,17 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// 2-D tensor copy into this CTA's shared memory whose completion is counted
+// on an mbarrier of the pair's even CTA (shared::cluster address `bar`).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
 }
 
