@@ -199,8 +199,10 @@ __device__ __forceinline__ void softmax_top(const TopK<KM> &t, int kk, float (&w
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-constexpr int kGateEpiWarps = 8;  // two per tensor-memory lane quarter
+constexpr int kGateParts = 4;                        // epilogue warps per lane quarter
+constexpr int kGateEpiWarps = 4 * kGateParts;
 constexpr int kGateThreads = 32 * (2 + kGateEpiWarps);
+constexpr int kPartCols = kGateChunk / kGateParts;   // 16 score columns per part and chunk
 
 template <bool kResident, int KM, bool kPair = false>
 struct GateCfg {
@@ -210,12 +212,13 @@ struct GateCfg {
     static constexpr int kStages = kResident ? 2 : 3;
     static constexpr int kStageBytes = kPair ? 2 * kKBytes : (kResident ? 2 * kKBytes : 3 * kKBytes);
     static constexpr int kXBytes = kResident ? 8 * kKBytes : 0;  // d <= 512
-    // Exchange of the final lists of half 1, [slot][row] order.
-    static constexpr int kXchBytes = KM * kGateRows * 8;
+    // Exchange of two parts' final lists at a time, [list][slot][row] order.
+    static constexpr int kXchBytes = 2 * KM * kGateRows * 8;
     static constexpr int kAcc = 4;  // accumulators (128 columns each)
     static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kAcc + 3) + 16;
     static constexpr int kSmem = kXBytes + kStages * kStageBytes + kXchBytes + 1024 + kBarBytes;
     static constexpr uint32_t kTmemCols = 128 * kAcc;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
 struct GateArgs {
@@ -251,13 +254,14 @@ __device__ __forceinline__ void epi_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kGateEpiWarps) : "memory");
 }
 
-// eps[row][col0 + j] for the 32 columns j of one chunk half (0 past C).
+// eps[row][col0 + j] for the NC columns j of one chunk part (0 past C).
 // Vector loads when the row stride and col0 allow 16-byte alignment.
-__device__ __forceinline__ void load_eps32(const float *__restrict__ row, int col0, int C,
-                                           bool vec, float (&ev)[32]) {
+template <int NC>
+__device__ __forceinline__ void load_eps(const float *__restrict__ row, int col0, int C, bool vec,
+                                         float (&ev)[NC]) {
     if (vec) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < NC / 4; ++q) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (col0 + 4 * q < C) v = __ldg(reinterpret_cast<const float4 *>(row + col0 + 4 * q));
             ev[4 * q] = v.x;
@@ -267,7 +271,7 @@ __device__ __forceinline__ void load_eps32(const float *__restrict__ row, int co
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ev[j] = (col0 + j < C) ? __ldg(row + col0 + j) : 0.0f;
+        for (int j = 0; j < NC; ++j) ev[j] = (col0 + j < C) ? __ldg(row + col0 + j) : 0.0f;
     }
 }
 
@@ -321,8 +325,8 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     uint8_t *sX = smem;                 // resident x tile (kResident)
     uint8_t *sS = smem + Cfg::kXBytes;  // stage ring
     uint8_t *sXch = sS + Cfg::kStages * Cfg::kStageBytes;
-    float *xch_v = reinterpret_cast<float *>(sXch);
-    int *xch_i = reinterpret_cast<int *>(sXch + KM * kGateRows * 4);
+    float *xch_v = reinterpret_cast<float *>(sXch);                        // [2][KM][rows]
+    int *xch_i = reinterpret_cast<int *>(sXch + 2 * KM * kGateRows * 4);   // [2][KM][rows]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sXch + Cfg::kXchBytes);
     constexpr int S = Cfg::kStages;
     constexpr int NA = Cfg::kAcc;
@@ -610,12 +614,12 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         }
     } else {
         // ------------------------------ epilogue ------------------------------
-        // Warp w (2..9) reads tensor-memory lanes 32*(w%4).. (row r of the
-        // tile) and column half `half` of every chunk: clean columns
-        // half*32 .. +32 and the matching noise columns 64 + half*32 .. +32.
-        // Each thread keeps the running top-k of its half; the halves merge
-        // through shared memory at the end of the tile.
-        const int half = (warp - 2) >> 2;
+        // Warp w (2..17) reads tensor-memory lanes 32*(w%4).. (row r of the
+        // tile) and part `part` (0..3) of every chunk: clean columns
+        // part*16 .. +16 and the matching noise columns 64 + part*16 .. +16.
+        // Each thread keeps the running top-k of its part; the four parts of
+        // a row merge through shared memory at the end of the tile.
+        const int part = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
@@ -650,95 +654,97 @@ __global__ void __launch_bounds__(kGateThreads, 1)
             TopK<KM> list;
             list.reset();
             for (int c = 0; c < a.chunks; ++c) {
-                const int col0 = c * kGateChunk + half * 32;  // list column of this half
+                const int col0 = c * kGateChunk + part * kPartCols;  // list column of this part
                 if (eps_row && c + 2 < a.chunks && col0 + 2 * kGateChunk < a.ncols)
                     prefetch_l2(eps_row + col0 + 2 * kGateChunk);
-                float ev[32];
+                float ev[kPartCols];
                 if (eps_row && col0 < a.ncols) {
-                    load_eps32(eps_row, col0, a.ncols, vec_eps, ev);
+                    load_eps<kPartCols>(eps_row, col0, a.ncols, vec_eps, ev);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) ev[j] = 0.0f;
+                    for (int j = 0; j < kPartCols; ++j) ev[j] = 0.0f;
                 }
+                // the gate biases of this part's columns, one per lane (read back by shuffles)
+                const float bgl = bg_row && lane < kPartCols && col0 + lane < a.ncols
+                                      ? __ldg(bg_row + col0 + lane)
+                                      : 0.0f;
                 if (ok && !mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, a.err,
                                              kSiteTcEpilogue))
                     ok = false;
-                ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the votes below need every lane
+                ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the shuffles below need every lane
                 if (ok) {
                     tc_fence_after();
                     const float thr = list.kth(a.kf);  // fixed for the span
+                    uint32_t cv[16], nv[16];
+                    const uint32_t col = static_cast<uint32_t>(acc * 128 + part * kPartCols);
+                    tmem_ld_32x32b_x16(tmem_base + lane_addr + col, cv);
+                    tmem_ld_32x32b_x16(tmem_base + lane_addr + col + 64, nv);
+                    tmem_ld_wait();
+                    // this warp's part of the accumulator is read
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (kPair)
+                            mbar_arrive_remote(mapa_shared(tempty(acc), 0));
+                        else
+                            mbar_arrive(tempty(acc));
+                    }
+                    if (a.c_out) {  // load mode: clean score, noise scale
+                        // (warp-uniform branch: the bias shuffles need every
+                        // lane; only the stores depend on the row)
+                        float *crow = a.c_out + t * a.ncols + col0;
+                        float *srow = a.s_out + t * a.ncols + col0;
 #pragma unroll
-                    for (int piece = 0; piece < 2; ++piece) {
-                        uint32_t cv[16], nv[16];
-                        const uint32_t col = static_cast<uint32_t>(acc * 128 + half * 32 + piece * 16);
-                        tmem_ld_32x32b_x16(tmem_base + lane_addr + col, cv);
-                        tmem_ld_32x32b_x16(tmem_base + lane_addr + col + 64, nv);
-                        tmem_ld_wait();
-                        if (piece == 1) {  // this warp's part of the accumulator is read
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) {
-                                if (kPair)
-                                    mbar_arrive_remote(mapa_shared(tempty(acc), 0));
-                                else
-                                    mbar_arrive(tempty(acc));
+                        for (int q = 0; q < 4; ++q) {  // four columns at a time
+                            float cc[4], ss[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = 4 * q + e;
+                                cc[e] = __uint_as_float(cv[j]) + __shfl_sync(0xffffffffu, bgl, j);
+                                ss[e] = softplus_fast(__uint_as_float(nv[j]));
                             }
-                        }
-                        // Pass 1 (branch-free): the noisy score of every column and
-                        // which ones beat the k-th entry of the list.  Within a
-                        // thread's list the columns arrive in increasing index order,
-                        // so an equal score never displaces an entry: '>' is exact.
-                        // Rows past the tile flag nothing but still take part in the
-                        // votes.
-                        if (a.c_out && valid) {  // load mode: clean score, noise scale
-                            const int cb = col0 + piece * 16;
-                            float *crow = a.c_out + t * a.ncols + cb;
-                            float *srow = a.s_out + t * a.ncols + cb;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {  // four columns at a time
-                                float cc[4], ss[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int j = 4 * q + e;
-                                    cc[e] = __uint_as_float(cv[j]) +
-                                            (bg_row && cb + j < a.ncols ? __ldg(bg_row + cb + j) : 0.0f);
-                                    ss[e] = softplus_fast(__uint_as_float(nv[j]));
+                            if (!valid) continue;
+                            if ((a.ncols & 3) == 0) {  // 16-byte rows: float4 stores
+                                if (col0 + 4 * q < a.ncols) {
+                                    reinterpret_cast<float4 *>(crow)[q] = make_float4(cc[0], cc[1], cc[2], cc[3]);
+                                    reinterpret_cast<float4 *>(srow)[q] = make_float4(ss[0], ss[1], ss[2], ss[3]);
                                 }
-                                if ((a.ncols & 3) == 0) {  // 16-byte rows: float4 stores
-                                    if (cb + 4 * q < a.ncols) {
-                                        reinterpret_cast<float4 *>(crow)[q] = make_float4(cc[0], cc[1], cc[2], cc[3]);
-                                        reinterpret_cast<float4 *>(srow)[q] = make_float4(ss[0], ss[1], ss[2], ss[3]);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    if (col0 + 4 * q + e < a.ncols) {
+                                        crow[4 * q + e] = cc[e];
+                                        srow[4 * q + e] = ss[e];
                                     }
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e)
-                                        if (cb + 4 * q + e < a.ncols) {
-                                            crow[4 * q + e] = cc[e];
-                                            srow[4 * q + e] = ss[e];
-                                        }
-                                }
                             }
                         }
-                        uint32_t pass = 0;
+                    }
+                    // Pass 1 (branch-free): the noisy score of every column and
+                    // which ones beat the k-th entry of the list.  Within a
+                    // thread's list the columns arrive in increasing index order,
+                    // so an equal score never displaces an entry: '>' is exact.
+                    // Rows past the tile flag nothing.
+                    uint32_t pass = 0;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int sc = col0 + piece * 16 + j;
-                            float h = __uint_as_float(cv[j]);
-                            if (bg_row && sc < a.ncols) h += __ldg(bg_row + sc);
-                            if (noisy) h += ev[piece * 16 + j] * softplus_fast(__uint_as_float(nv[j]));
-                            cv[j] = __float_as_uint(h);
-                            if (valid && sc < a.ncols && h > thr) pass |= 1u << j;
-                        }
-                        // Pass 2 (rare): insert the flagged columns.  The warp vote
-                        // keeps each column's insertion a real branch.
-                        if (__any_sync(0xffffffffu, pass != 0)) {
+                    for (int j = 0; j < 16; ++j) {
+                        const int sc = col0 + j;
+                        float h = __uint_as_float(cv[j]) + __shfl_sync(0xffffffffu, bgl, j);
+                        if (noisy) h += ev[j] * softplus_fast(__uint_as_float(nv[j]));
+                        cv[j] = __float_as_uint(h);
+                        if (valid && sc < a.ncols && h > thr) pass |= 1u << j;
+                    }
+                    // Pass 2 (rare after the first chunk): each lane inserts its
+                    // own flagged columns in increasing index order; the score
+                    // leaves the register list through a compile-time select
+                    // chain, so the list stays in registers.
+                    while (pass != 0u) {
+                        const int j = __ffs(pass) - 1;
+                        pass &= pass - 1u;
+                        float hv = __uint_as_float(cv[0]);
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                if (!__any_sync(0xffffffffu, (pass >> j) & 1u)) continue;
-                                if ((pass >> j) & 1u)
-                                    list.insert(__uint_as_float(cv[j]), col0 + piece * 16 + j);
-                            }
-                        }
+                        for (int q = 1; q < 16; ++q)
+                            if (q == j) hv = __uint_as_float(cv[q]);
+                        list.insert(hv, col0 + j);
                     }
                 }
                 if (++acc == NA) {
@@ -746,9 +752,26 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                     acc_phase ^= 1u;
                 }
             }
-            // half 1 hands its list to half 0, which merges and writes the row
-            epi_bar();  // half 0 is done with the previous tile's exchange
-            if (half == 1) {
+            // The four parts of a row merge in two rounds: parts 2 and 3 hand
+            // their lists to parts 0 and 1, then part 1 to part 0, which
+            // writes the row.  Every epilogue thread takes part in the barriers.
+            epi_bar();  // the previous tile's exchange is read
+            if (part >= 2) {
+#pragma unroll
+                for (int q = 0; q < KM; ++q) {
+                    xch_v[((part - 2) * KM + q) * kGateRows + r] = list.v[q];
+                    xch_i[((part - 2) * KM + q) * kGateRows + r] = list.i[q];
+                }
+            }
+            epi_bar();
+            if (part < 2 && ok && valid) {
+#pragma unroll
+                for (int q = 0; q < KM; ++q)
+                    list.insert(xch_v[(part * KM + q) * kGateRows + r],
+                                xch_i[(part * KM + q) * kGateRows + r]);
+            }
+            epi_bar();
+            if (part == 1) {
 #pragma unroll
                 for (int q = 0; q < KM; ++q) {
                     xch_v[q * kGateRows + r] = list.v[q];
@@ -756,7 +779,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                 }
             }
             epi_bar();
-            if (half == 0 && ok && valid) {
+            if (part == 0 && ok && valid) {
 #pragma unroll
                 for (int q = 0; q < KM; ++q)
                     list.insert(xch_v[q * kGateRows + r], xch_i[q * kGateRows + r]);
