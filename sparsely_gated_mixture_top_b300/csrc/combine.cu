@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const T *__restrict__ Y,
                                                       int d, int k, int64_t S,
                                                       T *__restrict__ y, int32_t *err) {
     constexpr int V = Vec<T>::N;
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
     if (t >= T_) return;
     const int lane = threadIdx.x & 31;
@@ -133,16 +135,16 @@ cudaError_t launch_combine(const moe_shape &s, const void *Y_slot, const int32_t
         const auto *Yb = static_cast<const __nv_bfloat16 *>(Y_slot);
         auto *yb = static_cast<__nv_bfloat16 *>(y);
         if (s.k <= 4)
-            combine_kernel<__nv_bfloat16, 4><<<blocks, 256, 0, st>>>(Yb, inv_perm, G, s.T, s.d, s.k, S, yb, err);
+            return launch_pdl(combine_kernel<__nv_bfloat16, 4>, dim3(blocks), dim3(256), 0, st, Yb, inv_perm, G, s.T, s.d, s.k, S, yb, err);
         else
-            combine_kernel<__nv_bfloat16, MOE_MAX_K><<<blocks, 256, 0, st>>>(Yb, inv_perm, G, s.T, s.d, s.k, S, yb, err);
+            return launch_pdl(combine_kernel<__nv_bfloat16, MOE_MAX_K>, dim3(blocks), dim3(256), 0, st, Yb, inv_perm, G, s.T, s.d, s.k, S, yb, err);
     } else {
         const auto *Yf = static_cast<const float *>(Y_slot);
         auto *yf = static_cast<float *>(y);
         if (s.k <= 4)
-            combine_kernel<float, 4><<<blocks, 256, 0, st>>>(Yf, inv_perm, G, s.T, s.d, s.k, S, yf, err);
+            return launch_pdl(combine_kernel<float, 4>, dim3(blocks), dim3(256), 0, st, Yf, inv_perm, G, s.T, s.d, s.k, S, yf, err);
         else
-            combine_kernel<float, MOE_MAX_K><<<blocks, 256, 0, st>>>(Yf, inv_perm, G, s.T, s.d, s.k, S, yf, err);
+            return launch_pdl(combine_kernel<float, MOE_MAX_K>, dim3(blocks), dim3(256), 0, st, Yf, inv_perm, G, s.T, s.d, s.k, S, yf, err);
     }
     return cudaGetLastError();
 }

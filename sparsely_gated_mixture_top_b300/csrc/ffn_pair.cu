@@ -192,6 +192,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // everything above is local; from here on the previous kernel's results are used
+    pdl_wait();
+    pdl_launch_dependents();
 
     const int nmt = Nout / kPairM;
     const int total = tiles[n] * nmt;
@@ -439,9 +442,9 @@ cudaError_t launch_grouped_gemm_pair(const moe_shape &s, const __nv_bfloat16 *X,
     if (pairs > max_units) pairs = max_units;
     if (pairs < 1) pairs = 1;
     const int out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
-    ffn_pair_gemm<<<static_cast<unsigned>(2 * pairs), kPairThreads, PairCfg::kSmem, st>>>(
-        mW, mX, tiles, tlist, s.n, K, Nout, W, X, bias, relu, out, out_v8, err);
-    return cudaGetLastError();
+    return launch_pdl(ffn_pair_gemm, dim3(static_cast<unsigned>(2 * pairs)), dim3(kPairThreads),
+                      PairCfg::kSmem, st, mW, mX, tiles, tlist, s.n, K, Nout, W, X, bias, relu, out,
+                      out_v8, err);
 }
 
 }  // namespace moe

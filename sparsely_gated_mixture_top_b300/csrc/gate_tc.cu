@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(128) gate_pack(const float *__restrict__ Wg,
                                                  int mchunks, int noisy, int pair,
                                                  uint8_t *__restrict__ pack) {
     __shared__ float tile[16][65];
+    pdl_wait();
+    pdl_launch_dependents();
     const int chunk = blockIdx.x;
     const int which = blockIdx.y;  // 0 clean, 1 noise
     const int kb = blockIdx.z >> 2, quarter = blockIdx.z & 3;
@@ -384,6 +386,9 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         tc_fence_after();
     }
     const uint32_t tmem_base = *tmem_slot;
+    // everything above is local; from here on the previous kernel's results are used
+    pdl_wait();
+    pdl_launch_dependents();
     // tiles of 128 rows (single CTA) or 256 rows (pair: 128 per CTA)
     const int tiles = kGrouped ? a.tiles_g[a.groups]
                                : static_cast<int>((a.T + (kPair ? 2 : 1) * kGateRows - 1) /
@@ -855,8 +860,8 @@ cudaError_t launch_gate_tc_t(const CUtensorMap &mx, const uint8_t *wpack, const 
     const cudaError_t attr = cudaFuncSetAttribute(
         gate_tc<kResident, kGrouped, KM>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (attr != cudaSuccess) return attr;
-    gate_tc<kResident, kGrouped, KM><<<grid, kGateThreads, Cfg::kSmem, st>>>(mx, wpack, ga, mx);
-    return cudaGetLastError();
+    return launch_pdl(gate_tc<kResident, kGrouped, KM>, dim3(grid), dim3(kGateThreads), Cfg::kSmem, st,
+                      mx, wpack, ga, mx);
 }
 
 // Packed W in the pair layout viewed as rows of 128 bytes (64 bf16, no
@@ -887,13 +892,15 @@ cudaError_t launch_gate_pair_t(const CUtensorMap &mx, const CUtensorMap &mw, con
     cfg.blockDim = dim3(kGateThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmem;
     cfg.stream = st;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, mx, wpack, ga, mw);
 }
 
@@ -967,7 +974,10 @@ cudaError_t launch_gate_tc_load(const moe_shape &s, const void *x, const float *
     ga.c_out = c_out;
     ga.s_out = s_out;
     ga.vk_out = vk_out;
-    gate_pack<<<dim3(ga.chunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wn, s.d, s.n, 0, s.n, 0, 1, 1, 0, pack);
+    {
+        const cudaError_t pe = launch_pdl(gate_pack, dim3(ga.chunks, 2, 4 * kblocks), dim3(128), 0, st, Wg, Wn, s.d, s.n, 0, s.n, 0, 1, 1, 0, pack);
+        if (pe != cudaSuccess) return pe;
+    }
     CUtensorMap mx;
     if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
         return cudaErrorInvalidValue;
@@ -1003,8 +1013,11 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
         ga.ncols = s.n;
         ga.chunks = chunks_of(s.n);
         const bool pair = resident;
-        gate_pack<<<dim3(ga.chunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wnp, s.d, C, 0, s.n, 0, 1,
+        {
+            const cudaError_t pe = launch_pdl(gate_pack, dim3(ga.chunks, 2, 4 * kblocks), dim3(128), 0, st, Wg, Wnp, s.d, C, 0, s.n, 0, 1,
                                                              noisy, pair ? 1 : 0, pack);
+            if (pe != cudaSuccess) return pe;
+        }
         CUtensorMap mx;
         if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
             return cudaErrorInvalidValue;
@@ -1029,8 +1042,11 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
     gp.ncols = Gn;
     gp.chunks = pchunks;
     const bool gpair = resident;
-    gate_pack<<<dim3(pchunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wnp, s.d, C, 0, Gn, 0, 1, noisy,
+    {
+        const cudaError_t pe = launch_pdl(gate_pack, dim3(pchunks, 2, 4 * kblocks), dim3(128), 0, st, Wg, Wnp, s.d, C, 0, Gn, 0, 1, noisy,
                                                           gpair ? 1 : 0, pack);
+        if (pe != cudaSuccess) return pe;
+    }
     CUtensorMap mx;
     if (!gate_map(&mx, x, s.d, static_cast<uint64_t>(s.T), resident ? kblocks : 1))
         return cudaErrorInvalidValue;
@@ -1061,8 +1077,11 @@ cudaError_t launch_gate_tc(const moe_shape &s, const void *x, const float *Wg, c
     e = launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), perm_g, offsets_g, Gn, P, s.d, kg,
                            xg, err, st);
     if (e != cudaSuccess) return e;
-    gate_pack<<<dim3(Gn * mchunks, 2, 4 * kblocks), 128, 0, st>>>(Wg, Wnp, s.d, C, Gn, s.n, m, mchunks,
+    {
+        const cudaError_t pe = launch_pdl(gate_pack, dim3(Gn * mchunks, 2, 4 * kblocks), dim3(128), 0, st, Wg, Wnp, s.d, C, Gn, s.n, m, mchunks,
                                                             noisy, 0, pack_i);
+        if (pe != cudaSuccess) return pe;
+    }
     CUtensorMap mg;
     if (!gate_map(&mg, xg, s.d, static_cast<uint64_t>(P), resident ? kblocks : 1))
         return cudaErrorInvalidValue;

@@ -393,6 +393,20 @@ __device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream is still
+// running; pdl_wait() blocks until that kernel has finished and its memory
+// is visible, so it comes before the first access to anything the previous
+// kernel writes or reads.  pdl_launch_dependents() lets the next kernel of
+// the stream be scheduled (it will itself wait in pdl_wait()).  Both are
+// no-ops for a kernel launched without the attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Numeric helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float softplus_f(float z) {

@@ -12,6 +12,26 @@
 
 namespace moe {
 
+// Launches `kern` on `st` with programmatic stream serialization (the kernel
+// calls pdl_wait() before touching what earlier kernels of the stream
+// produce), so that its launch and prologue overlap the previous kernel's
+// tail.  Cluster dimensions compiled into the kernel still apply.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+}
+
 constexpr int kRouteChunk = 1024;  // slots ranked per block by the routing kernels
 constexpr int kTcRows = 128;       // rows per tensor-core FFN tile (MMA M)
 constexpr int kSimtRows = 64;      // rows per fp32 SIMT FFN tile

@@ -39,6 +39,8 @@ __global__ void __launch_bounds__(1024) route_rank(const int32_t *__restrict__ i
                                                    int32_t *__restrict__ chunk,
                                                    float *__restrict__ chunk_imp, int32_t *err) {
     extern __shared__ __align__(8) unsigned char route_sh[];
+    pdl_wait();
+    pdl_launch_dependents();
     float *imp = reinterpret_cast<float *>(route_sh);                // [n]
     int32_t *cnt = reinterpret_cast<int32_t *>(route_sh + 4 * n);     // [n]
     __shared__ int32_t base_sh[32][32];
@@ -107,6 +109,8 @@ __global__ void __launch_bounds__(1024) route_rank_warps(const int32_t *__restri
                                                          float *__restrict__ chunk_imp,
                                                          int32_t *err) {
     extern __shared__ __align__(8) unsigned char route_sh[];
+    pdl_wait();
+    pdl_launch_dependents();
     int32_t *wc = reinterpret_cast<int32_t *>(route_sh);           // [32][n] counts, then bases
     float *wsum = reinterpret_cast<float *>(route_sh + 128 * n);    // [32][n] group sums
     for (int i = threadIdx.x; i < 32 * n; i += blockDim.x) {
@@ -294,6 +298,8 @@ __global__ void __launch_bounds__(1024) route_scan(int32_t *__restrict__ chunk,
     __shared__ int32_t part[32][33];
     __shared__ float ipart[32][33];
     __shared__ int is_last;
+    pdl_wait();
+    pdl_launch_dependents();
     const int tx = threadIdx.x, ty = threadIdx.y;
     const int e = blockIdx.x * 32 + tx;
     const int seg = (chunks + 31) / 32;
@@ -348,6 +354,8 @@ __global__ void route_scatter(const int32_t *__restrict__ idx, int64_t S, int n,
                               const int32_t *__restrict__ chunk,
                               const int32_t *__restrict__ local_rank, int32_t *__restrict__ perm,
                               int32_t *__restrict__ inv_perm) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t s = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (s >= S) return;
     const int e = idx[s];
@@ -372,6 +380,8 @@ __global__ void __launch_bounds__(256) route_scatter_gather(
     const int32_t *__restrict__ local_rank, int32_t *__restrict__ perm,
     int32_t *__restrict__ inv_perm, const __nv_bfloat16 *__restrict__ x,
     __nv_bfloat16 *__restrict__ xperm) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kScatterTokensPerBlock + threadIdx.x / 32;
     if (t >= T) return;
@@ -430,8 +440,9 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
                 route_rank_warps, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
             if (e != cudaSuccess) return e;
         }
-        route_rank_warps<<<chunks, 1024, smem, st>>>(idx, G, S, n, local_rank, chunk, chunk_imp,
-                                                     err);
+        cudaError_t e = launch_pdl(route_rank_warps, dim3(chunks), dim3(1024), smem, st, idx, G, S, n,
+                                   local_rank, chunk, chunk_imp, err);
+        if (e != cudaSuccess) return e;
     } else {
         const size_t smem = 8 * static_cast<size_t>(n);  // n floats and n ints (+4 KB static)
         if (smem + 4096 > 48 * 1024) {
@@ -439,7 +450,9 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
                 route_rank, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
             if (e != cudaSuccess) return e;
         }
-        route_rank<<<chunks, 1024, smem, st>>>(idx, G, S, n, local_rank, chunk, chunk_imp, err);
+        cudaError_t e = launch_pdl(route_rank, dim3(chunks), dim3(1024), smem, st, idx, G, S, n,
+                                   local_rank, chunk, chunk_imp, err);
+        if (e != cudaSuccess) return e;
     }
     ScanOut o{counts, imp_acc, offsets, importance, cv2, nullptr, 0, nullptr, nullptr};
     if (ex) {
@@ -449,17 +462,20 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
         o.plist = ex->plist;
     }
     int32_t *done = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kWsDoneCounterOffset);
-    route_scan<<<(n + 31) / 32, dim3(32, 32), 0, st>>>(chunk, chunk_imp, chunks, n, o, done);
+    cudaError_t e = launch_pdl(route_scan, dim3((n + 31) / 32), dim3(32, 32), 0, st, chunk,
+                               chunk_imp, chunks, n, o, done);
+    if (e != cudaSuccess) return e;
     if (ex && ex->x) {
-        route_scatter_gather<<<static_cast<unsigned>((s.T + kScatterTokensPerBlock - 1) /
-                                                     kScatterTokensPerBlock),
-                               256, 0, st>>>(idx, s.T, n, s.k, s.d, offsets, chunk, local_rank,
-                                             perm, inv_perm, ex->x, ex->xperm);
+        e = launch_pdl(route_scatter_gather,
+                       dim3(static_cast<unsigned>((s.T + kScatterTokensPerBlock - 1) /
+                                                  kScatterTokensPerBlock)),
+                       dim3(256), 0, st, idx, s.T, n, s.k, s.d, offsets, chunk, local_rank, perm,
+                       inv_perm, ex->x, ex->xperm);
     } else {
-        route_scatter<<<static_cast<unsigned>((S + 255) / 256), 256, 0, st>>>(
-            idx, S, n, offsets, chunk, local_rank, perm, inv_perm);
+        e = launch_pdl(route_scatter, dim3(static_cast<unsigned>((S + 255) / 256)), dim3(256), 0, st,
+                       idx, S, n, offsets, chunk, local_rank, perm, inv_perm);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace moe
