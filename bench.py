@@ -64,7 +64,7 @@ def parse():
     return p.parse_args()
 
 
-TRAFFIC_BENCH = "python bench.py --steps 3 --warmup 3 --e2e-steps 3 --no-cpu-baseline"
+TRAFFIC_BENCH = "python bench.py --steps 3 --warmup 3 --e2e-steps 3 --no-cpu-baseline --no-per-workload"
 TRAFFIC_NCU = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
                "--clock-control none -k regex:ffn_ -s 12 -c 4 --csv --log-file traffic.csv ")
 
@@ -93,7 +93,7 @@ def traffic_summary(csv_path: str, bench_json: str, w: wl.Workload) -> dict:
     return {
         "workload": w.name,
         "what": "DRAM bytes (read + write) of the four launches of one expert-FFN stage "
-                "(moe_expert_ffn), first timed step",
+                "(moe_expert_ffn: token-tile table, gather, two pair GEMMs), stage timing call",
         "command": f"{TRAFFIC_BENCH} (exit 0), then: {TRAFFIC_NCU}{TRAFFIC_BENCH}",
         "source_sha256": source_digest(),
         "ffn_stage_dram_bytes_per_launch": total,
@@ -116,7 +116,7 @@ def peaks():
         return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
 
 
-FFN_STAGE_SOURCES = ("ffn.cu", "ffn_tc.cu", "moe_device.cuh", "moe_launch.h")
+FFN_STAGE_SOURCES = ("ffn.cu", "ffn_tc.cu", "ffn_pair.cu", "moe_device.cuh", "moe_launch.h")
 
 
 def source_digest() -> str:
@@ -433,21 +433,41 @@ def config_of(w: wl.Workload) -> dict:
 # GPU arm
 # ---------------------------------------------------------------------------
 def launches_per_step(w: wl.Workload) -> int:
-    """Kernels moe_forward launches per step: gate (pack + scores/top-k),
-    dispatch (rank, column scan, finish, scatter), expert FFN (tile table,
-    gather + two grouped GEMMs in bf16; two SIMT GEMMs in fp32), combine."""
-    gate, dispatch, combine = 2, 4, 1
-    ffn = 4 if w.dtype == "bf16" else 3
-    return gate + dispatch + ffn + combine
+    """Kernels moe_forward launches per step.  Flat gating: gate (weight pack,
+    scores + KeepTopK) 2, dispatch (rank, column scan + tables, scatter with
+    the x-row gather) 3, expert FFN (two grouped GEMMs; their tables come from
+    the dispatch) 2, combine 1.  Hierarchical gating adds to the gate: the
+    group pass (pack, scores + KeepTopK), a dispatch of the (token, group)
+    pairs (3), their row tiles, the gather of their x rows, and the in-group
+    pass (pack, scores + KeepTopK)."""
+    gate = 2 if not w.groups else 2 + 3 + 1 + 1 + 2
+    return gate + 3 + 2 + 1
+
+
+def counted_launches(B, call, expected: int) -> dict:
+    """Kernels of one step, counted: call() is recorded as a CUDA graph and
+    its kernel nodes are counted.  Falls back to the expected count (and
+    says why) if the capture fails."""
+    try:
+        g = B.capture(call)
+        n = B.kernel_nodes(g)
+        del g
+        return {"per_step": n, "expected": expected, "source": "kernel nodes of one step "
+                "recorded as a CUDA graph"}
+    except Exception as exc:  # noqa: BLE001 - reported in the line
+        return {"per_step": expected, "expected": expected,
+                "source": f"expected count (graph capture failed: {exc})"}
 
 
 def backward_launches(w: wl.Workload) -> int:
-    """Kernels one moe_backward call launches (bf16 tensor-core path): dispatch
-    (4), recompute of the expert stage (4), weight transposes (2), dE rows,
-    two row GEMMs and the ReLU mask, k-block table, four padded transposes,
-    two weight-gradient GEMMs, Wg^T (and Wn^T), importance gradient, token
-    kernel, chunk table and the chunked row sums (gate, db2, db1: 6)."""
-    return 4 + 4 + 2 + 1 + 3 + 1 + 4 + 2 + (2 if w.noisy else 1) + 1 + 1 + 1 + 6
+    """Kernels one moe_backward call launches (bf16 tensor-core path, output
+    widths d and h multiples of 256): dispatch (3), recompute of the expert
+    stage (tile table, x-row gather, two GEMMs: 4), weight transposes (2), dE
+    rows, two row GEMMs and the ReLU mask, k-block table, four padded
+    transposes, two weight-gradient GEMMs, Wg^T (and Wn^T), importance
+    gradient, token kernel, chunk table and the chunked row sums (gate, db2,
+    db1: 6)."""
+    return 3 + 4 + 2 + 1 + 3 + 1 + 4 + 2 + (2 if w.noisy else 1) + 1 + 1 + 1 + 6
 
 
 def backward_arm(args, w: wl.Workload):
@@ -479,10 +499,10 @@ def backward_arm(args, w: wl.Workload):
     g = dict(dx=f32(w.T, w.d), dWg=f32(w.d, w.n), dWn=f32(w.d, w.n), dbg=f32(w.n),
              dW1=f32(w.n, w.h, w.d), db1=f32(w.n, w.h), dW2=f32(w.n, w.d, w.h), db2=f32(w.n, w.d))
 
-    def step():
+    def step(st=stream):
         B.moe_backward(s, d["x"], d["Wg"], d["Wn"], d["eps"], d["W1"], d["b1"], d["W2"], d["b2"],
                        fwd["idx"], fwd["G"], fwd["importance"], dy, w_imp, g["dx"], g["dWg"],
-                       g["dWn"], g["dbg"], g["dW1"], g["db1"], g["dW2"], g["db2"], bws, stream)
+                       g["dWn"], g["dbg"], g["dW1"], g["db1"], g["dW2"], g["db2"], bws, st)
 
     for _ in range(args.warmup):
         step()
@@ -501,6 +521,7 @@ def backward_arm(args, w: wl.Workload):
     if status != B.MOE_OK:
         raise RuntimeError(f"device error in the timed region: {B.status_string(status)}")
     ms = e0.elapsed_time(e1) / args.steps
+    launches = counted_launches(B, lambda: step(None), backward_launches(w))
     counts = fwd["counts"].cpu().numpy()
     hit = int((counts > 0).sum())
     eb = 2 if w.dtype == "bf16" else 4
@@ -549,7 +570,8 @@ def backward_arm(args, w: wl.Workload):
                                                w.h % 128 == 0) else "CUDA cores"),
         "tflops": flops / (ms / 1e3) / 1e12,
         "roofline": roof, "cpu_baseline": cpu, "e2e": None,
-        "gpu_launches": backward_launches(w) * args.steps, "clocks": clk,
+        "gpu_launches": launches["per_step"] * args.steps, "gpu_launches_per_step": launches,
+        "clocks": clk,
     }
     print(json.dumps(line), flush=True)
 
@@ -819,6 +841,12 @@ def main():
     ms, value = job_throughput(ms, w.T * args.steps, dist, dev)
     ms_step = ms / args.steps
 
+    # ---- launches: one step recorded as a CUDA graph, its kernel nodes ------
+    launches = counted_launches(B, lambda: B.moe_forward(
+        s, sets[0][0], dinp["Wg"], dinp["Wn"], dinp["bg"], sets[0][1], dinp["W1"], dinp["b1"],
+        dinp["W2"], dinp["b2"], out["y"], out["G"], out["idx"], out["importance"], out["cv2"],
+        out["counts"], ws, None), launches_per_step(w))
+
     # ---- stage timing: the expert FFN stage, same inputs, component calls ---
     ffn_ms = ffn_stage_ms(B, w, s, dinp, sets, out, ws, stream, dev, max(1, args.steps // 2))
     alg, roof, layer_roof = rooflines(w, out["counts"].cpu().numpy(), ms_step, ffn_ms, long_run)
@@ -923,7 +951,8 @@ def main():
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches_per_step(w) * args.steps,
+            "gpu_launches": launches["per_step"] * args.steps,
+            "gpu_launches_per_step": launches,
             "clocks": clk,
             "per_workload": per_workload,
         }

@@ -270,3 +270,34 @@ def moe_forward_balanced(shape, x, Wg, Wn, bg, eps, thr, rows_cap, W1, b1, W2, b
 def moe_selftest_timeout(ws, stream=None):
     """Diagnostic: a bounded wait that runs out (MOE_ERR_TIMEOUT in ws after ~2 s)."""
     _ok("moe_selftest_timeout", lib.moe_selftest_timeout(_p(ws), ws.numel(), _stream(stream)))
+
+
+# --------------------------------------------------------------------------
+# CUDA graphs: one layer call recorded once and replayed without per-kernel
+# launch cost.  The replay reads and writes the same tensors as the recorded
+# call; refill the inputs in place between replays.
+# --------------------------------------------------------------------------
+def capture(fn) -> torch.cuda.CUDAGraph:
+    """Records fn() as a CUDA graph.  fn calls this module's functions with
+    stream=None (the capture stream is then the current stream) on tensors
+    that exist before the capture; the graph is kept so that its nodes can
+    be inspected (kernel_nodes)."""
+    g = torch.cuda.CUDAGraph(keep_graph=True)
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        fn()
+    return g
+
+
+def kernel_nodes(g: torch.cuda.CUDAGraph) -> int:
+    """The number of kernel launches recorded in a captured graph (memset
+    and memcpy nodes are not counted)."""
+    from cuda.bindings import runtime as rt
+    handle = rt.cudaGraph_t(init_value=g.raw_cuda_graph())
+    err, _, num = rt.cudaGraphGetNodes(handle, 0)
+    if err != rt.cudaError_t.cudaSuccess:
+        raise RuntimeError(f"cudaGraphGetNodes: {err}")
+    err, nodes, num = rt.cudaGraphGetNodes(handle, num)
+    if err != rt.cudaError_t.cudaSuccess:
+        raise RuntimeError(f"cudaGraphGetNodes: {err}")
+    kernel = rt.cudaGraphNodeType.cudaGraphNodeTypeKernel
+    return sum(1 for nd in nodes[:num] if rt.cudaGraphNodeGetType(nd)[1] == kernel)

@@ -921,11 +921,9 @@ cudaError_t launch_backward_tc(const moe_shape &s, const void *x, const float *W
     if (e == cudaSuccess)
         e = launch_rows_scaled(static_cast<const __nv_bfloat16 *>(dy), G, perm, S, d, k, dE, err, st);
     // dA = dE W2 (B = W2^T rows, K = d), then dZ = dA * [a > 0];  dXs = dZ W1 (B = W1^T rows, K = h)
-    // Each GEMM runs on an SM pair when its output width allows (the tile
-    // tables of both kernels are built here from the routing).
-    if (e == cudaSuccess) e = launch_row_tiles(offsets, n, kTcRows, tiles, st);
-    if (e == cudaSuccess && (pair_gemm_supported(h) || pair_gemm_supported(d)))
-        e = launch_pair_tiles(offsets, n, ptiles, plist, st);
+    // Each GEMM runs on an SM pair when its output width allows.  Output
+    // widths h and d are the recompute's, so the tile tables it built from
+    // the same offsets serve here unchanged.
     auto row_gemm = [&](const __nv_bfloat16 *X, int K, const __nv_bfloat16 *Wt, int Nout,
                         __nv_bfloat16 *out) {
         return pair_gemm_supported(Nout)
