@@ -289,3 +289,24 @@ def forward_balanced(x, Wg, Wn, bg, eps, thr, W1, b1, W2, b2, k: int):
     if rc:
         raise ValueError("oracle_forward_balanced: bad arguments")
     return out
+
+
+def ep_regroup(recv_counts):
+    """Merged order of the rows one rank receives in the expert-parallel layer
+    ("Outrageously Large Neural Networks - 中文验证版", section 方法适配: the
+    devices' batches are merged at each expert).  recv_counts [P, nl]: rows of
+    local expert e sent by rank q; the received rows come ordered by q, then
+    e, then the sender's order.  The merged order puts every expert's rows
+    together, rank 0's first: a stable sort of the received rows by expert.
+    Returns offsets [nl+1], perm [R] (merged row -> received row), inv [R]."""
+    c = np.asarray(recv_counts, dtype=np.int64)
+    P, nl = c.shape
+    if (c < 0).any():
+        raise ValueError("negative count")
+    expert_of_row = np.repeat(np.tile(np.arange(nl), P), c.reshape(-1))
+    perm = np.argsort(expert_of_row, kind="stable").astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(c.sum(axis=0))]).astype(np.int32)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size, dtype=np.int32)
+    return offsets, perm, inv
+

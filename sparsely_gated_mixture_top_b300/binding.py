@@ -31,7 +31,8 @@ EXPORTS = ("moe_version", "moe_status_string", "moe_validate", "moe_workspace_by
            "moe_workspace_init", "moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine",
            "moe_forward", "moe_check", "moe_dispatch_noalloc", "moe_load_workspace_bytes",
            "moe_gate_load", "moe_backward_workspace_bytes", "moe_backward",
-           "moe_balanced_workspace_bytes", "moe_forward_balanced", "moe_selftest_timeout")
+           "moe_balanced_workspace_bytes", "moe_forward_balanced", "moe_selftest_timeout",
+           "moe_ep_regroup", "moe_gather_rows", "moe_importance_cv2")
 
 
 class MoEShape(ctypes.Structure):
@@ -73,9 +74,14 @@ def _load():
     lib.moe_balanced_workspace_bytes.restype = sz
     lib.moe_forward_balanced.argtypes = [shp] + [vp] * 6 + [ctypes.c_int64] + [vp] * 8 + [sz, vp]
     lib.moe_selftest_timeout.argtypes = [vp, sz, vp]
+    i64 = ctypes.c_int64
+    lib.moe_ep_regroup.argtypes = [i32, i32, vp, i64, vp, vp, vp, vp, vp]
+    lib.moe_gather_rows.argtypes = [vp, i64, vp, i32, i64, i32, i32, vp, vp, vp]
+    lib.moe_importance_cv2.argtypes = [vp, i32, vp, vp]
     for f in ("moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
               "moe_check", "moe_dispatch_noalloc", "moe_gate_load", "moe_backward",
-              "moe_forward_balanced", "moe_selftest_timeout"):
+              "moe_forward_balanced", "moe_selftest_timeout", "moe_ep_regroup",
+              "moe_gather_rows", "moe_importance_cv2"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -270,6 +276,31 @@ def moe_forward_balanced(shape, x, Wg, Wn, bg, eps, thr, rows_cap, W1, b1, W2, b
 def moe_selftest_timeout(ws, stream=None):
     """Diagnostic: a bounded wait that runs out (MOE_ERR_TIMEOUT in ws after ~2 s)."""
     _ok("moe_selftest_timeout", lib.moe_selftest_timeout(_p(ws), ws.numel(), _stream(stream)))
+
+
+# --------------------------------------------------------------------------
+# Expert-parallel device calls (include/moe_ep.h).  `err` is a workspace (its
+# error word is used) or None.
+# --------------------------------------------------------------------------
+def moe_ep_regroup(P, n_local, recv_counts, R, offsets_local, perm_local, inv_local, err=None,
+                   stream=None):
+    _ok("moe_ep_regroup", lib.moe_ep_regroup(int(P), int(n_local), _p(recv_counts), int(R),
+                                             _p(offsets_local), _p(perm_local), _p(inv_local),
+                                             _p(err), _stream(stream)))
+
+
+def moe_gather_rows(src, rows, div, dst, err=None, stream=None):
+    """dst[i] = src[rows[i] // div] (rows of src.shape[1] elements)."""
+    dt = {torch.bfloat16: MOE_BF16, torch.float32: MOE_F32}[src.dtype]
+    assert dst.dtype == src.dtype and dst.shape[1:] == src.shape[1:] and src.dim() == 2
+    _ok("moe_gather_rows", lib.moe_gather_rows(_p(src), src.shape[0], _p(rows), int(div),
+                                               dst.shape[0], src.shape[1], dt, _p(dst), _p(err),
+                                               _stream(stream)))
+
+
+def moe_importance_cv2(importance, cv2, stream=None):
+    _ok("moe_importance_cv2", lib.moe_importance_cv2(_p(importance), importance.numel(),
+                                                     _p(cv2), _stream(stream)))
 
 
 # --------------------------------------------------------------------------

@@ -45,6 +45,8 @@ enum Site : int32_t {
     kSiteTcMma = 11,
     kSiteTcEpilogue = 12,
     kSiteTcDrain = 13,
+    kSiteEpCounts = 20,
+    kSiteEpGather = 21,
 };
 
 // ---------------------------------------------------------------------------
@@ -445,6 +447,52 @@ __device__ __forceinline__ float to_f<float>(float v) {
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
     return __bfloat162float(v);
+}
+
+// Exclusive scan of one int per thread over a block of 1024 threads (in
+// thread order); returns this thread's prefix, *total the block's sum.
+__device__ __forceinline__ int32_t block_exclusive_scan_1024(int32_t v, int32_t *sh, int32_t *total) {
+    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    int32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+    }
+    if (lane == 31) sh[warp] = inc;
+    __syncthreads();
+    int32_t base = 0, all = 0;
+    for (int w = 0; w < 32; ++w) {
+        if (w < warp) base += sh[w];
+        all += sh[w];
+    }
+    __syncthreads();
+    *total = all;
+    return base + inc - v;
+}
+
+// Sum of one float per thread over a block of 1024 threads in a fixed order:
+// a shuffle tree in each warp, then a shuffle tree over the 32 warp sums in
+// warp 0; every thread gets the result.  (fp32: on this GPU a dependent fp64
+// add costs ~15x an fp32 add; a tree keeps the error near log2(1024) ulps.)
+__device__ __forceinline__ float block_sum_1024(float v, float *sh) {
+    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) sh[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float r = sh[lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+        if (lane == 0) sh[32] = r;
+    }
+    __syncthreads();
+    const float r = sh[32];
+    __syncthreads();
+    return r;
 }
 
 }  // namespace moe
