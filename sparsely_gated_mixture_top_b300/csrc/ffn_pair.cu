@@ -23,20 +23,22 @@
 //
 // Token tiles: an expert with R rows gets ceil(R / 256) tiles of Tn rows,
 // Tn = ceil(R / tiles) rounded up to 16 (at most 256); the tile count is then
-// ceil(R / Tn), so no tile is empty.  A unit of work is (token tile, block of
+// ceil(R / Tn), so no tile is empty.  A tile's MMA N is its row count rounded
+// up to 32 (so each SM's half is a multiple of 16 rows).  A unit of work is (token tile, block of
 // 256 output features); units are numbered tile-major, so the feature blocks
 // of one tile run side by side on different pairs and share its rows in L2.
 //
 // Structure (clusters of two CTAs, one CTA per SM, persistent):
 //   warp 0     TMA producer in each CTA: per stage one copy of this CTA's 128
-//              weight rows and one of up to 128 token rows, each of two 64-wide
-//              k-blocks (128-byte swizzle, 32 KB); both CTAs' copies complete on
-//              the even CTA's barrier.  A copy costs a fixed ~0.3 us of issue
+//              weight rows and one of its N/2 token rows (a box of exactly that
+//              many rows, so no neighbouring rows are read), each of two 64-wide
+//              k-blocks (128-byte swizzle, up to 64 KB); both CTAs' copies
+//              complete on the even CTA's barrier.  A copy costs a fixed ~0.3 us of issue
 //              time per SM up to 64 KB, so copies are made as large as the
 //              three-stage ring allows
 //   warp 1     tensor memory (512 columns, allocated by both CTAs together);
 //              in the even CTA one lane issues the pair MMAs (M = 256,
-//              N = tile rows rounded to 16, K = 16) and commits each stage and
+//              N = tile rows rounded to 32, K = 16) and commits each stage and
 //              each finished accumulator to the barriers of both CTAs
 //   warps 2-17 epilogue in each CTA: tcgen05.ld of its 128 accumulator rows
 //              (output features) x 32 token columns, bias, activation, bf16,
@@ -74,6 +76,12 @@ static_assert(PairCfg::kSmem <= 227 * 1024, "shared memory budget");
 
 struct PairUnit {
     int e, row0, rows, N, mt;
+};
+
+// Token-row maps of one activation matrix, box i holding 16*(i+1) rows and
+// two k-blocks: a unit of N tokens copies exactly its N/2 rows per CTA.
+struct XMaps {
+    CUtensorMap m[8];
 };
 
 // Unit q -> expert, token tile and block of output features, from the
@@ -118,7 +126,7 @@ __global__ void __launch_bounds__(1024) ffn_pair_tiles(const int32_t *__restrict
         token_tiling(R, tn, nt);
         for (int j = 0; j < nt; ++j) {
             const int rows = min(tn, R - j * tn);
-            tlist[run + j] = make_int4(i, offsets[i] + j * tn, rows, (rows + 15) & ~15);
+            tlist[run + j] = make_int4(i, offsets[i] + j * tn, rows, (rows + 31) & ~31);
         }
         run += nt;
     }
@@ -138,7 +146,7 @@ __device__ __forceinline__ bool pair_drain(uint32_t bar, uint32_t parity, int32_
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
-    ffn_pair_gemm(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
+    ffn_pair_gemm(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ XMaps mapX,
                   const int32_t *__restrict__ tiles, const int4 *__restrict__ tlist, int n,
                   int K, int Nout, const __nv_bfloat16 *__restrict__ Wg,
                   const __nv_bfloat16 *__restrict__ Xg, const float *__restrict__ bias, int relu,
@@ -178,7 +186,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&mapW);
-        tma_prefetch_map(&mapX);
+        for (int i = 0; i < 8; ++i) tma_prefetch_map(&mapX.m[i]);
     }
     // A pair allocation is issued by one warp of each CTA once both CTAs are
     // known to be running; the second cluster barrier publishes the barriers
@@ -219,9 +227,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                         break;
                     }
                     const uint32_t fb = mapa_shared(full(stage), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full(stage), 2 * Cfg::kStageBytes);
+                    // this CTA's N/2 token rows (a multiple of 16) in one box
+                    const int hrows = u.N >> 1;
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(full(stage), 2 * (Cfg::kABytes + hrows * 128 * kPairKB));
                     tma_load_3d_pair(smem_u32(sA + stage * Cfg::kABytes), &mapW, fb, 0, wrow, kb);
-                    tma_load_3d_pair(smem_u32(sB + stage * Cfg::kBBytes), &mapX, fb, 0, xrow, kb);
+                    tma_load_3d_pair(smem_u32(sB + stage * Cfg::kBBytes), &mapX.m[(hrows >> 4) - 1], fb,
+                                     0, xrow, kb);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -260,6 +272,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(sA + stage * Cfg::kABytes);
                     const uint32_t b0 = smem_u32(sB + stage * Cfg::kBBytes);
+                    const uint32_t bkb = static_cast<uint32_t>(u.N >> 1) * 128;  // B k-block stride
                     // a k-block past K (the box's zero-filled tail) is skipped
                     const int nkb = min(kPairKB, kblocks - kb);
                     for (int j = 0; j < nkb; ++j) {
@@ -267,7 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                         for (int kk = 0; kk < 4; ++kk)
                             tc_mma_f16_pair(d_tmem,
                                             sdesc_kmajor_sw128(a0 + j * Cfg::kKBlockBytes + kk * 32),
-                                            sdesc_kmajor_sw128(b0 + j * Cfg::kKBlockBytes + kk * 32),
+                                            sdesc_kmajor_sw128(b0 + j * bkb + kk * 32),
                                             idesc, (kb | j | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit_pair_both(empty(stage));
@@ -426,11 +439,15 @@ cudaError_t launch_grouped_gemm_pair(const moe_shape &s, const __nv_bfloat16 *X,
                                      const int32_t *tiles, const int4 *tlist,
                                      __nv_bfloat16 *out, int32_t *err, cudaStream_t st) {
     const int64_t S = slots(s);
-    CUtensorMap mW, mX;
+    CUtensorMap mW;
+    XMaps mX;
     if (!make_kmajor_map(&mW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(s.n) * Nout, 128,
-                         kPairKB) ||
-        !make_kmajor_map(&mX, X, static_cast<uint64_t>(K), static_cast<uint64_t>(S), 128, kPairKB))
+                         kPairKB))
         return cudaErrorInvalidValue;
+    for (int i = 0; i < 8; ++i)
+        if (!make_kmajor_map(&mX.m[i], X, static_cast<uint64_t>(K), static_cast<uint64_t>(S),
+                             static_cast<uint32_t>(16 * (i + 1)), kPairKB))
+            return cudaErrorInvalidValue;
     // The opt-in above 48 KB belongs to the current device's context: set it
     // before every launch (a cheap host call).
     cudaError_t e = cudaFuncSetAttribute(ffn_pair_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -212,7 +212,7 @@ int sm_count();
 // (tiles[e] = token tiles of the experts before e, tiles[n] = total) and the
 // GEMM  out[r, c] = act(X[r] . W[e*Nout + c] + bias[e*Nout + c]).
 // tlist: one int4 per token tile {expert, first row, rows, rows rounded up to
-// 16}, at most pair_tile_capacity(S, n) entries.
+// 32}, at most pair_tile_capacity(S, n) entries.
 bool pair_gemm_supported(int Nout);
 cudaError_t launch_pair_tiles(const int32_t *offsets, int n, int32_t *tiles, int4 *tlist,
                               cudaStream_t st);

@@ -214,7 +214,7 @@ __device__ void dispatch_finish(int n, const ScanOut &o) {
             token_tiling(c, tn, nt);
             for (int j = 0; j < nt; ++j) {
                 const int rows = min(tn, c - j * tn);
-                o.plist[prun + j] = make_int4(i, run + j * tn, rows, (rows + 15) & ~15);
+                o.plist[prun + j] = make_int4(i, run + j * tn, rows, (rows + 31) & ~31);
             }
             prun += nt;
         }
