@@ -79,7 +79,10 @@ __global__ void __launch_bounds__(128) gate_pack(const float *__restrict__ Wg,
                                                  int mchunks, int noisy, int pair,
                                                  uint8_t *__restrict__ pack) {
     __shared__ float tile[16][65];
-    pdl_wait();
+    // The weights are inputs of the call, not results of the previous kernel
+    // (which only ever reads this buffer two launches back, in the previous
+    // gate): pack first, and let the gate start its prologue meanwhile.  The
+    // wait at the end keeps the stream order for everything after this.
     pdl_launch_dependents();
     const int chunk = blockIdx.x;
     const int which = blockIdx.y;  // 0 clean, 1 noise
@@ -135,6 +138,7 @@ __global__ void __launch_bounds__(128) gate_pack(const float *__restrict__ Wg,
         *reinterpret_cast<uint4 *>(pack + hunit + kKBytes / 2 + off) =
             make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
+    pdl_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -181,6 +185,51 @@ struct TopK {
     }
 };
 
+// Compare-exchange of two (score, column) entries: a takes the better one
+// (larger score, equal scores by lower column).
+__device__ __forceinline__ void cas_entry(float &va, int &ia, float &vb, int &ib) {
+    const bool sw = (vb > va) | ((vb == va) & (ib < ia));
+    const float tv = sw ? vb : va;
+    const int ti = sw ? ib : ia;
+    vb = sw ? va : vb;
+    ib = sw ? ia : ib;
+    va = tv;
+    ia = ti;
+}
+
+// The best four of sixteen entries, in order, by a fixed network: four
+// sorted groups of four (5 exchanges each), then three merges of two sorted
+// fours into the best four (the better of a[i] and b[3-i] forms a bitonic
+// sequence, sorted by 4 exchanges).  Branch-free: the same for every lane.
+__device__ __forceinline__ void top4_of16(float (&v)[16], int (&ix)[16], float (&ov)[4],
+                                          int (&oi)[4]) {
+#pragma unroll
+    for (int g = 0; g < 16; g += 4) {
+        cas_entry(v[g], ix[g], v[g + 1], ix[g + 1]);
+        cas_entry(v[g + 2], ix[g + 2], v[g + 3], ix[g + 3]);
+        cas_entry(v[g], ix[g], v[g + 2], ix[g + 2]);
+        cas_entry(v[g + 1], ix[g + 1], v[g + 3], ix[g + 3]);
+        cas_entry(v[g + 1], ix[g + 1], v[g + 2], ix[g + 2]);
+    }
+    // merge group b into group a (a, b: first entries of two sorted fours)
+    auto merge4 = [&](int a, int b) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cas_entry(v[a + q], ix[a + q], v[b + 3 - q], ix[b + 3 - q]);
+        cas_entry(v[a], ix[a], v[a + 2], ix[a + 2]);
+        cas_entry(v[a + 1], ix[a + 1], v[a + 3], ix[a + 3]);
+        cas_entry(v[a], ix[a], v[a + 1], ix[a + 1]);
+        cas_entry(v[a + 2], ix[a + 2], v[a + 3], ix[a + 3]);
+    };
+    merge4(0, 4);
+    merge4(8, 12);
+    merge4(0, 8);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        ov[q] = v[q];
+        oi[q] = ix[q];
+    }
+}
+
 // Softmax over the first kk entries (descending): w[q] = e^(v[q]-v[0]) / sum.
 template <int KM>
 __device__ __forceinline__ void softmax_top(const TopK<KM> &t, int kk, float (&w)[KM]) {
@@ -216,9 +265,14 @@ struct GateCfg {
     static constexpr int kXBytes = kResident ? 8 * kKBytes : 0;  // d <= 512
     // Exchange of two parts' final lists at a time, [list][slot][row] order.
     static constexpr int kXchBytes = 2 * KM * kGateRows * 8;
+    // Each part's k-th score per row after a chunk, two chunks deep (lists
+    // of up to 8; the 16-deep lists' exchange leaves no room for it).
+    static constexpr bool kShareThr = KM <= 8;
+    static constexpr int kThrBytes = kShareThr ? 2 * kGateParts * kGateRows * 4 : 0;
     static constexpr int kAcc = 4;  // accumulators (128 columns each)
     static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kAcc + 3) + 16;
-    static constexpr int kSmem = kXBytes + kStages * kStageBytes + kXchBytes + 1024 + kBarBytes;
+    static constexpr int kSmem =
+        kXBytes + kStages * kStageBytes + kXchBytes + kThrBytes + 1024 + kBarBytes;
     static constexpr uint32_t kTmemCols = 128 * kAcc;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
@@ -254,6 +308,11 @@ struct GateArgs {
 // Named barrier of the eight epilogue warps.
 __device__ __forceinline__ void epi_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kGateEpiWarps) : "memory");
+}
+
+// The four warps that read one lane quarter (rows 32*quad ..), one per part.
+__device__ __forceinline__ void quad_bar(int quad) {
+    asm volatile("bar.sync %0, %1;" ::"r"(2 + quad), "n"(32 * kGateParts) : "memory");
 }
 
 // eps[row][col0 + j] for the NC columns j of one chunk part (0 past C).
@@ -329,7 +388,8 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     uint8_t *sXch = sS + Cfg::kStages * Cfg::kStageBytes;
     float *xch_v = reinterpret_cast<float *>(sXch);                        // [2][KM][rows]
     int *xch_i = reinterpret_cast<int *>(sXch + 2 * KM * kGateRows * 4);   // [2][KM][rows]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sXch + Cfg::kXchBytes);
+    float *thr_sh = reinterpret_cast<float *>(sXch + Cfg::kXchBytes);   // [2][parts][rows]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sXch + Cfg::kXchBytes + Cfg::kThrBytes);
     constexpr int S = Cfg::kStages;
     constexpr int NA = Cfg::kAcc;
     // full[S], empty[S], tfull[NA], tempty[NA], xfull, xempty, drain
@@ -386,14 +446,31 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         tc_fence_after();
     }
     const uint32_t tmem_base = *tmem_slot;
-    // everything above is local; from here on the previous kernel's results are used
+    const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    // Flat gating reads x, an input of the call: the first tile's resident x
+    // rows are requested before waiting for the previous kernel (the packed
+    // weights).  The grouped pass reads rows the previous kernels gathered.
+    const bool x_early = kResident && !kGrouped &&
+                         tile0 < static_cast<int>((a.T + (kPair ? 2 : 1) * kGateRows - 1) /
+                                                  ((kPair ? 2 : 1) * kGateRows));
+    if (x_early && warp == 0 && lane == 0) {
+        const GateTile ti = gate_tile<kGrouped, kPair>(tile0, a, rank);
+        const int kbl = a.d / kGateBK;
+        if constexpr (kPair) {
+            if (rank == 0) mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(2 * kbl * kKBytes));
+            tma_load_3d_pair(smem_u32(sX), &mapX, mapa_shared(xfull, 0), 0, ti.row0, 0);
+        } else {
+            mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(kbl * kKBytes));
+            tma_load_3d(smem_u32(sX), &mapX, xfull, 0, ti.row0, 0);
+        }
+    }
+    // from here on the previous kernel's results are used
     pdl_wait();
     pdl_launch_dependents();
     // tiles of 128 rows (single CTA) or 256 rows (pair: 128 per CTA)
     const int tiles = kGrouped ? a.tiles_g[a.groups]
                                : static_cast<int>((a.T + (kPair ? 2 : 1) * kGateRows - 1) /
                                                   ((kPair ? 2 : 1) * kGateRows));
-    const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
     const int tstep = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     const int kblocks = a.d / kGateBK;
 
@@ -406,7 +483,9 @@ __global__ void __launch_bounds__(kGateThreads, 1)
             int64_t issued = 0;
             for (int tile = tile0; tile < tiles && ok; tile += tstep) {
                 const GateTile ti = gate_tile<kGrouped, kPair>(tile, a, rank);
-                if (kResident) {
+                if (kResident && x_early && tile == tile0) {
+                    xphase ^= 1u;  // requested before the wait above
+                } else if (kResident) {
                     if (!mbar_wait_bounded(xempty, xphase ^ 1u, abort_flag, a.err, kSiteTcProducer)) {
                         ok = false;
                         break;
@@ -677,9 +756,21 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                                              kSiteTcEpilogue))
                     ok = false;
                 ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the shuffles below need every lane
+                // The row's k-th best so far is at least the largest of the
+                // four parts' k-th scores after the previous chunk (each part's
+                // list holds k of the row's columns): a tighter filter than
+                // this part's own list, exact because every column of this
+                // chunk has a higher index than every column before it.
+                float thr_rows = -INFINITY;
+                if (Cfg::kShareThr && c > 0) {
+                    quad_bar(quad);
+                    const float *tb = thr_sh + ((c - 1) & 1) * kGateParts * kGateRows + r;
+                    thr_rows = fmaxf(fmaxf(tb[0], tb[kGateRows]),
+                                     fmaxf(tb[2 * kGateRows], tb[3 * kGateRows]));
+                }
                 if (ok) {
                     tc_fence_after();
-                    const float thr = list.kth(a.kf);  // fixed for the span
+                    const float thr = fmaxf(list.kth(a.kf), thr_rows);  // fixed for the span
                     uint32_t cv[16], nv[16];
                     const uint32_t col = static_cast<uint32_t>(acc * 128 + part * kPartCols);
                     tmem_ld_32x32b_x16(tmem_base + lane_addr + col, cv);
@@ -738,6 +829,23 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                         cv[j] = __float_as_uint(h);
                         if (valid && sc < a.ncols && h > thr) pass |= 1u << j;
                     }
+                    if constexpr (KM == 4) {
+                        // First chunk of the tile, empty list: the list is the
+                        // best four of these sixteen columns (columns past the
+                        // row or the tile rank last), by a fixed network.
+                        if (c == 0) {
+                            float v16[16];
+                            int i16[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const bool use = valid && col0 + j < a.ncols;
+                                v16[j] = use ? __uint_as_float(cv[j]) : -INFINITY;
+                                i16[j] = use ? col0 + j : INT_MAX;
+                            }
+                            top4_of16(v16, i16, list.v, list.i);
+                            pass = 0u;
+                        }
+                    }
                     // Pass 2 (rare after the first chunk): each lane inserts its
                     // own flagged columns in increasing index order; the score
                     // leaves the register list through a compile-time select
@@ -752,6 +860,8 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                         list.insert(hv, col0 + j);
                     }
                 }
+                if (Cfg::kShareThr && c + 1 < a.chunks)
+                    thr_sh[(c & 1) * kGateParts * kGateRows + part * kGateRows + r] = list.kth(a.kf);
                 if (++acc == NA) {
                     acc = 0;
                     acc_phase ^= 1u;
