@@ -310,3 +310,86 @@ def ep_regroup(recv_counts):
     inv[perm] = np.arange(perm.size, dtype=np.int32)
     return offsets, perm, inv
 
+
+
+def backward_hier(x, Wg, Wn, bg, eps, W1, b1, W2, b2, dy, k: int, groups: int, k_groups: int,
+                  w_imp: float = 0.0):
+    """Gradients of L = sum_t <dy_t, y_t> + w_imp * CV^2(importance) for the
+    hierarchical layer ("MoE:稀疏门控混合专家", section 三: the two-level choice,
+    k_groups groups by their noisy score, then k/k_groups experts in each kept
+    group by that group's columns; weight = group weight x inner weight), the
+    selection held fixed (the oracle's own gate_hier).  Score columns: groups
+    0..G-1, then expert e at G + e.  The chain, per token, with c the clean
+    score x.Wg + bg and r = x.Wn of a column:
+        dG_s   = <dy, E_s> + w_imp dCV^2/dimp_e                   (slot s = (q, j))
+        Gp_q   = sum_j G_qj,  Gi_qj = G_qj / Gp_q
+        dGp_q  = sum_j dG_qj Gi_qj,  dGi_qj = dG_qj Gp_q
+        dHi_qj = Gi_qj (dGi_qj - sum_l Gi_ql dGi_ql)               (inner softmax)
+        dHp_q  = Gp_q (dGp_q - sum_l Gp_l dGp_l)                   (group softmax)
+        each column's dH gives dc = dH and dr = dH eps sigmoid(r); dx gets
+        dc Wg[:, col] + dr Wn[:, col]; dWg[:, col] += dc x, dWn[:, col] += dr x,
+        dbg[col] += dc
+    and the experts as in `backward`.  Plain numpy in float64; returns the same
+    dict as `backward` (dWg, dWn, dbg over all G + n columns)."""
+    x, Wg, Wn, bg, eps, W1, b1, W2, b2, dy = map(_f64, (x, Wg, Wn, bg, eps, W1, b1, W2, b2, dy))
+    T, d = x.shape
+    n, h, _ = W1.shape
+    Gn, kg = groups, k_groups
+    m, ki = n // Gn, k // kg
+    C = Gn + n
+    idx, G, _ = gate_hier(x, Wg, Wn, bg, eps, groups, k_groups, k)
+    idx = idx.astype(np.int64)
+    raw = x @ Wn if (Wn is not None and eps is not None) else None
+    # experts: forward pieces per slot, then the chain back
+    E = np.zeros((T, k, d))
+    dx = np.zeros((T, d))
+    dW1, db1 = np.zeros((n, h, d)), np.zeros((n, h))
+    dW2, db2 = np.zeros((n, d, h)), np.zeros((n, d))
+    for e in range(n):
+        tt, jj = np.nonzero(idx == e)
+        if tt.size == 0:
+            continue
+        xs = x[tt]
+        z = xs @ W1[e].T + (b1[e] if b1 is not None else 0.0)
+        a = np.maximum(z, 0.0)
+        E[tt, jj] = a @ W2[e].T + (b2[e] if b2 is not None else 0.0)
+        dE = G[tt, jj][:, None] * dy[tt]
+        dW2[e] = dE.T @ a
+        db2[e] = dE.sum(axis=0)
+        dz = (dE @ W2[e]) * (z > 0)
+        dW1[e] = dz.T @ xs
+        db1[e] = dz.sum(axis=0)
+        np.add.at(dx, tt, dz @ W1[e])
+    # the importance term, per expert
+    imp = np.bincount(idx.ravel(), weights=G.ravel(), minlength=n)
+    mu = imp.mean()
+    gimp = np.zeros(n)
+    if mu != 0.0 and w_imp != 0.0:
+        var = ((imp - mu) ** 2).mean()
+        gimp = w_imp * (2.0 * (imp - mu) / (n * mu * mu) - 2.0 * var / (n * mu ** 3))
+    dG = np.einsum("td,tkd->tk", dy, E) + gimp[idx]
+    # two softmax levels
+    G3 = G.reshape(T, kg, ki)
+    dG3 = dG.reshape(T, kg, ki)
+    Gp = G3.sum(axis=2)
+    Gi = G3 / Gp[:, :, None]
+    dGp = (dG3 * Gi).sum(axis=2)
+    dGi = dG3 * Gp[:, :, None]
+    dHi = Gi * (dGi - (Gi * dGi).sum(axis=2, keepdims=True))
+    dHp = Gp * (dGp - (Gp * dGp).sum(axis=1, keepdims=True))
+    # the score columns of every kept (token, column) pair
+    cols = np.concatenate([idx[:, ::ki] // m, Gn + idx], axis=1)        # [T, kg + k]
+    dH = np.concatenate([dHp, dHi.reshape(T, k)], axis=1)
+    dWg, dWn, dbg = np.zeros((d, C)), np.zeros((d, C)), np.zeros(C)
+    for q in range(cols.shape[1]):
+        c = cols[:, q]
+        dc = dH[:, q]
+        dx += dc[:, None] * Wg[:, c].T
+        np.add.at(dWg.T, c, dc[:, None] * x)
+        np.add.at(dbg, c, dc)
+        if raw is not None:
+            dr = dc * eps[np.arange(T), c] / (1.0 + np.exp(-raw[np.arange(T), c]))
+            dx += dr[:, None] * Wn[:, c].T
+            np.add.at(dWn.T, c, dr[:, None] * x)
+    return dict(dx=dx, dWg=dWg, dWn=dWn, dbg=dbg, dW1=dW1, db1=db1, dW2=dW2, db2=db2,
+                idx=idx.astype(np.int32), G=G)
