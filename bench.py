@@ -467,18 +467,17 @@ def backward_launches(w: wl.Workload) -> int:
     transposes, two weight-gradient GEMMs, Wg^T (and Wn^T), importance
     gradient, token kernel, chunk table and the chunked row sums (gate, db2,
     db1: 6)."""
-    return 3 + 4 + 2 + 1 + 3 + 1 + 4 + 2 + (2 if w.noisy else 1) + 1 + 1 + 1 + 6
+    flat = 3 + 4 + 2 + 1 + 3 + 1 + 4 + 2 + (2 if w.noisy else 1) + 1 + 1 + 1 + 6
+    # hierarchical: the pairs (token, kept group) built and routed by group
+    # (1 + 3), and their chunk table and two-pass sums for the group columns (3)
+    return flat + (7 if w.groups else 0)
 
 
 def backward_arm(args, w: wl.Workload):
-    """Times moe_backward (flat layer) on the workload: the forward runs once
-    for idx, G and importance; each timed step is one backward call with the
-    upstream gradient dy resident on the device."""
+    """Times moe_backward on the workload: the forward runs once for idx, G
+    and importance; each timed step is one backward call with the upstream
+    gradient dy resident on the device."""
     from sparsely_gated_mixture_top_b300 import binding as B
-    if w.groups:
-        print(json.dumps({"metric": "MoE-layer backward tokens/sec", "unavailable":
-                          "the backward pass covers flat gating only"}))
-        return
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
@@ -496,7 +495,8 @@ def backward_arm(args, w: wl.Workload):
     def f32(*shape):
         return torch.empty(shape, dtype=torch.float32, device=dev)
 
-    g = dict(dx=f32(w.T, w.d), dWg=f32(w.d, w.n), dWn=f32(w.d, w.n), dbg=f32(w.n),
+    C = w.n + w.groups   # gate score columns (the group columns first)
+    g = dict(dx=f32(w.T, w.d), dWg=f32(w.d, C), dWn=f32(w.d, C), dbg=f32(C),
              dW1=f32(w.n, w.h, w.d), db1=f32(w.n, w.h), dW2=f32(w.n, w.d, w.h), db2=f32(w.n, w.d))
 
     def step(st=stream):
@@ -530,7 +530,7 @@ def backward_arm(args, w: wl.Workload):
     # matrices; write their gradients (fp32) and dx; contractions: the four
     # backward GEMMs (8 S d h) and the first layer recomputed for a (2 S d h)
     bytes_ = (hit * 2 * w.d * w.h * (eb + 4) + w.T * w.d * (2 * eb + 4) +
-              (w.T * w.n * 4 if w.noisy else 0) + 4 * w.d * w.n * 4 + S * 8)
+              (w.T * C * 4 if w.noisy else 0) + 4 * w.d * C * 4 + S * 8)
     flops = 10.0 * S * w.d * w.h
     pk = peaks()
     long_run = ms * args.steps > 1000.0
@@ -552,9 +552,15 @@ def backward_arm(args, w: wl.Workload):
         import oracle
         ntok = min(w.T, 64)
         t0 = time.time()
-        oracle.backward(host["x"][:ntok], host["Wg"], host["Wn"], host["bg"],
-                        host["eps"][:ntok] if host["eps"] is not None else None, host["W1"],
-                        host["b1"], host["W2"], host["b2"], dy[:ntok].cpu(), w.k, w_imp)
+        eps_s = host["eps"][:ntok] if host["eps"] is not None else None
+        if w.groups:
+            oracle.backward_hier(host["x"][:ntok], host["Wg"], host["Wn"], host["bg"], eps_s,
+                                 host["W1"], host["b1"], host["W2"], host["b2"], dy[:ntok].cpu(),
+                                 w.k, w.groups, w.k_groups, w_imp)
+        else:
+            oracle.backward(host["x"][:ntok], host["Wg"], host["Wn"], host["bg"], eps_s,
+                            host["W1"], host["b1"], host["W2"], host["b2"], dy[:ntok].cpu(), w.k,
+                            w_imp)
         dt_cpu = time.time() - t0
         cpu = {"value": ntok / dt_cpu, "unit": "tokens/s", "cores": oracle.num_threads(),
                "kind": "oracle", "sample": f"first {ntok} tokens, one fp64 oracle backward "

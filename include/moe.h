@@ -250,18 +250,24 @@ MOE_API moe_status moe_gate_load(const moe_shape *shape, const void *x, const fl
                                  size_t ws_bytes, void *lws, size_t lws_bytes, void *stream);
 
 /*
- * Backward pass of the flat layer (groups == 0; MOE_ERR_UNSUPPORTED for the
- * hierarchical gate).  The pages train the layer with noise in the gate
- * ("MoE:稀疏门控混合专家", section 四) and an importance loss beside the task
- * loss ("Outrageously Large Neural Networks — MoE 怎样让模型“很大但不每次全算”",
- * section 方法怎么做); the gradients are the chain rule of the forward pass
- * with the forward's selection idx held fixed, for the loss
+ * Backward pass of the layer, flat or hierarchical.  The pages train the
+ * layer with noise in the gate ("MoE:稀疏门控混合专家", section 四) and an
+ * importance loss beside the task loss ("Outrageously Large Neural Networks —
+ * MoE 怎样让模型“很大但不每次全算”", section 方法怎么做); the gradients are the
+ * chain rule of the forward pass with the forward's selection idx held
+ * fixed, for the loss
  *   L = sum_t <dy[t], y[t]> + w_importance * CV^2(importance).
+ * Hierarchical gate (section 三 of the first page): the final weight of slot
+ * (q, j) is Gp_q * Gi_qj, the group weight times the in-group weight; the
+ * gradient passes through both softmaxes to the kept group columns and the
+ * kept expert columns of Wg, Wnoise and bg.
  * Inputs: the forward's inputs (x, W1, W2, dy in the shape's dtype; Wg, Wnoise
- * [d,n], eps [T,n], b1, b2 fp32; bg is not needed), its outputs idx [T,k], G
- * [T,k] and importance [n] (only read when w_importance != 0), and dy [T,d].
- * Outputs, all fp32 and overwritten: dx [T,d], dWg [d,n], dWnoise [d,n] (all
- * zero when noisy == 0; may then be NULL), dbg [n], dW1 [n,h,d], db1 [n,h],
+ * [d,C], eps [T,C], b1, b2 fp32, with C the gate's score columns: n flat,
+ * groups + n hierarchical, the group columns first; bg is not needed), its
+ * outputs idx [T,k], G [T,k] and importance [n] (only read when
+ * w_importance != 0), and dy [T,d].
+ * Outputs, all fp32 and overwritten: dx [T,d], dWg [d,C], dWnoise [d,C] (all
+ * zero when noisy == 0; may then be NULL), dbg [C], dW1 [n,h,d], db1 [n,h],
  * dW2 [n,d,h], db2 [n,d]; dbg, db1, db2 may be NULL when not wanted.
  * Every sum runs in a fixed order, so results are bit-reproducible.  bf16
  * shapes whose d and h are multiples of 128 run the contractions on the

@@ -49,7 +49,39 @@ constexpr int32_t kSiteBwdPerm = 20;
 constexpr int kBT = 64;  // rows and columns of a SIMT tile
 constexpr int kBK = 16;  // k per shared-memory step
 
+// Hierarchical gating: the (token, kept group) pairs routed by group, for
+// the gradients of the group columns.
+struct PairLayout {
+    size_t gidx = 0, gw = 0, counts = 0, offsets = 0, perm = 0, inv = 0, imp = 0, cv2 = 0;
+    size_t local_rank = 0, chunk = 0, chunk_imp = 0, imp_acc = 0, dcg = 0, drg = 0, ctiles = 0;
+};
+
+template <class Take>
+PairLayout take_pairs(const moe_shape &s, Take &&take) {
+    PairLayout P;
+    if (s.groups == 0) return P;
+    const size_t np = static_cast<size_t>(s.T) * s.k_groups, Gn = static_cast<size_t>(s.groups);
+    const size_t chunks = (np + kRouteChunk - 1) / kRouteChunk;
+    P.gidx = take(np * 4);
+    P.gw = take(np * 4);
+    P.counts = take(Gn * 4);
+    P.offsets = take((Gn + 1) * 4);
+    P.perm = take(np * 4);
+    P.inv = take(np * 4);
+    P.imp = take(Gn * 4);
+    P.cv2 = take(4);
+    P.local_rank = take(np * 4);
+    P.chunk = take(chunks * Gn * 4);
+    P.chunk_imp = take(chunks * Gn * 4);
+    P.imp_acc = take(Gn * 4);
+    P.dcg = take(np * 4);
+    P.drg = take(np * 4);
+    P.ctiles = take((Gn + 1) * 4);
+    return P;
+}
+
 struct BwdLayout {
+    PairLayout pairs;
     size_t local_rank = 0, chunk = 0, chunk_imp = 0, imp_acc = 0;
     size_t counts = 0, offsets = 0, perm = 0, inv_perm = 0, imp = 0, cv2 = 0, tiles = 0;
     size_t WgT = 0, WnT = 0, gimp = 0, dc = 0, dr = 0;
@@ -87,11 +119,13 @@ BwdLayout bwd_layout(const moe_shape &s) {
     L.imp = take(n * 4);
     L.cv2 = take(4);
     L.tiles = take((n + 1) * 4);
-    L.WgT = take(n * d * 4);
-    L.WnT = take(n * d * 4);
+    const size_t Cg = static_cast<size_t>(gate_cols(s));
+    L.WgT = take(Cg * d * 4);
+    L.WnT = take(Cg * d * 4);
     L.gimp = take(n * 4);
     L.dc = take(S * 4);
     L.dr = take(S * 4);
+    L.pairs = take_pairs(s, take);
     L.Z = take(S * h * 4);
     L.dZ = take(S * h * 4);
     L.E = take(S * d * 4);
@@ -704,6 +738,203 @@ cudaError_t launch_token(int64_t T, int d, int n, int k, const void *x, const vo
 }
 
 
+// Hierarchical gating, one warp per token.  The k slots hold kg kept
+// groups of ki experts each, group-major (slot q*ki + j); G = Gp_q Gi_qj with
+// Gp the weights of the kept groups and Gi those of the experts inside group
+// q.  Score columns: group g at g, expert e at Gn + e (C in all).  From
+// dG_s = <dy, E_s> + gimp[e_s]:
+//   dGp_q = sum_j dG_qj Gi_qj,  dGi_qj = dG_qj Gp_q
+//   dHi_qj = Gi_qj (dGi_qj - sum_l Gi_ql dGi_ql),  dHp_q = Gp_q (dGp_q - sum_l Gp_l dGp_l)
+// and every kept column gives dc = dH, dr = dH eps sigmoid(x . Wn[:, col]) and
+// its share of dx.  Slot columns go to dc/dr [S], group columns to dcg/drg
+// [T*kg].  The slot loops run over compile-time indices (the per-slot
+// arrays stay in registers); slot j belongs to group j / ki.
+template <int KM>
+__global__ void __launch_bounds__(256) bwd_token_hier(
+    int64_t T, int d, int n, int k, int Gn, int kg, const void *__restrict__ x,
+    const void *__restrict__ dy, int bf16, const void *__restrict__ E,
+    const void *__restrict__ dXs, int ebf16, const int32_t *__restrict__ inv_perm,
+    const int32_t *__restrict__ idx, const float *__restrict__ G, const float *__restrict__ gimp,
+    const float *__restrict__ WgT, const float *__restrict__ WnT, const float *__restrict__ eps,
+    float *__restrict__ dc, float *__restrict__ dr, float *__restrict__ dcg,
+    float *__restrict__ drg, float *__restrict__ dx, int32_t *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+    if (t >= T) return;
+    const int64_t S = T * k;
+    const int ki = k / kg, m = n / Gn, C = Gn + n;
+    int ex[KM], row[KM], grp[KM];
+    float aE[KM], aR[KM], aRg[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        ex[j] = 0;
+        row[j] = -1;
+        grp[j] = 0;
+        aE[j] = 0.0f;
+        aR[j] = 0.0f;
+        aRg[j] = 0.0f;
+        if (j >= k) continue;
+        const int64_t s = t * k + j;
+        const int e = idx[s];
+        const int r = inv_perm[s];
+        if (e < 0 || e >= n || r < 0 || r >= S) {
+            if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteBwdPerm, static_cast<int32_t>(s));
+            continue;
+        }
+        ex[j] = e;
+        row[j] = r;
+    }
+    // group of kept group q: that of its first slot
+#pragma unroll
+    for (int q = 0; q < KM; ++q) {
+        if (q >= kg) break;
+#pragma unroll
+        for (int j = 0; j < KM; ++j)
+            if (j < k && j == q * ki) grp[q] = ex[j] / m;
+    }
+#pragma unroll 4
+    for (int c = lane; c < d; c += 32) {
+        const float dv = ldf(dy, t * d + c, bf16);
+        const float xv = eps ? ldf(x, t * d + c, bf16) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+            if (j >= k) break;
+            if (row[j] >= 0) aE[j] = fmaf(dv, ldf(E, static_cast<int64_t>(row[j]) * d + c, ebf16), aE[j]);
+            if (eps) aR[j] = fmaf(xv, WnT[static_cast<int64_t>(Gn + ex[j]) * d + c], aR[j]);
+        }
+        if (eps) {
+#pragma unroll
+            for (int q = 0; q < KM; ++q) {
+                if (q >= kg) break;
+                aRg[q] = fmaf(xv, WnT[static_cast<int64_t>(grp[q]) * d + c], aRg[q]);
+            }
+        }
+    }
+    float dG[KM], Gs[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        dG[j] = 0.0f;
+        Gs[j] = 0.0f;
+        if (j >= k) continue;
+        dG[j] = warp_sum(aE[j]) + gimp[ex[j]];
+        Gs[j] = G[t * k + j];
+    }
+    // the two softmax levels
+    float Gp[KM], dGp[KM], sI[KM];
+#pragma unroll
+    for (int q = 0; q < KM; ++q) {
+        Gp[q] = 0.0f;
+        dGp[q] = 0.0f;
+        sI[q] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KM; ++j)
+            if (j < k && j / ki == q) Gp[q] += Gs[j];
+    }
+    float Gi[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        Gi[j] = 0.0f;
+        if (j >= k) continue;
+#pragma unroll
+        for (int q = 0; q < KM; ++q)
+            if (j / ki == q) {
+                Gi[j] = Gp[q] != 0.0f ? Gs[j] / Gp[q] : 0.0f;
+                dGp[q] = fmaf(dG[j], Gi[j], dGp[q]);
+                sI[q] = fmaf(Gi[j], dG[j] * Gp[q], sI[q]);   // sum_l Gi_ql dGi_ql
+            }
+    }
+    float sP = 0.0f;
+#pragma unroll
+    for (int q = 0; q < KM; ++q)
+        if (q < kg) sP = fmaf(Gp[q], dGp[q], sP);
+    float dH[KM], drv[KM], dHg[KM], drgv[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        dH[j] = 0.0f;
+        drv[j] = 0.0f;
+        if (j >= k) continue;
+#pragma unroll
+        for (int q = 0; q < KM; ++q)
+            if (j / ki == q) dH[j] = Gi[j] * (dG[j] * Gp[q] - sI[q]);
+        if (eps) {
+            const float r = warp_sum(aR[j]);
+            drv[j] = dH[j] * eps[t * C + Gn + ex[j]] / (1.0f + __expf(-r));
+        }
+        if (lane == 0) {
+            dc[t * k + j] = dH[j];
+            dr[t * k + j] = drv[j];
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < KM; ++q) {
+        dHg[q] = 0.0f;
+        drgv[q] = 0.0f;
+        if (q >= kg) continue;
+        dHg[q] = Gp[q] * (dGp[q] - sP);
+        if (eps) {
+            const float r = warp_sum(aRg[q]);
+            drgv[q] = dHg[q] * eps[t * C + grp[q]] / (1.0f + __expf(-r));
+        }
+        if (lane == 0) {
+            dcg[t * kg + q] = dHg[q];
+            drg[t * kg + q] = drgv[q];
+        }
+    }
+#pragma unroll 4
+    for (int c = lane; c < d; c += 32) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+            if (j >= k) break;
+            const int64_t we = static_cast<int64_t>(Gn + ex[j]) * d + c;
+            acc = fmaf(dH[j], WgT[we], acc);
+            if (eps) acc = fmaf(drv[j], WnT[we], acc);
+            if (row[j] >= 0) acc += ldf(dXs, static_cast<int64_t>(row[j]) * d + c, ebf16);
+        }
+#pragma unroll
+        for (int q = 0; q < KM; ++q) {
+            if (q >= kg) break;
+            const int64_t wg = static_cast<int64_t>(grp[q]) * d + c;
+            acc = fmaf(dHg[q], WgT[wg], acc);
+            if (eps) acc = fmaf(drgv[q], WnT[wg], acc);
+        }
+        dx[t * d + c] = acc;
+    }
+}
+
+// (token, kept group) pairs of the forward's selection: pair t*kg + q takes
+// the group of slot t*k + q*ki and the weight Gp_q (sum of the group's slots).
+__global__ void bwd_pairs(const int32_t *__restrict__ idx, const float *__restrict__ G, int64_t T,
+                          int k, int kg, int m, int32_t *__restrict__ gidx, float *__restrict__ gw) {
+    const int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (p >= T * kg) return;
+    const int ki = k / kg;
+    const int64_t s0 = (p / kg) * k + (p % kg) * ki;
+    const int e = idx[s0];
+    gidx[p] = e >= 0 ? e / m : -1;
+    float w = 0.0f;
+    for (int j = 0; j < ki; ++j) w += G[s0 + j];
+    gw[p] = w;
+}
+
+cudaError_t launch_token_hier(const moe_shape &s, const void *x, const void *dy, int bf16,
+                              const void *E, const void *dXs, int ebf16, const int32_t *inv,
+                              const int32_t *idx, const float *G, const float *gimp,
+                              const float *WgT, const float *WnT, const float *eps, float *dc,
+                              float *dr, float *dcg, float *drg, float *dx, int32_t *err,
+                              cudaStream_t st) {
+    const dim3 grid(static_cast<unsigned>((s.T + 7) / 8));
+    if (s.k <= 4)
+        bwd_token_hier<4><<<grid, 256, 0, st>>>(s.T, s.d, s.n, s.k, s.groups, s.k_groups, x, dy,
+                                                bf16, E, dXs, ebf16, inv, idx, G, gimp, WgT, WnT,
+                                                eps, dc, dr, dcg, drg, dx, err);
+    else
+        bwd_token_hier<MOE_MAX_K><<<grid, 256, 0, st>>>(s.T, s.d, s.n, s.k, s.groups, s.k_groups, x,
+                                                        dy, bf16, E, dXs, ebf16, inv, idx, G, gimp,
+                                                        WgT, WnT, eps, dc, dr, dcg, drg, dx, err);
+    return cudaGetLastError();
+}
+
 // Gate weight gradients, in the same two passes: per chunk c of one expert's
 // rows, pg[c, q] = sum of x[t, q] dc[s], pn[c, q] = sum of x[t, q] dr[s] and
 // pb[c] = sum of dc[s] (rows in order; one thread per input column q) ...
@@ -753,8 +984,10 @@ __global__ void __launch_bounds__(256) bwd_gate_part(
     pn[c * d + q] = an;
 }
 
-// ... then dWg[q, e], dWn[q, e], dbg[e] = the sums over e's chunks in order.
-__global__ void __launch_bounds__(256) bwd_gate_fin(int d, int n, const int32_t *__restrict__ ctiles,
+// ... then dWg[q, col0 + e], dWn[q, col0 + e], dbg[col0 + e] = the sums over
+// e's chunks in order (row stride ldc: the gate's C score columns).
+__global__ void __launch_bounds__(256) bwd_gate_fin(int d, int n, int ldc, int col0,
+                                                    const int32_t *__restrict__ ctiles,
                                                     const float *__restrict__ pg,
                                                     const float *__restrict__ pn,
                                                     const float *__restrict__ pb,
@@ -766,7 +999,7 @@ __global__ void __launch_bounds__(256) bwd_gate_fin(int d, int n, const int32_t 
     if (dbg && blockIdx.x == 0 && threadIdx.x == 0) {
         float ab = 0.0f;
         for (int c = c0; c < c1; ++c) ab += pb[c];
-        dbg[e] = ab;
+        dbg[col0 + e] = ab;
     }
     if (q >= d) return;
     float ag = 0.0f, an = 0.0f;
@@ -774,31 +1007,57 @@ __global__ void __launch_bounds__(256) bwd_gate_fin(int d, int n, const int32_t 
         ag += pg[static_cast<int64_t>(c) * d + q];
         an += pn[static_cast<int64_t>(c) * d + q];
     }
-    dWg[static_cast<int64_t>(q) * n + e] = ag;
-    if (dWn) dWn[static_cast<int64_t>(q) * n + e] = an;
+    dWg[static_cast<int64_t>(q) * ldc + col0 + e] = ag;
+    if (dWn) dWn[static_cast<int64_t>(q) * ldc + col0 + e] = an;
 }
 
 // Chunk table, gate gradients and bias sums (both paths): the chunked row
 // sums of dc/dr into dWg, dWn, dbg, of dE into db2 and of dz into db1.
+// Hierarchical gating: the expert columns start at G (the group columns
+// come first), and the group columns get the same sums over the (token,
+// kept group) pairs, routed by group (Pairs).
 struct RowSums {
     int32_t *ctiles;
     float *pg, *pn, *pb, *pc;
 };
 
+struct Pairs {
+    const int32_t *offsets, *perm;   // the pairs t*kg + q in group order
+    const float *dc, *dr;            // per pair
+    int32_t *ctiles;                 // [G + 1] chunk table of the pairs
+};
+
 cudaError_t row_sums(const moe_shape &s, const RowSums &R, const int32_t *offsets,
                      const int32_t *perm, const void *x, int bf16, const float *dc, const float *dr,
                      float *dWg, float *dWn, float *dbg, const RowOp &dE_op, float *db2,
-                     const RowOp &dz_op, float *db1, int32_t *err, cudaStream_t st) {
+                     const RowOp &dz_op, float *db1, int32_t *err, cudaStream_t st,
+                     const Pairs *pairs = nullptr) {
     const int64_t S = slots(s);
     const int n = s.n, d = s.d, h = s.h;
+    const int C = gate_cols(s), col0 = s.groups;
     const unsigned chunks = static_cast<unsigned>((S + kChunkRows - 1) / kChunkRows + n);
     cudaError_t e = launch_row_tiles(offsets, n, kChunkRows, R.ctiles, st);
     if (e != cudaSuccess) return e;
     bwd_gate_part<<<dim3(chunks, (d + 255) / 256), 256, 0, st>>>(d, s.k, S, x, bf16, perm, offsets,
                                                                  R.ctiles, n, dc, dr, R.pg, R.pn,
                                                                  R.pb, err);
-    bwd_gate_fin<<<dim3((d + 255) / 256, n), 256, 0, st>>>(d, n, R.ctiles, R.pg, R.pn, R.pb, dWg, dWn,
-                                                           dbg);
+    bwd_gate_fin<<<dim3((d + 255) / 256, n), 256, 0, st>>>(d, n, C, col0, R.ctiles, R.pg, R.pn, R.pb,
+                                                           dWg, dWn, dbg);
+    if (pairs) {
+        // the group columns: the same two passes over the pairs of each group
+        // (P = T*kg pairs, fewer rows and columns than the slots: the partial
+        // buffers fit)
+        const int Gn = s.groups, kg = s.k_groups;
+        const int64_t P = s.T * kg;
+        const unsigned pchunks = static_cast<unsigned>((P + kChunkRows - 1) / kChunkRows + Gn);
+        if ((e = launch_row_tiles(pairs->offsets, Gn, kChunkRows, pairs->ctiles, st)) != cudaSuccess)
+            return e;
+        bwd_gate_part<<<dim3(pchunks, (d + 255) / 256), 256, 0, st>>>(
+            d, kg, P, x, bf16, pairs->perm, pairs->offsets, pairs->ctiles, Gn, pairs->dc, pairs->dr,
+            R.pg, R.pn, R.pb, err);
+        bwd_gate_fin<<<dim3((d + 255) / 256, Gn), 256, 0, st>>>(d, Gn, C, 0, pairs->ctiles, R.pg,
+                                                                R.pn, R.pb, dWg, dWn, dbg);
+    }
     if (db2) {
         bwd_colsum_part<<<dim3(chunks, (d + 255) / 256), 256, 0, st>>>(dE_op, d, offsets, R.ctiles, n,
                                                                        S, R.pc, err);
@@ -810,6 +1069,59 @@ cudaError_t row_sums(const moe_shape &s, const RowSums &R, const int32_t *offset
         bwd_colsum_fin<<<dim3((h + 255) / 256, n), 256, 0, st>>>(R.pc, h, R.ctiles, db1);
     }
     return cudaGetLastError();
+}
+
+// Routes the (token, kept group) pairs of a hierarchical selection by group
+// (the dispatch's own kernels on the pairs), for the group columns' sums.
+cudaError_t route_pairs(const moe_shape &s, const int32_t *idx, const float *G, void *ws,
+                        const PairLayout &P, cudaStream_t st) {
+    const int64_t np = s.T * s.k_groups;
+    int32_t *gidx = ws_ptr<int32_t>(ws, P.gidx);
+    float *gw = ws_ptr<float>(ws, P.gw);
+    bwd_pairs<<<static_cast<unsigned>((np + 255) / 256), 256, 0, st>>>(idx, G, s.T, s.k, s.k_groups,
+                                                                       s.n / s.groups, gidx, gw);
+    moe_shape sg = s;
+    sg.n = s.groups;
+    sg.k = s.k_groups;
+    sg.groups = 0;
+    sg.k_groups = 0;
+    WsLayout RL{};
+    RL.local_rank = P.local_rank;
+    RL.chunk = P.chunk;
+    RL.chunk_imp = P.chunk_imp;
+    RL.imp_acc = P.imp_acc;
+    return launch_dispatch(sg, gidx, gw, ws_ptr<int32_t>(ws, P.counts), ws_ptr<int32_t>(ws, P.offsets),
+                           ws_ptr<int32_t>(ws, P.perm), ws_ptr<int32_t>(ws, P.inv),
+                           ws_ptr<float>(ws, P.imp), ws_ptr<float>(ws, P.cv2), ws, RL, st);
+}
+
+// Gate side of both paths: W_g^T and W_noise^T over the C score columns, the
+// importance term, the token kernel (flat or two-level) and, for the
+// hierarchical gate, the pairs' routing for the group columns' sums.
+cudaError_t gate_side(const moe_shape &s, const void *x, const float *Wg, const float *Wn,
+                      const float *eps, const int32_t *idx, const float *G,
+                      const float *importance, const void *dy, int bf16, float w_imp,
+                      const void *E, const void *dXs, int ebf16, const int32_t *inv, float *WgT,
+                      float *WnT, float *gimp, float *dc, float *dr, float *dx, void *ws,
+                      const PairLayout &P, int32_t *err, cudaStream_t st) {
+    const int d = s.d, n = s.n, C = gate_cols(s);
+    bwd_transpose<<<dim3((C + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wg, d, C, WgT);
+    if (eps)
+        bwd_transpose<<<dim3((C + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wn, d, C, WnT);
+    bwd_gimp<<<1, 256, 0, st>>>(w_imp != 0.0f ? importance : nullptr, n, w_imp, gimp);
+    if (s.groups == 0)
+        return launch_token(s.T, d, n, s.k, x, dy, bf16, E, dXs, ebf16, inv, idx, G, gimp, WgT, WnT,
+                            eps, dc, dr, dx, err, st);
+    cudaError_t e = launch_token_hier(s, x, dy, bf16, E, dXs, ebf16, inv, idx, G, gimp, WgT, WnT,
+                                      eps, dc, dr, ws_ptr<float>(ws, P.dcg),
+                                      ws_ptr<float>(ws, P.drg), dx, err, st);
+    if (e != cudaSuccess) return e;
+    return route_pairs(s, idx, G, ws, P, st);
+}
+
+Pairs pairs_of(const moe_shape &s, void *ws, const PairLayout &P) {
+    return Pairs{ws_ptr<int32_t>(ws, P.offsets), ws_ptr<int32_t>(ws, P.perm),
+                 ws_ptr<float>(ws, P.dcg), ws_ptr<float>(ws, P.drg), ws_ptr<int32_t>(ws, P.ctiles)};
 }
 
 cudaError_t row_gemm(const RowGemm &g, int64_t S, int n, cudaStream_t st) {
@@ -836,11 +1148,12 @@ struct BtLayout {
     size_t W1T = 0, W2T = 0, dE = 0, dA = 0, dXs = 0, kblk = 0, PdE = 0, Pa = 0, PdZ = 0, Px = 0;
     size_t WgT = 0, WnT = 0, gimp = 0, dc = 0, dr = 0;
     size_t ctiles = 0, pg = 0, pn = 0, pb = 0, pc = 0;
+    PairLayout pairs;
     size_t total = 0;
 };
 
 bool backward_tc_supported(const moe_shape &s) {
-    return s.dtype == MOE_BF16 && s.groups == 0 && s.d % 128 == 0 && s.h % 128 == 0;
+    return s.dtype == MOE_BF16 && s.d % 128 == 0 && s.h % 128 == 0;
 }
 
 BtLayout bt_layout(const moe_shape &s) {
@@ -867,9 +1180,11 @@ BtLayout bt_layout(const moe_shape &s) {
     L.Pa = take(h * K * 2);
     L.PdZ = take(h * K * 2);
     L.Px = take(d * K * 2);
-    L.WgT = take(n * d * 4);
-    L.WnT = take(n * d * 4);
+    const size_t Cg = static_cast<size_t>(gate_cols(s));
+    L.WgT = take(Cg * d * 4);
+    L.WnT = take(Cg * d * 4);
     L.gimp = take(n * 4);
+    L.pairs = take_pairs(s, take);
     L.dc = take(S * 4);
     L.dr = take(S * 4);
     const size_t C = row_chunks(s);
@@ -907,7 +1222,7 @@ cudaError_t launch_backward_tc(const moe_shape &s, const void *x, const float *W
     float *gimp = ws_ptr<float>(ws, B.gimp), *dc = ws_ptr<float>(ws, B.dc), *dr = ws_ptr<float>(ws, B.dr);
     const float *eps_used = s.noisy ? eps : nullptr;
     float *dWn_used = s.noisy ? dWn : nullptr;
-    if (!s.noisy && dWn) cudaMemsetAsync(dWn, 0, sizeof(float) * d * n, st);
+    if (!s.noisy && dWn) cudaMemsetAsync(dWn, 0, sizeof(float) * d * gate_cols(s), st);
 
     cudaError_t e = launch_dispatch(s, idx, G, ws_ptr<int32_t>(ws, L.counts), offsets, perm, inv,
                                     ws_ptr<float>(ws, L.importance), ws_ptr<float>(ws, L.cv2), ws,
@@ -946,19 +1261,16 @@ cudaError_t launch_backward_tc(const moe_shape &s, const void *x, const float *W
     if (e != cudaSuccess) return e;
 
     // gate side and the sums over rows, on the CUDA cores
-    bwd_transpose<<<dim3((n + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wg, d, n, WgT);
-    if (eps_used)
-        bwd_transpose<<<dim3((n + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wn, d, n, WnT);
-    bwd_gimp<<<1, 256, 0, st>>>(w_imp != 0.0f ? importance : nullptr, n, w_imp, gimp);
-    if ((e = launch_token(s.T, d, n, k, x, dy, 1, E, dXs, 1, inv, idx, G, gimp, WgT, WnT, eps_used,
-                          dc, dr, dx, err, st)) != cudaSuccess)
+    if ((e = gate_side(s, x, Wg, Wn, eps_used, idx, G, importance, dy, 1, w_imp, E, dXs, 1, inv, WgT,
+                       WnT, gimp, dc, dr, dx, ws, B.pairs, err, st)) != cudaSuccess)
         return e;
     const RowOp dE_op{dy, 1, d, perm, k, G, 0};
     const RowOp dz_op{dZ, 1, h, nullptr, 1, nullptr, 0};
     const RowSums R{ws_ptr<int32_t>(ws, B.ctiles), ws_ptr<float>(ws, B.pg), ws_ptr<float>(ws, B.pn),
                     ws_ptr<float>(ws, B.pb), ws_ptr<float>(ws, B.pc)};
+    const Pairs pr = pairs_of(s, ws, B.pairs);
     return row_sums(s, R, offsets, perm, x, 1, dc, dr, dWg, dWn_used, dbg, dE_op, db2, dz_op, db1, err,
-                    st);
+                    st, s.groups ? &pr : nullptr);
 }
 
 size_t backward_workspace_bytes(const moe_shape &s) {
@@ -988,7 +1300,7 @@ cudaError_t launch_backward(const moe_shape &s, const void *x, const float *Wg, 
     float *E = ws_ptr<float>(ws, B.E), *dXs = ws_ptr<float>(ws, B.dXs);
     const float *eps_used = s.noisy ? eps : nullptr;
     float *dWn_used = s.noisy ? dWn : nullptr;
-    if (!s.noisy && dWn) cudaMemsetAsync(dWn, 0, sizeof(float) * d * n, st);
+    if (!s.noisy && dWn) cudaMemsetAsync(dWn, 0, sizeof(float) * d * gate_cols(s), st);
 
     // routing of the forward's selection (the dispatch's own chunk regions)
     WsLayout RL{};
@@ -1053,12 +1365,8 @@ cudaError_t launch_backward(const moe_shape &s, const void *x, const float *Wg, 
     g.N = d;
     if ((e = row_gemm(g, S, n, st)) != cudaSuccess) return e;
 
-    bwd_transpose<<<dim3((n + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wg, d, n, WgT);
-    if (eps_used)
-        bwd_transpose<<<dim3((n + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(Wn, d, n, WnT);
-    bwd_gimp<<<1, 256, 0, st>>>(w_imp != 0.0f ? importance : nullptr, n, w_imp, gimp);
-    if ((e = launch_token(s.T, d, n, k, x, dy, bf16, E, dXs, 0, inv, idx, G, gimp, WgT, WnT,
-                          eps_used, dc, dr, dx, err, st)) != cudaSuccess)
+    if ((e = gate_side(s, x, Wg, Wn, eps_used, idx, G, importance, dy, bf16, w_imp, E, dXs, 0, inv,
+                       WgT, WnT, gimp, dc, dr, dx, ws, B.pairs, err, st)) != cudaSuccess)
         return e;
 
     // dW2[e] = sum dE a^T  (M = d, N = h),  dW1[e] = sum dz x^T  (M = h, N = d)
@@ -1070,8 +1378,9 @@ cudaError_t launch_backward(const moe_shape &s, const void *x, const float *Wg, 
     bwd_wgrad<<<dim3(d / kBT, h / kBT, n), 256, 0, st>>>(dz_op, x_op, h, d, offsets, S, dW1, err);
     const RowSums R{ws_ptr<int32_t>(ws, B.ctiles), ws_ptr<float>(ws, B.pg), ws_ptr<float>(ws, B.pn),
                     ws_ptr<float>(ws, B.pb), ws_ptr<float>(ws, B.pc)};
+    const Pairs pr = pairs_of(s, ws, B.pairs);
     return row_sums(s, R, offsets, perm, x, bf16, dc, dr, dWg, dWn_used, dbg, dE_op, db2, dz_op, db1,
-                    err, st);
+                    err, st, s.groups ? &pr : nullptr);
 }
 
 }  // namespace
@@ -1082,7 +1391,7 @@ using namespace moe;
 extern "C" {
 
 size_t moe_backward_workspace_bytes(const moe_shape *s) {
-    if (moe_validate(s) != MOE_OK || s->groups != 0) return 0;
+    if (moe_validate(s) != MOE_OK) return 0;
     return backward_workspace_bytes(*s);
 }
 
@@ -1094,7 +1403,6 @@ moe_status moe_backward(const moe_shape *s, const void *x, const float *Wg, cons
                         float *db2, void *ws, size_t ws_bytes, void *stream) {
     moe_status v = moe_validate(s);
     if (v != MOE_OK) return v;
-    if (s->groups != 0) return MOE_ERR_UNSUPPORTED;
     auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     auto req = [&](const void *p) { return p != nullptr && al(p); };
     auto opt = [&](const void *p) { return p == nullptr || al(p); };
@@ -1113,12 +1421,12 @@ moe_status moe_backward(const moe_shape *s, const void *x, const float *Wg, cons
         ws_bytes < backward_workspace_bytes(*s))
         return MOE_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int64_t n = s->n, d = s->d, h = s->h;
+    const int64_t n = s->n, d = s->d, h = s->h, C = gate_cols(*s);
     if (s->T == 0) {
         // no slot: every gradient is zero
-        cudaMemsetAsync(dWg, 0, sizeof(float) * d * n, st);
-        if (dWnoise) cudaMemsetAsync(dWnoise, 0, sizeof(float) * d * n, st);
-        if (dbg) cudaMemsetAsync(dbg, 0, sizeof(float) * n, st);
+        cudaMemsetAsync(dWg, 0, sizeof(float) * d * C, st);
+        if (dWnoise) cudaMemsetAsync(dWnoise, 0, sizeof(float) * d * C, st);
+        if (dbg) cudaMemsetAsync(dbg, 0, sizeof(float) * C, st);
         cudaMemsetAsync(dW1, 0, sizeof(float) * n * h * d, st);
         cudaMemsetAsync(dW2, 0, sizeof(float) * n * d * h, st);
         if (db1) cudaMemsetAsync(db1, 0, sizeof(float) * n * h, st);

@@ -126,9 +126,12 @@ def test_backward_rejects_bad_arguments_before_any_launch():
     assert call(w=float("nan")) == B.MOE_ERR_INVALID_ARG
     assert call(nbytes=n - 256) == B.MOE_ERR_WORKSPACE
     assert call(ws=mis) == B.MOE_ERR_WORKSPACE
+    # the hierarchical gate has a backward too: its workspace adds the routed
+    # (token, group) pairs and the transposes of all groups + n score columns
     hier = B.make_shape(**dict(GOOD, n=16, groups=4, k_groups=2, k=4))
-    assert B.backward_workspace_bytes(hier) == 0
-    assert call(shape=hier) == B.MOE_ERR_UNSUPPORTED
+    hb = B.backward_workspace_bytes(hier)
+    assert hb > n and hb % 256 == 0
+    assert call(shape=hier) == B.MOE_ERR_WORKSPACE         # the flat shape's workspace is short
     assert call(shape=B.make_shape(**dict(GOOD, k=0))) == B.MOE_ERR_INVALID_ARG
 
 

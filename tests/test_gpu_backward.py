@@ -48,6 +48,20 @@ CASES = [
     (W("bwd_tc_k16", T=200, d=128, h=128, n=20, k=16, seed=54), 0.0),
     (W("bwd_tc_wide_experts", T=700, d=512, h=1024, n=3, k=1, bias_std=0.1, seed=55), 0.4),
     (W("bwd_tc_k8", T=200, d=256, h=256, n=20, k=8, bias_std=0.1, seed=56), 0.6),
+    # hierarchical gate (the 16 x 256 scheme of "MoE:稀疏门控混合专家", section 三,
+    # at test sizes): both softmax levels, group and expert columns
+    (W("bwd_hier_f32", T=120, d=64, h=128, n=16, k=4, groups=4, k_groups=2, dtype="f32",
+       bias_std=0.1, seed=61), 0.8),
+    (W("bwd_hier_bf16_cuda_cores", T=150, d=64, h=128, n=24, k=4, groups=6, k_groups=2,
+       seed=62), 0.5),
+    (W("bwd_hier_tc", T=400, d=256, h=512, n=64, k=4, groups=8, k_groups=2, bias_std=0.05,
+       seed=63), 1.0),
+    (W("bwd_hier_tc_one_group_kept", T=300, d=128, h=256, n=32, k=4, groups=4, k_groups=1,
+       seed=64), 0.3),
+    (W("bwd_hier_one_expert_per_group", T=100, d=128, h=128, n=16, k=2, groups=8, k_groups=2,
+       seed=65), 0.4),
+    (W("bwd_hier_k8_f32", T=100, d=64, h=64, n=32, k=8, groups=4, k_groups=2, dtype="f32",
+       seed=66), 0.6),
 ]
 
 
@@ -73,11 +87,12 @@ def run_backward(w, dinp, fwd, dy, w_imp):
     s = B.shape_of(w)
     ws = B.backward_workspace(s)
     T, d, h, n = w.T, w.d, w.h, w.n
+    C = n + w.groups   # gate score columns, the group columns first
 
     def f32(*shape):
         return torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
 
-    g = dict(dx=f32(T, d), dWg=f32(d, n), dWn=f32(d, n), dbg=f32(n), dW1=f32(n, h, d),
+    g = dict(dx=f32(T, d), dWg=f32(d, C), dWn=f32(d, C), dbg=f32(C), dW1=f32(n, h, d),
              db1=f32(n, h), dW2=f32(n, d, h), db2=f32(n, d))
     B.moe_backward(s, dinp["x"], dinp["Wg"], dinp["Wn"], dinp["eps"] if w.noisy else None,
                    dinp["W1"], dinp["b1"], dinp["W2"], dinp["b2"], fwd["idx"], fwd["G"],
@@ -89,6 +104,10 @@ def run_backward(w, dinp, fwd, dy, w_imp):
 
 
 def oracle_backward(w, inp, dy, w_imp):
+    if w.groups:
+        return oracle.backward_hier(inp["x"], inp["Wg"], inp["Wn"], inp["bg"],
+                                    inp["eps"] if w.noisy else None, inp["W1"], inp["b1"],
+                                    inp["W2"], inp["b2"], dy, w.k, w.groups, w.k_groups, w_imp)
     return oracle.backward(inp["x"], inp["Wg"], inp["Wn"], inp["bg"],
                            inp["eps"] if w.noisy else None, inp["W1"], inp["b1"], inp["W2"],
                            inp["b2"], dy, w.k, w_imp)
@@ -111,6 +130,14 @@ def test_backward_matches_oracle(w, w_imp):
         assert not got["dWn"].any()
     if w.k == 1:
         assert not got["dWg"].any() and not got["dbg"].any()
+    if w.groups:
+        # both softmaxes are shift invariant: the bias gradients of the group
+        # columns sum to zero, and so do those of each group's own columns
+        m, G = w.n // w.groups, w.groups
+        scale = 1.0 + np.abs(got["dbg"]).sum()
+        assert abs(float(got["dbg"][:G].sum())) <= 1e-4 * scale
+        for grp in range(G):
+            assert abs(float(got["dbg"][G + grp * m:G + (grp + 1) * m].sum())) <= 1e-4 * scale
 
 
 @pytest.mark.parametrize("case", [2, 9], ids=["cuda_cores", "tensor_cores"])
