@@ -183,7 +183,13 @@ def algorithmic(w: wl.Workload, counts: np.ndarray) -> dict:
     # buffer, hidden activations and gathered rows are not algorithmic
     ffn_bytes = weights + x_b
     flops = 4.0 * S * w.d * w.h
-    return dict(layer_bytes=layer_bytes, ffn_bytes=ffn_bytes, flops=flops, experts_hit=hit)
+    # the gate's contraction: x against the score columns each token is
+    # scored on (flat: n; hierarchical: the G group columns and the m columns
+    # of each of its k_groups kept groups), clean and (noisy) noise matrices
+    scored = w.n if w.groups == 0 else w.groups + w.k_groups * (w.n // w.groups)
+    gate_flops = 2.0 * w.T * w.d * scored * (2 if w.noisy else 1)
+    return dict(layer_bytes=layer_bytes, ffn_bytes=ffn_bytes, flops=flops,
+                gate_flops=gate_flops, layer_flops=flops + gate_flops, experts_hit=hit)
 
 
 # ---------------------------------------------------------------------------
@@ -626,7 +632,7 @@ def balanced_arm(args, w: wl.Workload):
     ms = e0.elapsed_time(e1) / args.steps
     alg = algorithmic(w, counts.cpu().numpy())
     pk = peaks()
-    t_roof = max(alg["layer_bytes"] / (pk["hbm"] * 1e9), alg["flops"] / (pk["bf16"] * 1e12))
+    t_roof = max(alg["layer_bytes"] / (pk["hbm"] * 1e9), alg["layer_flops"] / (pk["bf16"] * 1e12))
     line = {
         "metric": "MoE-layer tokens/sec with the batchwise mask (moe_forward_balanced, 1xB300)",
         "value": w.T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
@@ -636,7 +642,7 @@ def balanced_arm(args, w: wl.Workload):
         "config": dict(config_of(w), rows_per_expert=m, gate_scores="fp32 CUDA cores"),
         "layer_roofline": {"t_roof_us": t_roof * 1e6, "t_meas_us": ms * 1e3,
                            "frac": t_roof / (ms / 1e3), "algorithmic_bytes": alg["layer_bytes"],
-                           "flops": alg["flops"]},
+                           "flops": alg["layer_flops"]},
         "e2e": None, "cpu_baseline": None, "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -722,13 +728,14 @@ def rooflines(w, counts, ms_step, ffn_ms, long_run):
                                       if ffn_bound_hbm else "4*S*d*h FLOPs")
     roof["ms_per_launch"] = ffn_ms
     t_hbm = alg["layer_bytes"] / (pk["hbm"] * 1e9)
-    t_tc = alg["flops"] / (tc_peak * 1e12)
+    t_tc = alg["layer_flops"] / (tc_peak * 1e12)
     t_roof = max(t_hbm, t_tc)
     layer_roof = {"bound": "hbm" if t_hbm >= t_tc else "tensor",
                   "tensor_peak": f"{tc_label} {tc_peak} TFLOP/s",
                   "t_roof_us": t_roof * 1e6, "t_meas_us": ms_step * 1e3,
                   "frac": t_roof / (ms_step / 1e3), "algorithmic_bytes": alg["layer_bytes"],
-                  "flops": alg["flops"], "experts_hit": alg["experts_hit"]}
+                  "flops": alg["layer_flops"], "flops_accounting": "4*S*d*h (experts) + "
+                  "2*T*d*(scored columns) per gate matrix", "experts_hit": alg["experts_hit"]}
     return alg, roof, layer_roof
 
 
@@ -767,7 +774,8 @@ def time_workload(B, w: wl.Workload, dev, stream, steps: int, warmup: int) -> di
     alg, roof, layer_roof = rooflines(w, out["counts"].cpu().numpy(), ms_step, ffn_ms,
                                       ms > 1000.0)
     rec = {"config": config_of(w), "steps": steps, "warmup": warmup, "ms_per_step": ms_step,
-           "tokens_per_s": w.T / (ms_step / 1e3), "tflops": alg["flops"] / (ms_step / 1e3) / 1e12,
+           "tokens_per_s": w.T / (ms_step / 1e3),
+           "tflops": alg["layer_flops"] / (ms_step / 1e3) / 1e12,
            "layer_roofline_frac": layer_roof["frac"], "layer_bound": layer_roof["bound"],
            "t_roof_us": layer_roof["t_roof_us"],
            "ffn_stage": {"ms": ffn_ms, "bound": roof["bound"], "achieved": roof["achieved"],
@@ -959,7 +967,7 @@ def main():
             if w.dtype == "bf16" else "f32", "data": "synthetic (seeded counter-based normal)",
             "config": dict(config_of(w), l2=f"{nsets} rotating x/eps sets ({nsets * per_set / 1e6:.0f} MB)"
                            f" + {alg['layer_bytes'] / 1e9:.2f} GB algorithmic bytes per step > 126 MB L2"),
-            "tflops": alg["flops"] / (ms_step / 1e3) / 1e12,
+            "tflops": alg["layer_flops"] / (ms_step / 1e3) / 1e12,
             "layer_roofline": layer_roof,
             "roofline": roof,
             "cpu_baseline": cpu,

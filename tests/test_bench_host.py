@@ -40,6 +40,12 @@ def test_algorithmic_bytes_and_flops():
     weights = 3 * (2 * 64 * 128 * 2 + 4 * (64 + 128))
     assert a["experts_hit"] == 3
     assert a["flops"] == 4.0 * S * 64 * 128
+    # the gate: x (T x d) against the 4 clean and 4 noise columns
+    assert a["gate_flops"] == 2.0 * 10 * 64 * 4 * 2
+    assert a["layer_flops"] == a["flops"] + a["gate_flops"]
+    wh = wl.Workload("h", T=10, d=64, h=128, n=8, k=4, groups=4, k_groups=2)
+    # hierarchical: 4 group columns + 2 kept groups x 2 columns each
+    assert bench.algorithmic(wh, np.ones(8))["gate_flops"] == 2.0 * 10 * 64 * (4 + 2 * 2) * 2
     # the FFN stage: hit weights and x once; the slot buffer is not algorithmic
     assert a["ffn_bytes"] == weights + 10 * 64 * 2
     assert a["layer_bytes"] == (weights + 2 * 10 * 64 * 2 + 10 * 4 * 4 + 2 * 64 * 4 * 4 +
