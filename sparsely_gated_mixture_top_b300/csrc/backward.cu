@@ -1,4 +1,5 @@
-// backward.cu -- the backward pass of the flat layer (moe_backward in moe.h).
+// backward.cu -- the backward pass of the layer (moe_backward in moe.h), flat
+// or hierarchical gating.
 //
 // The pages train the layer: noise in the gate during training
 // ("MoE:稀疏门控混合专家", section 四) and an importance loss beside the task
@@ -16,6 +17,10 @@
 //   dx_t  = sum_j dc_j Wg[:,e_j] + dr_j Wn[:,e_j] + W1[e_j]^T dz_j
 //   dWg[:,e] = sum dc x,  dWn[:,e] = sum dr x,  dbg[e] = sum dc
 //   dW2[e] = sum dE a^T,  db2[e] = sum dE,  dW1[e] = sum dz x^T,  db1[e] = sum dz
+// For the hierarchical gate ("MoE:稀疏门控混合专家", section 三) the slot weight
+// is G = Gp_q Gi_qj and dG passes through both softmax levels to the kept
+// group columns and expert columns (bwd_token_hier, below); the expert
+// columns sit after the G group columns of Wg, Wn and bg.
 //
 // bf16 shapes whose widths are multiples of 128 run the contractions on the
 // tensor cores (launch_backward_tc below: bf16 operands, fp32 accumulation,

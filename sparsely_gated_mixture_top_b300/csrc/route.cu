@@ -92,9 +92,6 @@ __global__ void __launch_bounds__(1024) route_rank(const int32_t *__restrict__ i
     }
 }
 
-// Block (32 x 32): 32 experts (x) by 32 chunk segments (y).  Chunk counts
-// become chunk bases (exclusive scan down the chunks); the expert's count
-// and importance (fp32, chunk order) are the column totals.
 // route_rank for n <= kRankWarpsMaxN: the same outputs without the 32
 // barrier rounds.  Each warp's leaders write their group's count and fp32
 // gate-weight sum to a [32 warps][n] table; one thread per expert then walks
