@@ -754,67 +754,22 @@ cudaError_t launch_token(int64_t T, int d, int n, int k, const void *x, const vo
 // its share of dx.  Slot columns go to dc/dr [S], group columns to dcg/drg
 // [T*kg].  The slot loops run over compile-time indices (the per-slot
 // arrays stay in registers); slot j belongs to group j / ki.
+// The two softmax levels of one token (all lanes hold the warp sums):
+// from aE (<dy, E_s> partials), aR / aRg (x . Wn partials of the slot and
+// group columns) to dH, dr of the slots and dHg, drg of the kept groups;
+// lane 0 writes dc, dr, dcg, drg.
 template <int KM>
-__global__ void __launch_bounds__(256) bwd_token_hier(
-    int64_t T, int d, int n, int k, int Gn, int kg, const void *__restrict__ x,
-    const void *__restrict__ dy, int bf16, const void *__restrict__ E,
-    const void *__restrict__ dXs, int ebf16, const int32_t *__restrict__ inv_perm,
-    const int32_t *__restrict__ idx, const float *__restrict__ G, const float *__restrict__ gimp,
-    const float *__restrict__ WgT, const float *__restrict__ WnT, const float *__restrict__ eps,
-    float *__restrict__ dc, float *__restrict__ dr, float *__restrict__ dcg,
-    float *__restrict__ drg, float *__restrict__ dx, int32_t *err) {
-    const int lane = threadIdx.x & 31;
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
-    if (t >= T) return;
-    const int64_t S = T * k;
-    const int ki = k / kg, m = n / Gn, C = Gn + n;
-    int ex[KM], row[KM], grp[KM];
-    float aE[KM], aR[KM], aRg[KM];
-#pragma unroll
-    for (int j = 0; j < KM; ++j) {
-        ex[j] = 0;
-        row[j] = -1;
-        grp[j] = 0;
-        aE[j] = 0.0f;
-        aR[j] = 0.0f;
-        aRg[j] = 0.0f;
-        if (j >= k) continue;
-        const int64_t s = t * k + j;
-        const int e = idx[s];
-        const int r = inv_perm[s];
-        if (e < 0 || e >= n || r < 0 || r >= S) {
-            if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteBwdPerm, static_cast<int32_t>(s));
-            continue;
-        }
-        ex[j] = e;
-        row[j] = r;
-    }
-    // group of kept group q: that of its first slot
-#pragma unroll
-    for (int q = 0; q < KM; ++q) {
-        if (q >= kg) break;
-#pragma unroll
-        for (int j = 0; j < KM; ++j)
-            if (j < k && j == q * ki) grp[q] = ex[j] / m;
-    }
-#pragma unroll 4
-    for (int c = lane; c < d; c += 32) {
-        const float dv = ldf(dy, t * d + c, bf16);
-        const float xv = eps ? ldf(x, t * d + c, bf16) : 0.0f;
-#pragma unroll
-        for (int j = 0; j < KM; ++j) {
-            if (j >= k) break;
-            if (row[j] >= 0) aE[j] = fmaf(dv, ldf(E, static_cast<int64_t>(row[j]) * d + c, ebf16), aE[j]);
-            if (eps) aR[j] = fmaf(xv, WnT[static_cast<int64_t>(Gn + ex[j]) * d + c], aR[j]);
-        }
-        if (eps) {
-#pragma unroll
-            for (int q = 0; q < KM; ++q) {
-                if (q >= kg) break;
-                aRg[q] = fmaf(xv, WnT[static_cast<int64_t>(grp[q]) * d + c], aRg[q]);
-            }
-        }
-    }
+__device__ __forceinline__ void hier_levels(int lane, int64_t t, int k, int kg, int Gn, int n,
+                                            const int (&ex)[KM], const int (&grp)[KM],
+                                            const float (&aE)[KM], const float (&aR)[KM],
+                                            const float (&aRg)[KM], const float *__restrict__ G,
+                                            const float *__restrict__ gimp,
+                                            const float *__restrict__ eps, float *__restrict__ dc,
+                                            float *__restrict__ dr, float *__restrict__ dcg,
+                                            float *__restrict__ drg, float (&dH)[KM],
+                                            float (&drv)[KM], float (&dHg)[KM],
+                                            float (&drgv)[KM]) {
+    const int ki = k / kg, C = Gn + n;
     float dG[KM], Gs[KM];
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
@@ -824,7 +779,6 @@ __global__ void __launch_bounds__(256) bwd_token_hier(
         dG[j] = warp_sum(aE[j]) + gimp[ex[j]];
         Gs[j] = G[t * k + j];
     }
-    // the two softmax levels
     float Gp[KM], dGp[KM], sI[KM];
 #pragma unroll
     for (int q = 0; q < KM; ++q) {
@@ -852,7 +806,6 @@ __global__ void __launch_bounds__(256) bwd_token_hier(
 #pragma unroll
     for (int q = 0; q < KM; ++q)
         if (q < kg) sP = fmaf(Gp[q], dGp[q], sP);
-    float dH[KM], drv[KM], dHg[KM], drgv[KM];
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
         dH[j] = 0.0f;
@@ -885,25 +838,198 @@ __global__ void __launch_bounds__(256) bwd_token_hier(
             drg[t * kg + q] = drgv[q];
         }
     }
+}
+
+// The slots' experts, expert rows and kept groups of token t (group of kept
+// group q: that of its first slot).  Bad entries are reported and skipped.
+template <int KM>
+__device__ __forceinline__ void hier_slots(int lane, int64_t t, int64_t S, int k, int kg, int n,
+                                           int Gn, const int32_t *__restrict__ idx,
+                                           const int32_t *__restrict__ inv_perm, int32_t *err,
+                                           int (&ex)[KM], int (&row)[KM], int (&grp)[KM]) {
+    const int ki = k / kg, m = n / Gn;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        ex[j] = 0;
+        row[j] = -1;
+        grp[j] = 0;
+    }
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        if (j >= k) continue;
+        const int64_t s = t * k + j;
+        const int e = idx[s];
+        const int r = inv_perm[s];
+        if (e < 0 || e >= n || r < 0 || r >= S) {
+            if (lane == 0) report(err, MOE_ERR_DEVICE, kSiteBwdPerm, static_cast<int32_t>(s));
+            continue;
+        }
+        ex[j] = e;
+        row[j] = r;
+    }
+#pragma unroll
+    for (int q = 0; q < KM; ++q) {
+        if (q >= kg) break;
+#pragma unroll
+        for (int j = 0; j < KM; ++j)
+            if (j < k && j == q * ki) grp[q] = ex[j] / m;
+    }
+}
+
+// Hierarchical gating, one warp per token.  The k slots hold kg kept
+// groups of ki experts each, group-major (slot q*ki + j); G = Gp_q Gi_qj with
+// Gp the weights of the kept groups and Gi those of the experts inside group
+// q.  Score columns: group g at g, expert e at Gn + e (C in all).  From
+// dG_s = <dy, E_s> + gimp[e_s]:
+//   dGp_q = sum_j dG_qj Gi_qj,  dGi_qj = dG_qj Gp_q
+//   dHi_qj = Gi_qj (dGi_qj - sum_l Gi_ql dGi_ql),  dHp_q = Gp_q (dGp_q - sum_l Gp_l dGp_l)
+// and every kept column gives dc = dH, dr = dH eps sigmoid(x . Wn[:, col]) and
+// its share of dx.  Slot columns go to dc/dr [S], group columns to dcg/drg
+// [T*kg].  The slot loops run over compile-time indices (the per-slot
+// arrays stay in registers); slot j belongs to group j / ki.  V8: bf16 rows
+// with d a multiple of 256, 8 consecutive columns per lane and step (16-byte
+// loads of the bf16 rows, 32-byte loads of the fp32 gate columns); else one
+// column per lane and step, any dtype.
+template <int KM, bool V8>
+__global__ void __launch_bounds__(256) bwd_token_hier(
+    int64_t T, int d, int n, int k, int Gn, int kg, const void *__restrict__ x,
+    const void *__restrict__ dy, int bf16, const void *__restrict__ E,
+    const void *__restrict__ dXs, int ebf16, const int32_t *__restrict__ inv_perm,
+    const int32_t *__restrict__ idx, const float *__restrict__ G, const float *__restrict__ gimp,
+    const float *__restrict__ WgT, const float *__restrict__ WnT, const float *__restrict__ eps,
+    float *__restrict__ dc, float *__restrict__ dr, float *__restrict__ dcg,
+    float *__restrict__ drg, float *__restrict__ dx, int32_t *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+    if (t >= T) return;
+    int ex[KM], row[KM], grp[KM];
+    hier_slots<KM>(lane, t, T * k, k, kg, n, Gn, idx, inv_perm, err, ex, row, grp);
+    float aE[KM], aR[KM], aRg[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) aE[j] = aR[j] = aRg[j] = 0.0f;
+    if constexpr (V8) {
+        const auto *xb = static_cast<const __nv_bfloat16 *>(x);
+        const auto *dyb = static_cast<const __nv_bfloat16 *>(dy);
+        const auto *Eb = static_cast<const __nv_bfloat16 *>(E);
+        for (int c0 = lane * 8; c0 < d; c0 += 256) {
+            float dv[8], xv[8];
+            bf16x8(dyb + t * d + c0, dv);
+            if (eps) bf16x8(xb + t * d + c0, xv);
+#pragma unroll
+            for (int j = 0; j < KM; ++j) {
+                if (j >= k) break;
+                if (row[j] >= 0) {
+                    float ev[8];
+                    bf16x8(Eb + static_cast<int64_t>(row[j]) * d + c0, ev);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) aE[j] = fmaf(dv[i], ev[i], aE[j]);
+                }
+                if (eps) {
+                    float wv[8];
+                    f32x8(WnT + static_cast<int64_t>(Gn + ex[j]) * d + c0, wv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) aR[j] = fmaf(xv[i], wv[i], aR[j]);
+                }
+            }
+            if (eps) {
+#pragma unroll
+                for (int q = 0; q < KM; ++q) {
+                    if (q >= kg) break;
+                    float wv[8];
+                    f32x8(WnT + static_cast<int64_t>(grp[q]) * d + c0, wv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) aRg[q] = fmaf(xv[i], wv[i], aRg[q]);
+                }
+            }
+        }
+    } else {
 #pragma unroll 4
-    for (int c = lane; c < d; c += 32) {
-        float acc = 0.0f;
+        for (int c = lane; c < d; c += 32) {
+            const float dv = ldf(dy, t * d + c, bf16);
+            const float xv = eps ? ldf(x, t * d + c, bf16) : 0.0f;
 #pragma unroll
-        for (int j = 0; j < KM; ++j) {
-            if (j >= k) break;
-            const int64_t we = static_cast<int64_t>(Gn + ex[j]) * d + c;
-            acc = fmaf(dH[j], WgT[we], acc);
-            if (eps) acc = fmaf(drv[j], WnT[we], acc);
-            if (row[j] >= 0) acc += ldf(dXs, static_cast<int64_t>(row[j]) * d + c, ebf16);
-        }
+            for (int j = 0; j < KM; ++j) {
+                if (j >= k) break;
+                if (row[j] >= 0) aE[j] = fmaf(dv, ldf(E, static_cast<int64_t>(row[j]) * d + c, ebf16), aE[j]);
+                if (eps) aR[j] = fmaf(xv, WnT[static_cast<int64_t>(Gn + ex[j]) * d + c], aR[j]);
+            }
+            if (eps) {
 #pragma unroll
-        for (int q = 0; q < KM; ++q) {
-            if (q >= kg) break;
-            const int64_t wg = static_cast<int64_t>(grp[q]) * d + c;
-            acc = fmaf(dHg[q], WgT[wg], acc);
-            if (eps) acc = fmaf(drgv[q], WnT[wg], acc);
+                for (int q = 0; q < KM; ++q) {
+                    if (q >= kg) break;
+                    aRg[q] = fmaf(xv, WnT[static_cast<int64_t>(grp[q]) * d + c], aRg[q]);
+                }
+            }
         }
-        dx[t * d + c] = acc;
+    }
+    float dH[KM], drv[KM], dHg[KM], drgv[KM];
+    hier_levels<KM>(lane, t, k, kg, Gn, n, ex, grp, aE, aR, aRg, G, gimp, eps, dc, dr, dcg, drg,
+                    dH, drv, dHg, drgv);
+    if constexpr (V8) {
+        const auto *dXb = static_cast<const __nv_bfloat16 *>(dXs);
+        for (int c0 = lane * 8; c0 < d; c0 += 256) {
+            float acc[8] = {};
+#pragma unroll
+            for (int j = 0; j < KM; ++j) {
+                if (j >= k) break;
+                const int64_t we = static_cast<int64_t>(Gn + ex[j]) * d + c0;
+                float wg[8];
+                f32x8(WgT + we, wg);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(dH[j], wg[i], acc[i]);
+                if (eps) {
+                    float wn[8];
+                    f32x8(WnT + we, wn);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(drv[j], wn[i], acc[i]);
+                }
+                if (row[j] >= 0) {
+                    float xr[8];
+                    bf16x8(dXb + static_cast<int64_t>(row[j]) * d + c0, xr);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] += xr[i];
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < KM; ++q) {
+                if (q >= kg) break;
+                const int64_t wq = static_cast<int64_t>(grp[q]) * d + c0;
+                float wg[8];
+                f32x8(WgT + wq, wg);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(dHg[q], wg[i], acc[i]);
+                if (eps) {
+                    float wn[8];
+                    f32x8(WnT + wq, wn);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(drgv[q], wn[i], acc[i]);
+                }
+            }
+            float4 *o = reinterpret_cast<float4 *>(dx + t * d + c0);
+            o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+    } else {
+#pragma unroll 4
+        for (int c = lane; c < d; c += 32) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int j = 0; j < KM; ++j) {
+                if (j >= k) break;
+                const int64_t we = static_cast<int64_t>(Gn + ex[j]) * d + c;
+                acc = fmaf(dH[j], WgT[we], acc);
+                if (eps) acc = fmaf(drv[j], WnT[we], acc);
+                if (row[j] >= 0) acc += ldf(dXs, static_cast<int64_t>(row[j]) * d + c, ebf16);
+            }
+#pragma unroll
+            for (int q = 0; q < KM; ++q) {
+                if (q >= kg) break;
+                const int64_t wg = static_cast<int64_t>(grp[q]) * d + c;
+                acc = fmaf(dHg[q], WgT[wg], acc);
+                if (eps) acc = fmaf(drgv[q], WnT[wg], acc);
+            }
+            dx[t * d + c] = acc;
+        }
     }
 }
 
@@ -929,16 +1055,26 @@ cudaError_t launch_token_hier(const moe_shape &s, const void *x, const void *dy,
                               float *dr, float *dcg, float *drg, float *dx, int32_t *err,
                               cudaStream_t st) {
     const dim3 grid(static_cast<unsigned>((s.T + 7) / 8));
-    if (s.k <= 4)
-        bwd_token_hier<4><<<grid, 256, 0, st>>>(s.T, s.d, s.n, s.k, s.groups, s.k_groups, x, dy,
-                                                bf16, E, dXs, ebf16, inv, idx, G, gimp, WgT, WnT,
-                                                eps, dc, dr, dcg, drg, dx, err);
-    else
-        bwd_token_hier<MOE_MAX_K><<<grid, 256, 0, st>>>(s.T, s.d, s.n, s.k, s.groups, s.k_groups, x,
-                                                        dy, bf16, E, dXs, ebf16, inv, idx, G, gimp,
-                                                        WgT, WnT, eps, dc, dr, dcg, drg, dx, err);
+    const bool v8 = bf16 && ebf16 && s.d % 256 == 0;
+#define MOE_TOKEN_HIER(KM, V)                                                                   \
+    bwd_token_hier<KM, V><<<grid, 256, 0, st>>>(s.T, s.d, s.n, s.k, s.groups, s.k_groups, x, dy, \
+                                                bf16, E, dXs, ebf16, inv, idx, G, gimp, WgT, WnT, \
+                                                eps, dc, dr, dcg, drg, dx, err)
+    if (s.k <= 4) {
+        if (v8)
+            MOE_TOKEN_HIER(4, true);
+        else
+            MOE_TOKEN_HIER(4, false);
+    } else {
+        if (v8)
+            MOE_TOKEN_HIER(MOE_MAX_K, true);
+        else
+            MOE_TOKEN_HIER(MOE_MAX_K, false);
+    }
+#undef MOE_TOKEN_HIER
     return cudaGetLastError();
 }
+
 
 // Gate weight gradients, in the same two passes: per chunk c of one expert's
 // rows, pg[c, q] = sum of x[t, q] dc[s], pn[c, q] = sum of x[t, q] dr[s] and
