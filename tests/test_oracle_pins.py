@@ -228,6 +228,47 @@ def test_hierarchical_single_group_reduces_to_flat():
     np.testing.assert_allclose(G_h, G_f, rtol=1e-15)
 
 
+def test_hierarchical_one_expert_per_group_is_the_flat_group_gate():
+    """m = 1: every kept group holds one expert with in-group weight 1, so the
+    layer's choice and weights are the flat gate over the G group columns."""
+    rng = np.random.default_rng(6)
+    T, G, d = 20, 7, 6
+    x = rng.normal(size=(T, d))
+    Wg, Wn = rng.normal(size=(d, 2 * G)), rng.normal(size=(d, 2 * G))
+    bg, eps = rng.normal(size=2 * G) * 0.3, rng.normal(size=(T, 2 * G))
+    idx_h, G_h, _ = oracle.gate_hier(x, Wg, Wn, bg, eps, G, 3, 3)
+    idx_f, G_f, _, _ = oracle.gate_flat(x, Wg[:, :G], Wn[:, :G], bg[:G], eps[:, :G], 3)
+    assert np.array_equal(idx_h, idx_f)
+    np.testing.assert_allclose(G_h, G_f, rtol=1e-15)
+
+
+@pytest.mark.parametrize("G,m,kg,ki", [(4, 6, 2, 3), (3, 5, 3, 2), (5, 4, 2, 1)])
+def test_hierarchical_levels_are_flat_gates(G, m, kg, ki):
+    """Each level of the two-level gate is the (independently pinned) flat
+    gate on its own columns: the kept groups and the group weights (the sums
+    of each group's final weights) are the flat gate over the group columns,
+    and within a kept group the experts and the weight ratios are the flat
+    gate over that group's columns; the final weight is their product."""
+    rng = np.random.default_rng(100 * G + m)
+    T = 25
+    x, Wg, Wn, bg, eps = _hier_case(rng, T, G, m, noisy=True)
+    idx_h, G_h, _ = oracle.gate_hier(x, Wg, Wn, bg, eps, G, kg, kg * ki)
+    idx_g, G_g, _, _ = oracle.gate_flat(x, Wg[:, :G], Wn[:, :G], bg[:G], eps[:, :G], kg)
+    for t in range(T):
+        for q in range(kg):
+            sl = slice(q * ki, (q + 1) * ki)
+            g = int(idx_g[t, q])
+            assert set((idx_h[t, sl] // m).tolist()) == {g}
+            wsum = G_h[t, sl].sum()
+            assert wsum == pytest.approx(G_g[t, q], rel=1e-13)
+            cols = slice(G + g * m, G + (g + 1) * m)
+            idx_i, G_i, _, _ = oracle.gate_flat(x[t:t + 1], Wg[:, cols], Wn[:, cols], bg[cols],
+                                                eps[t:t + 1, cols], ki)
+            assert (idx_h[t, sl] - g * m).tolist() == idx_i[0].tolist()
+            np.testing.assert_allclose(G_h[t, sl] / wsum, G_i[0], rtol=1e-12)
+            np.testing.assert_allclose(G_h[t, sl], G_g[t, q] * G_i[0], rtol=1e-12)
+
+
 # --------------------------------------------------------------------------
 # Routing: counts, offsets, stable permutation, importance, CV^2.
 # --------------------------------------------------------------------------
