@@ -52,11 +52,12 @@ def parse():
     p.add_argument("--no-per-workload", action="store_true",
                    help="skip the other full-size workloads (per_workload field)")
     p.add_argument("--per-workload-steps", type=int, default=20)
-    p.add_argument("--pass", dest="which", choices=["forward", "backward", "balanced"],
+    p.add_argument("--pass", dest="which", choices=["forward", "backward", "balanced", "ep"],
                    default="forward",
-                   help="forward: moe_forward (the headline); backward: moe_backward of the flat "
-                        "layer with the forward's selection; balanced: moe_forward_balanced with "
-                        "the batchwise mask")
+                   help="forward: moe_forward (the headline); backward: moe_backward with the "
+                        "forward's selection; balanced: moe_forward_balanced with the batchwise "
+                        "mask; ep: the expert-parallel layer (experts split over the ranks, "
+                        "all-to-all over NCCL; one rank when run without torchrun)")
     p.add_argument("--traffic-summary", nargs=2, metavar=("NCU_CSV", "BENCH_JSON"),
                    help="print the DRAM-traffic record of one expert-FFN stage from an ncu "
                         "--csv log of the stage's launches (TRAFFIC_NCU) and the bench line "
@@ -588,6 +589,76 @@ def backward_arm(args, w: wl.Workload):
     print(json.dumps(line), flush=True)
 
 
+def ep_arm(args, w: wl.Workload):
+    """Times the expert-parallel layer (ExpertParallelMoE.forward): every rank
+    gates its own batch of the workload's T tokens against all n experts,
+    holds n/P of the experts, and the rows travel by NCCL all-to-all.  Without
+    torchrun it runs as a one-rank group (the exchange is then local).  The
+    job time is the slowest rank's; value counts every rank's tokens."""
+    import socket
+    import torch.distributed as dist
+    from sparsely_gated_mixture_top_b300 import binding as B
+    from sparsely_gated_mixture_top_b300.expert_parallel import ExpertParallelMoE
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world == 1 and "MASTER_PORT" not in os.environ:
+        with socket.socket() as so:
+            so.bind(("127.0.0.1", 0))
+            os.environ["MASTER_PORT"] = str(so.getsockname()[1])
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", rank=0, world_size=1, device_id=dev)
+    else:
+        dist.init_process_group("nccl", device_id=dev)
+    try:
+        host = wl.make_inputs(w.with_(seed=w.seed + rank))
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+        fields = dict(d=w.d, h=w.h, n=w.n, k=w.k, groups=w.groups, k_groups=w.k_groups,
+                      dtype=w.dtype, noisy=w.noisy)
+        layer = ExpertParallelMoE(fields, B.make_shape)
+        sl = slice(layer.first_expert, layer.first_expert + layer.n_local)
+        W1, W2 = d["W1"][sl].contiguous(), d["W2"][sl].contiguous()
+        b1 = None if d["b1"] is None else d["b1"][sl].contiguous()
+        b2 = None if d["b2"] is None else d["b2"][sl].contiguous()
+
+        def step():
+            return layer.forward(d["x"], d["Wg"], d["Wn"], d["bg"], d["eps"], W1, b1, W2, b2)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        layer.ops.check()
+        dist.barrier()
+        clocks = ClockSampler(local)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            out = step()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        dist.barrier()
+        layer.ops.check()
+        ms, value = job_throughput(e0.elapsed_time(e1), w.T * args.steps, dist, dev)
+        if rank == 0:
+            print(json.dumps({
+                "metric": "MoE-layer tokens/sec, expert-parallel (ExpertParallelMoE.forward)",
+                "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == "bf16" else "f32",
+                "data": "synthetic (seeded counter-based normal)",
+                "config": dict(config_of(w), experts_per_rank=layer.n_local,
+                               exchange="NCCL all-to-all (counts, rows out, rows back), "
+                                        "all-reduce of importance"),
+                "rows_in_last_step": out["rows_in"], "e2e": None, "cpu_baseline": None,
+                "clocks": clk}), flush=True)
+    finally:
+        dist.destroy_process_group()
+
+
 def balanced_arm(args, w: wl.Workload):
     """Times moe_forward_balanced with the batchwise mask (every expert keeps
     floor(k*T/n) tokens) on the workload, inputs resident on the device."""
@@ -800,6 +871,9 @@ def main():
         return
     if args.which == "balanced":
         balanced_arm(args, w)
+        return
+    if args.which == "ep":
+        ep_arm(args, w)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
