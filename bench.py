@@ -60,19 +60,30 @@ def parse():
                         "all-to-all over NCCL; one rank when run without torchrun)")
     p.add_argument("--traffic-summary", nargs=2, metavar=("NCU_CSV", "BENCH_JSON"),
                    help="print the DRAM-traffic record of one expert-FFN stage from an ncu "
-                        "--csv log of the stage's launches (TRAFFIC_NCU) and the bench line "
+                        "--csv log of the stage's launches (traffic_ncu) and the bench line "
                         "of the same command, then exit")
     return p.parse_args()
 
 
 TRAFFIC_BENCH = "python bench.py --steps 3 --warmup 3 --e2e-steps 3 --no-cpu-baseline --no-per-workload"
-TRAFFIC_NCU = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
-               "--clock-control none -k regex:ffn_ -s 12 -c 4 --csv --log-file traffic.csv ")
+
+
+def traffic_ncu(w: wl.Workload) -> str:
+    """The ncu command (before TRAFFIC_BENCH) that counts the DRAM bytes of
+    the launches of one moe_expert_ffn call (tile table, gather, then the
+    fused kernel or the two grouped GEMMs).  TRAFFIC_BENCH runs six forward
+    steps first, each launching the FFN kernels alone (their tables come from
+    the dispatch); those launches are skipped."""
+    per_step = 1 if fused_ffn(w) else 2
+    return ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
+            f"--clock-control none -k regex:ffn_ -s {6 * per_step} -c {2 + per_step} --csv "
+            "--log-file traffic.csv ")
 
 
 def traffic_summary(csv_path: str, bench_json: str, w: wl.Workload) -> dict:
-    """DRAM bytes of the four launches of one expert-FFN stage (tile table,
-    gather, two grouped GEMMs) of the first timed step, as ncu counted them."""
+    """DRAM bytes of the launches of one expert-FFN stage (tile table, gather,
+    the fused kernel or two grouped GEMMs) of the stage timing call, as ncu
+    counted them."""
     import csv
     with open(csv_path) as f:
         lines = [ln for ln in f if ln.startswith('"')]
@@ -93,9 +104,11 @@ def traffic_summary(csv_path: str, bench_json: str, w: wl.Workload) -> dict:
     total = sum(k["dram_read_bytes"] + k["dram_write_bytes"] for k in kernels)
     return {
         "workload": w.name,
-        "what": "DRAM bytes (read + write) of the four launches of one expert-FFN stage "
-                "(moe_expert_ffn: token-tile table, gather, two pair GEMMs), stage timing call",
-        "command": f"{TRAFFIC_BENCH} (exit 0), then: {TRAFFIC_NCU}{TRAFFIC_BENCH}",
+        "what": "DRAM bytes (read + write) of the launches of one expert-FFN stage "
+                "(moe_expert_ffn: token-tile table, gather, "
+                + ("both layers in one kernel" if fused_ffn(w) else "two pair GEMMs")
+                + "), stage timing call",
+        "command": f"{TRAFFIC_BENCH} (exit 0), then: {traffic_ncu(w)}{TRAFFIC_BENCH}",
         "source_sha256": source_digest(),
         "ffn_stage_dram_bytes_per_launch": total,
         "algorithmic_bytes_per_launch": line["roofline"]["algorithmic_per_launch"],
@@ -117,7 +130,8 @@ def peaks():
         return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
 
 
-FFN_STAGE_SOURCES = ("ffn.cu", "ffn_tc.cu", "ffn_pair.cu", "moe_device.cuh", "moe_launch.h")
+FFN_STAGE_SOURCES = ("ffn.cu", "ffn_tc.cu", "ffn_pair.cu", "ffn_fused.cu", "moe_device.cuh",
+                     "moe_launch.h")
 
 
 def source_digest() -> str:
@@ -439,16 +453,25 @@ def config_of(w: wl.Workload) -> dict:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+def fused_ffn(w: wl.Workload) -> bool:
+    """Whether the expert stage runs both layers in one kernel (bf16, model
+    width 256 or 512, hidden width a multiple of 256, at most 128 rows per
+    expert on average)."""
+    return (w.dtype == "bf16" and w.d % 256 == 0 and w.d <= 512 and w.h % 256 == 0
+            and w.T * w.k <= 128 * w.n)
+
+
 def launches_per_step(w: wl.Workload) -> int:
     """Kernels moe_forward launches per step.  Flat gating: gate (weight pack,
     scores + KeepTopK) 2, dispatch (rank, column scan + tables, scatter with
-    the x-row gather) 3, expert FFN (two grouped GEMMs; their tables come from
-    the dispatch) 2, combine 1.  Hierarchical gating adds to the gate: the
+    the x-row gather) 3, expert FFN (one kernel for both layers where the
+    widths allow, else two grouped GEMMs; their tables come from the
+    dispatch) 1 or 2, combine 1.  Hierarchical gating adds to the gate: the
     group pass (pack, scores + KeepTopK), a dispatch of the (token, group)
     pairs (3), their row tiles, the gather of their x rows, and the in-group
     pass (pack, scores + KeepTopK)."""
     gate = 2 if not w.groups else 2 + 3 + 1 + 1 + 2
-    return gate + 3 + 2 + 1
+    return gate + 3 + (1 if fused_ffn(w) else 2) + 1
 
 
 def counted_launches(B, call, expected: int) -> dict:

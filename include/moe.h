@@ -115,6 +115,13 @@ MOE_API int32_t moe_version(void);
 /* Static text for a status code. */
 MOE_API const char *moe_status_string(moe_status s);
 
+/* The CUDA error code (a cudaError_t value) behind the last MOE_ERR_CUDA that
+ * an entry point returned on the calling host thread, 0 if there was none,
+ * and the CUDA runtime's static name for such a code.  Host-only; no device
+ * work. */
+MOE_API int32_t moe_last_cuda_error(void);
+MOE_API const char *moe_cuda_error_name(int32_t code);
+
 /* Host-only check of a shape against the rules above.  No device work. */
 MOE_API moe_status moe_validate(const moe_shape *shape);
 

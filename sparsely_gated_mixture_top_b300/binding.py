@@ -27,7 +27,8 @@ MOE_ERR_DEVICE = -6
 MOE_F32 = 0
 MOE_BF16 = 1
 
-EXPORTS = ("moe_version", "moe_status_string", "moe_validate", "moe_workspace_bytes",
+EXPORTS = ("moe_version", "moe_status_string", "moe_last_cuda_error", "moe_cuda_error_name",
+           "moe_validate", "moe_workspace_bytes",
            "moe_workspace_init", "moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine",
            "moe_forward", "moe_check", "moe_dispatch_noalloc", "moe_load_workspace_bytes",
            "moe_gate_load", "moe_backward_workspace_bytes", "moe_backward",
@@ -44,7 +45,11 @@ class MoEShape(ctypes.Structure):
 class MoEError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn}: {status_string(status)} ({status})")
+        msg = f"{fn}: {status_string(status)} ({status})"
+        if status == MOE_ERR_CUDA:
+            code = lib.moe_last_cuda_error()
+            msg += f" [{lib.moe_cuda_error_name(code).decode()} = {code}]"
+        super().__init__(msg)
 
 
 def _load():
@@ -55,6 +60,8 @@ def _load():
     vp, sz, i32, shp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.POINTER(MoEShape)
     lib.moe_version.argtypes, lib.moe_version.restype = [], i32
     lib.moe_status_string.argtypes, lib.moe_status_string.restype = [i32], ctypes.c_char_p
+    lib.moe_last_cuda_error.argtypes, lib.moe_last_cuda_error.restype = [], i32
+    lib.moe_cuda_error_name.argtypes, lib.moe_cuda_error_name.restype = [i32], ctypes.c_char_p
     lib.moe_validate.argtypes, lib.moe_validate.restype = [shp], i32
     lib.moe_workspace_bytes.argtypes, lib.moe_workspace_bytes.restype = [shp], sz
     lib.moe_workspace_init.argtypes, lib.moe_workspace_init.restype = [vp, sz, vp], i32

@@ -36,9 +36,18 @@ moe_status check_ws(const moe_shape *s, const void *ws, size_t ws_bytes) {
     return MOE_OK;
 }
 
-moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+moe_status cuda_status(cudaError_t e) { return cuda_to_status(e); }
+
+thread_local int32_t g_last_cuda_error = 0;
 
 }  // namespace
+
+moe_status cuda_to_status(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    g_last_cuda_error = static_cast<int32_t>(e);
+    return MOE_ERR_CUDA;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -46,6 +55,12 @@ using namespace moe;
 extern "C" {
 
 int32_t moe_version(void) { return 100; }
+
+int32_t moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *moe_cuda_error_name(int32_t code) {
+    return cudaGetErrorName(static_cast<cudaError_t>(code));
+}
 
 const char *moe_status_string(moe_status s) {
     switch (s) {

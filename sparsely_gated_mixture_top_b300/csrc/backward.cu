@@ -1369,7 +1369,8 @@ cudaError_t launch_backward_tc(const moe_shape &s, const void *x, const float *W
                                     ws_ptr<float>(ws, L.importance), ws_ptr<float>(ws, L.cv2), ws,
                                     L, st);
     // recompute x rows, a = ReLU(x W1^T + b1) and E = a W2^T + b2 (bf16, expert order)
-    if (e == cudaSuccess) e = launch_expert_ffn(s, x, perm, offsets, W1, b1, W2, b2, E, ws, L, st);
+    if (e == cudaSuccess)
+        e = launch_expert_ffn(s, x, perm, offsets, W1, b1, W2, b2, E, ws, L, st, false, true);
     if (e == cudaSuccess)
         e = launch_transpose_experts(static_cast<const __nv_bfloat16 *>(W2), n, d, h, W2T, st);
     if (e == cudaSuccess)
@@ -1572,12 +1573,12 @@ moe_status moe_backward(const moe_shape *s, const void *x, const float *Wg, cons
         cudaMemsetAsync(dW2, 0, sizeof(float) * n * d * h, st);
         if (db1) cudaMemsetAsync(db1, 0, sizeof(float) * n * h, st);
         if (db2) cudaMemsetAsync(db2, 0, sizeof(float) * n * d, st);
-        return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+        return cuda_to_status(cudaGetLastError());
     }
     const auto run = backward_tc_supported(*s) ? launch_backward_tc : launch_backward;
     const cudaError_t e = run(*s, x, Wg, Wnoise, eps, W1, b1, W2, b2, idx, G, importance, dy,
                               w_importance, dx, dWg, dWnoise, dbg, dW1, db1, dW2, db2, ws, st);
-    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return cuda_to_status(e);
 }
 
 }  // extern "C"

@@ -540,11 +540,11 @@ moe_status moe_forward_balanced(const moe_shape *s, const void *x, const float *
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (s->T == 0) {
         cudaMemsetAsync(counts, 0, sizeof(int32_t) * s->n, st);
-        return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+        return cuda_to_status(cudaGetLastError());
     }
     const cudaError_t e = launch_forward_balanced(*s, x, Wg, Wn, bg, eps, thr, rows_cap, W1, b1, W2, b2,
                                                   y, counts, W, ws, st);
-    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return cuda_to_status(e);
 }
 
 }  // extern "C"

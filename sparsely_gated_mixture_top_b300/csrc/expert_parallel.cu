@@ -155,7 +155,7 @@ moe_status moe_ep_regroup(int32_t P, int32_t n_local, const int32_t *recv_counts
         static_cast<unsigned>(R > 0 ? (R + kEpRowsPerBlock - 1) / kEpRowsPerBlock : 1);
     ep_regroup<<<blocks, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
         P, n_local, recv_counts, R, offsets_local, perm_local, inv_local, err);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return cuda_to_status(cudaGetLastError());
 }
 
 moe_status moe_gather_rows(const void *src, int64_t src_rows, const int32_t *rows, int32_t div,
@@ -173,14 +173,14 @@ moe_status moe_gather_rows(const void *src, int64_t src_rows, const int32_t *row
                   static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4 *>(src), src_rows, rows, div, R, static_cast<int>(row_bytes / 16),
         static_cast<uint4 *>(dst), err);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return cuda_to_status(cudaGetLastError());
 }
 
 moe_status moe_importance_cv2(const float *importance, int32_t n, float *cv2, void *stream) {
     if (n <= 0 || !importance || !cv2 || !aligned16(importance) || !aligned16(cv2))
         return MOE_ERR_INVALID_ARG;
     imp_cv2<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(importance, n, cv2);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return cuda_to_status(cudaGetLastError());
 }
 
 }  // extern "C"

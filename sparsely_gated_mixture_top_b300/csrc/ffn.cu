@@ -6,8 +6,10 @@
 //   ffn_gather     x rows copied into expert order (bf16 path): xperm[r] = x[perm[r]/k]
 //   grouped_gemm_simt  fp32 path: the same grouped GEMM on CUDA cores (gathering
 //                  x through perm directly), fp32 throughout
-// The bf16 path runs the two layers on the tensor cores (ffn_tc.cu) with the
-// hidden activation rounded once to bf16 in between.
+// The bf16 path runs the two layers on the tensor cores with the hidden
+// activation rounded once to bf16 in between: in one kernel that keeps it on
+// chip (ffn_fused.cu) where the widths allow, else as two grouped GEMMs
+// (ffn_pair.cu, ffn_tc.cu) through the workspace.
 #include "moe_device.cuh"
 #include "moe_launch.h"
 
@@ -194,6 +196,12 @@ DispatchExtras dispatch_extras_for_ffn(const moe_shape &s, const void *x, void *
         const bool pair1 = pair_gemm_supported(s.h), pair2 = pair_gemm_supported(s.d);
         ex.x = static_cast<const __nv_bfloat16 *>(x);
         ex.xperm = ws_ptr<__nv_bfloat16>(ws, L.xperm);
+        if (fused_ffn_supported(s)) {
+            ex.ptiles = ws_ptr<int32_t>(ws, L.ptiles);
+            ex.plist = ws_ptr<int4>(ws, L.plist);
+            ex.pcap = 128;
+            return ex;
+        }
         if (pair1 || pair2) {
             ex.ptiles = ws_ptr<int32_t>(ws, L.ptiles);
             ex.plist = ws_ptr<int4>(ws, L.plist);
@@ -212,11 +220,28 @@ DispatchExtras dispatch_extras_for_ffn(const moe_shape &s, const void *x, void *
 cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *perm,
                               const int32_t *offsets, const void *W1, const float *b1,
                               const void *W2, const float *b2, void *Y_slot, void *ws,
-                              const WsLayout &L, cudaStream_t st, bool prepared) {
+                              const WsLayout &L, cudaStream_t st, bool prepared,
+                              bool keep_hidden) {
     const int64_t S = slots(s);
     if (S == 0) return cudaSuccess;
     int32_t *err = ws_ptr<int32_t>(ws, 0);
     int32_t *tiles = ws_ptr<int32_t>(ws, L.tiles);
+    if (s.dtype == MOE_BF16 && !keep_hidden && fused_ffn_supported(s)) {
+        // both layers in one kernel, the hidden activations on chip
+        int32_t *ptiles = ws_ptr<int32_t>(ws, L.ptiles);
+        int4 *plist = ws_ptr<int4>(ws, L.plist);
+        __nv_bfloat16 *xperm = ws_ptr<__nv_bfloat16>(ws, L.xperm);
+        if (!prepared) {
+            cudaError_t e = launch_pair_tiles(offsets, s.n, ptiles, plist, st, 128);
+            if (e != cudaSuccess) return e;
+            ffn_gather<<<static_cast<unsigned>((S + 8 * kGatherRows - 1) / (8 * kGatherRows)), 256,
+                         0, st>>>(static_cast<const __nv_bfloat16 *>(x), perm, offsets, s.n, S, s.d,
+                                  s.k, xperm, err);
+        }
+        return launch_ffn_fused(s, xperm, static_cast<const __nv_bfloat16 *>(W1), b1,
+                                static_cast<const __nv_bfloat16 *>(W2), b2, ptiles, plist,
+                                static_cast<__nv_bfloat16 *>(Y_slot), err, st);
+    }
     if (s.dtype == MOE_BF16) {
         // Each layer runs on a pair of SMs when its output width is a
         // multiple of 256 (ffn_pair.cu), else on the single-SM kernel.

@@ -96,18 +96,19 @@ __device__ __forceinline__ PairUnit unit_of(int4 t, int mt) {
     return u;
 }
 
-// One block of 1024 threads: tiles[e] = token tiles of the experts before e
-// (tiles[n] = all of them), and the table entry of every tile.
+// One block of 1024 threads: tiles[e] = token tiles (at most cap rows each)
+// of the experts before e (tiles[n] = all of them), and the table entry of
+// every tile.
 __global__ void __launch_bounds__(1024) ffn_pair_tiles(const int32_t *__restrict__ offsets, int n,
                                                        int32_t *__restrict__ tiles,
-                                                       int4 *__restrict__ tlist) {
+                                                       int4 *__restrict__ tlist, int cap) {
     __shared__ int32_t part[1024];
     const int per = (n + 1023) / 1024;
     const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
     int32_t sum = 0;
     for (int i = i0; i < i1; ++i) {
         int tn, nt;
-        token_tiling(offsets[i + 1] - offsets[i], tn, nt);
+        token_tiling(offsets[i + 1] - offsets[i], tn, nt, cap);
         sum += nt;
     }
     part[threadIdx.x] = sum;
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(1024) ffn_pair_tiles(const int32_t *__restrict
         tiles[i] = run;
         const int R = offsets[i + 1] - offsets[i];
         int tn, nt;
-        token_tiling(R, tn, nt);
+        token_tiling(R, tn, nt, cap);
         for (int j = 0; j < nt; ++j) {
             const int rows = min(tn, R - j * tn);
             tlist[run + j] = make_int4(i, offsets[i] + j * tn, rows, (rows + 31) & ~31);
@@ -429,8 +430,8 @@ static int pair_clusters() {
 bool pair_gemm_supported(int Nout) { return Nout % kPairM == 0; }
 
 cudaError_t launch_pair_tiles(const int32_t *offsets, int n, int32_t *tiles, int4 *tlist,
-                              cudaStream_t st) {
-    ffn_pair_tiles<<<1, 1024, 0, st>>>(offsets, n, tiles, tlist);
+                              cudaStream_t st, int cap) {
+    ffn_pair_tiles<<<1, 1024, 0, st>>>(offsets, n, tiles, tlist, cap);
     return cudaGetLastError();
 }
 

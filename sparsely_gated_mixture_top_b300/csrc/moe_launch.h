@@ -32,6 +32,10 @@ inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, si
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
 }
 
+// MOE_OK for cudaSuccess, else MOE_ERR_CUDA, remembering the CUDA error for
+// moe_last_cuda_error (per host thread).
+moe_status cuda_to_status(cudaError_t e);
+
 constexpr int kRouteChunk = 1024;  // slots ranked per block by the routing kernels
 constexpr int kTcRows = 128;       // rows per tensor-core FFN tile (MMA M)
 constexpr int kSimtRows = 64;      // rows per fp32 SIMT FFN tile
@@ -47,26 +51,27 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool gate_tc_supported(const moe_shape &s);
 size_t gate_tc_pack_bytes(const moe_shape &s);
 
-// Token tiling of the pair FFN for an expert with R rows: ceil(R / 256) tiles
-// of tn rows, tn = ceil(R / tiles) rounded up to 16 (at most 256); the tile
+// Token tiling of the pair FFN for an expert with R rows and tiles of at most
+// cap rows (256, or 128 for the fused two-layer kernel): ceil(R / cap) tiles
+// of tn rows, tn = ceil(R / tiles) rounded up to 16 (at most cap); the tile
 // count is then ceil(R / tn), so no tile is empty.
-__host__ __device__ inline void token_tiling(int R, int &tn, int &ntile) {
+__host__ __device__ inline void token_tiling(int R, int &tn, int &ntile, int cap = 256) {
     if (R <= 0) {
         tn = 0;
         ntile = 0;
         return;
     }
-    const int n0 = (R + 255) / 256;
+    const int n0 = (R + cap - 1) / cap;
     int t = (R + n0 - 1) / n0;
     t = (t + 15) & ~15;
-    if (t > 256) t = 256;
+    if (t > cap) t = cap;
     tn = t;
     ntile = (R + t - 1) / t;
 }
 
 // Entries of the pair FFN's token-tile table: an expert of R rows has at most
-// ceil(R / 256) tiles.
-inline size_t pair_tile_capacity(int64_t S, int n) { return static_cast<size_t>(S / 256 + n + 1); }
+// ceil(R / 128) tiles (tiles of at least 128 rows, or the expert's own rows).
+inline size_t pair_tile_capacity(int64_t S, int n) { return static_cast<size_t>(S / 128 + n + 1); }
 
 // Byte offsets of every region of a workspace (all 256-byte aligned).
 struct WsLayout {
@@ -156,6 +161,7 @@ struct DispatchExtras {
     int bm = 0;
     int32_t *ptiles = nullptr;          // pair token-tile starts and table (when set)
     int4 *plist = nullptr;
+    int pcap = 256;                     // rows per pair token tile at most (256 or 128)
 };
 
 cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float *G,
@@ -165,10 +171,14 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
 
 // prepared: the dispatch already built the stage's schedules and (bf16) the x
 // rows in expert order (dispatch_extras_for_ffn), so they are not rebuilt.
+// keep_hidden: the hidden activations must be left in the workspace's hidden
+// region (the backward pass reads them), so the two layers run as separate
+// GEMMs even where the fused kernel applies.
 cudaError_t launch_expert_ffn(const moe_shape &s, const void *x, const int32_t *perm,
                               const int32_t *offsets, const void *W1, const float *b1,
                               const void *W2, const float *b2, void *Y_slot, void *ws,
-                              const WsLayout &L, cudaStream_t st, bool prepared = false);
+                              const WsLayout &L, cudaStream_t st, bool prepared = false,
+                              bool keep_hidden = false);
 
 // The DispatchExtras that prepare the expert stage of shape s (ffn.cu).
 DispatchExtras dispatch_extras_for_ffn(const moe_shape &s, const void *x, void *ws,
@@ -215,11 +225,21 @@ int sm_count();
 // 32}, at most pair_tile_capacity(S, n) entries.
 bool pair_gemm_supported(int Nout);
 cudaError_t launch_pair_tiles(const int32_t *offsets, int n, int32_t *tiles, int4 *tlist,
-                              cudaStream_t st);
+                              cudaStream_t st, int cap = 256);
 cudaError_t launch_grouped_gemm_pair(const moe_shape &s, const __nv_bfloat16 *X, int K,
                                      const __nv_bfloat16 *W, int Nout, const float *bias, int relu,
                                      const int32_t *tiles, const int4 *tlist,
                                      __nv_bfloat16 *out, int32_t *err, cudaStream_t st);
+
+// Both layers of the expert networks in one kernel on SM pairs, the hidden
+// activations kept on chip (ffn_fused.cu): bf16, d = 256 or 512, h % 256 == 0,
+// at most 128 rows per expert on average (S <= 128 n).  Its token tiles hold
+// at most 128 rows (launch_pair_tiles with cap 128).
+bool fused_ffn_supported(const moe_shape &s);
+cudaError_t launch_ffn_fused(const moe_shape &s, const __nv_bfloat16 *X, const __nv_bfloat16 *W1,
+                             const float *b1, const __nv_bfloat16 *W2, const float *b2,
+                             const int32_t *tiles, const int4 *tlist, __nv_bfloat16 *Y,
+                             int32_t *err, cudaStream_t st);
 
 // Tensor map of a bf16 matrix [rows, K] (K contiguous, K % 64 == 0) seen as a
 // 3-D tensor {64, rows, K/64}: a box of box_rows rows and box_kblocks 64-wide

@@ -170,6 +170,7 @@ struct ScanOut {
     int bm;
     int32_t *ptiles;    // optional: pair token tiles per expert, and their table
     int4 *plist;
+    int pcap;           // rows per pair token tile at most
 };
 
 // The serial tail of the dispatch, run by one block of 1024 threads once every
@@ -189,7 +190,7 @@ __device__ void dispatch_finish(int n, const ScanOut &o) {
         if (o.rtiles) rt += (c + o.bm - 1) / o.bm;
         if (o.ptiles) {
             int tn, nt;
-            token_tiling(c, tn, nt);
+            token_tiling(c, tn, nt, o.pcap);
             pt += nt;
         }
     }
@@ -208,7 +209,7 @@ __device__ void dispatch_finish(int n, const ScanOut &o) {
         if (o.ptiles) {
             o.ptiles[i] = prun;
             int tn, nt;
-            token_tiling(c, tn, nt);
+            token_tiling(c, tn, nt, o.pcap);
             for (int j = 0; j < nt; ++j) {
                 const int rows = min(tn, c - j * tn);
                 o.plist[prun + j] = make_int4(i, run + j * tn, rows, (rows + 31) & ~31);
@@ -405,12 +406,13 @@ cudaError_t launch_dispatch(const moe_shape &s, const int32_t *idx, const float 
                                    local_rank, chunk, chunk_imp, err);
         if (e != cudaSuccess) return e;
     }
-    ScanOut o{counts, imp_acc, offsets, importance, cv2, nullptr, 0, nullptr, nullptr};
+    ScanOut o{counts, imp_acc, offsets, importance, cv2, nullptr, 0, nullptr, nullptr, 256};
     if (ex) {
         o.rtiles = ex->rtiles;
         o.bm = ex->bm;
         o.ptiles = ex->ptiles;
         o.plist = ex->plist;
+        o.pcap = ex->pcap;
     }
     int32_t *done = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kWsDoneCounterOffset);
     cudaError_t e = launch_pdl(route_scan, dim3((n + 31) / 32), dim3(32, 32), 0, st, chunk,

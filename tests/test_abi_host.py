@@ -32,6 +32,8 @@ def test_every_declared_symbol_is_exported():
 
 def test_version_and_status_strings():
     assert B.lib.moe_version() >= 100
+    assert B.lib.moe_last_cuda_error() == 0              # no CUDA call has failed
+    assert B.lib.moe_cuda_error_name(1).decode() == "cudaErrorInvalidValue"
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert B.status_string(code) and B.status_string(code) != "unknown status"
     assert B.status_string(42) == "unknown status"

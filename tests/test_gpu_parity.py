@@ -47,6 +47,14 @@ SMALL = [
     W("many_blocks_ragged", T=3000, d=256, h=512, n=24, k=4, bias_std=0.2, seed=29),
     W("zipf_empty_experts", T=2500, d=256, h=256, n=200, k=4, gate_bias="zipf", seed=30),
     W("full_widths_16_experts", T=2400, d=512, h=1024, n=16, k=4, bias_std=0.1, seed=31),
+    # Both expert layers in one kernel (at most 128 rows per expert on
+    # average): one hidden chunk and two output blocks; an odd number of
+    # hidden chunks with experts of a few rows (tiles of 32 columns, 16 token
+    # rows per SM of the pair); the full widths with experts of one to three
+    # token tiles.
+    W("fused_one_chunk", T=600, d=512, h=256, n=12, k=2, bias_std=0.1, seed=32),
+    W("fused_short_tiles_odd_chunks", T=40, d=256, h=768, n=24, k=3, bias_std=0.1, seed=33),
+    W("fused_full_widths", T=2000, d=512, h=1024, n=64, k=4, bias_std=0.1, seed=34),
 ]
 
 
