@@ -151,6 +151,50 @@ def test_one_expert_takes_every_token():
     check_against_oracle(w, out, ref)
 
 
+def test_one_expert_takes_every_token_fused_ffn():
+    """Both expert layers in one kernel (experts average at most 128 rows)
+    while one expert holds all 1000 rows: eight token tiles of one expert."""
+    w = W("hot_expert_fused", T=1000, d=256, h=512, n=8, k=1, bias_std=0.1, seed=36)
+    bg = torch.tensor([50.0] + [0.0] * 7)
+    inp = prepared_inputs(w, bg=bg)
+    ref = oracle_full(w, inp)
+    assert ref["counts"][0] == w.T
+    out, _ = run_forward(w, to_dev(inp))
+    check_against_oracle(w, out, ref)
+
+
+@pytest.mark.parametrize("counts", [
+    [128, 129, 0, 256, 1, 31, 32, 33],        # tiles: 128 | 80 + 49 | 2 x 128 | 1 row (N = 32)
+    [0, 0, 0, 610, 0, 0, 0, 0],               # one expert: 4 x 128 + 98 rows
+    [17, 15, 16, 14, 18, 13, 19, 498],        # tiles of 32 columns beside 3 x 128 + 114
+], ids=["tile_edges", "one_expert", "small_tiles"])
+def test_expert_stage_tile_edges_fused_ffn(counts):
+    """moe_expert_ffn (the fused two-layer kernel at these widths) on chosen
+    expert row counts and a shuffled slot order, against the oracle's
+    experts applied to the same rows."""
+    w = W("tile_edges", T=610, d=256, h=768, n=8, k=1, bias_std=0.1, seed=37)
+    assert sum(counts) == w.T * w.k
+    inp = wl.make_inputs(w)
+    s = B.shape_of(w)
+    ws = B.workspace(s)
+    dinp = to_dev(inp)
+    rng = np.random.default_rng(37)
+    perm = rng.permutation(w.T * w.k).astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    experts = np.repeat(np.arange(w.n), counts)
+    Y = torch.empty((w.T * w.k, w.d), dtype=torch.bfloat16, device="cuda")
+    B.moe_expert_ffn(s, dinp["x"], torch.from_numpy(perm).cuda(), torch.from_numpy(offsets).cuda(),
+                     dinp["W1"], dinp["b1"], dinp["W2"], dinp["b2"], Y, ws)
+    assert B.moe_check(ws) == B.MOE_OK
+    Yref = oracle.expert_rows(oracle._f64(inp["x"])[perm // w.k], experts, inp["W1"], inp["b1"],
+                              inp["W2"], inp["b2"])
+    assert rel_fro(Y.cpu().double().numpy(), Yref) <= TOL_Y["bf16"]
+    # every row individually (a row written to the wrong place fails here)
+    err = np.abs(Y.cpu().double().numpy() - Yref).max(axis=1)
+    scale = np.abs(Yref).max(axis=1) + 1e-3
+    assert (err / scale).max() < 5e-2
+
+
 def test_noise_off():
     w = W("clean_gate", T=500, d=128, h=192, n=16, k=2, noisy=False, seed=33)
     inp = wl.make_inputs(w)
