@@ -492,12 +492,12 @@ def counted_launches(B, call, expected: int) -> dict:
 def backward_launches(w: wl.Workload) -> int:
     """Kernels one moe_backward call launches (bf16 tensor-core path, output
     widths d and h multiples of 256): dispatch (3), recompute of the expert
-    stage (tile table, x-row gather, two GEMMs: 4), weight transposes (2), dE
-    rows, two row GEMMs and the ReLU mask, k-block table, four padded
-    transposes, two weight-gradient GEMMs, Wg^T (and Wn^T), importance
+    stage (tile table, x-row gather, two GEMMs: 4), dE
+    rows, two row GEMMs (the weights read in their stored layout) and the
+    ReLU mask, k-block table, four padded transposes, two weight-gradient GEMMs, Wg^T (and Wn^T), importance
     gradient, token kernel, chunk table and the chunked row sums (gate, db2,
     db1: 6)."""
-    flat = 3 + 4 + 2 + 1 + 3 + 1 + 4 + 2 + (2 if w.noisy else 1) + 1 + 1 + 1 + 6
+    flat = 3 + 4 + 1 + 3 + 1 + 4 + 2 + (2 if w.noisy else 1) + 1 + 1 + 1 + 6
     # hierarchical: the pairs (token, kept group) built and routed by group
     # (1 + 3), and their chunk table and two-pass sums for the group columns (3)
     return flat + (7 if w.groups else 0)

@@ -1277,7 +1277,8 @@ cudaError_t row_gemm(const RowGemm &g, int64_t S, int n, cudaStream_t st) {
 // The forward's workspace comes first (routing, x rows in expert order,
 // hidden activations a = ReLU(z) and expert outputs E, all bf16, from a
 // recompute of the expert stage); then:
-//   W1T, W2T  the experts' weights transposed ([n, d, h] and [n, h, d])
+//   W1T, W2T  the experts' weights transposed ([n, d, h] and [n, h, d]), for
+//             the single-SM GEMM (output widths not multiples of 256)
 //   dE        [S, d] rows G dy in expert order;  dA -> dZ [S, h];  dXs [S, d]
 //   kblk      64-row blocks per expert (tile table), the k-blocks of the
 //             weight-gradient contractions
@@ -1371,27 +1372,29 @@ cudaError_t launch_backward_tc(const moe_shape &s, const void *x, const float *W
     // recompute x rows, a = ReLU(x W1^T + b1) and E = a W2^T + b2 (bf16, expert order)
     if (e == cudaSuccess)
         e = launch_expert_ffn(s, x, perm, offsets, W1, b1, W2, b2, E, ws, L, st, false, true);
-    if (e == cudaSuccess)
+    // dA = dE W2 (K = d), then dZ = dA * [a > 0];  dXs = dZ W1 (K = h).
+    // An output width that suits the SM-pair GEMM reads the weights in their
+    // stored layout (an MN-major operand); otherwise the single-SM GEMM reads
+    // a transposed copy (W2^T, W1^T rows).  Output widths h and d are the
+    // recompute's, so the tile tables it built from the same offsets serve
+    // here unchanged.
+    if (e == cudaSuccess && !pair_gemm_supported(h))
         e = launch_transpose_experts(static_cast<const __nv_bfloat16 *>(W2), n, d, h, W2T, st);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !pair_gemm_supported(d))
         e = launch_transpose_experts(static_cast<const __nv_bfloat16 *>(W1), n, h, d, W1T, st);
     if (e == cudaSuccess)
         e = launch_rows_scaled(static_cast<const __nv_bfloat16 *>(dy), G, perm, S, d, k, dE, err, st);
-    // dA = dE W2 (B = W2^T rows, K = d), then dZ = dA * [a > 0];  dXs = dZ W1 (B = W1^T rows, K = h)
-    // Each GEMM runs on an SM pair when its output width allows.  Output
-    // widths h and d are the recompute's, so the tile tables it built from
-    // the same offsets serve here unchanged.
-    auto row_gemm = [&](const __nv_bfloat16 *X, int K, const __nv_bfloat16 *Wt, int Nout,
-                        __nv_bfloat16 *out) {
+    auto row_gemm = [&](const __nv_bfloat16 *X, int K, const void *W, const __nv_bfloat16 *Wt,
+                        int Nout, __nv_bfloat16 *out) {
         return pair_gemm_supported(Nout)
-                   ? launch_grouped_gemm_pair(s, X, K, Wt, Nout, nullptr, 0, ptiles, plist, out,
-                                              err, st)
+                   ? launch_grouped_gemm_pair_wmn(s, X, K, static_cast<const __nv_bfloat16 *>(W),
+                                                  Nout, ptiles, plist, out, err, st)
                    : launch_grouped_gemm_tc(s, X, K, Wt, Nout, nullptr, 0, offsets, tiles, out,
                                             err, st);
     };
-    if (e == cudaSuccess) e = row_gemm(dE, d, W2T, h, dZ);
+    if (e == cudaSuccess) e = row_gemm(dE, d, W2, W2T, h, dZ);
     if (e == cudaSuccess) e = launch_relu_mask(dZ, hid, S * static_cast<int64_t>(h), st);
-    if (e == cudaSuccess) e = row_gemm(dZ, h, W1T, d, dXs);
+    if (e == cudaSuccess) e = row_gemm(dZ, h, W1, W1T, d, dXs);
     // weight gradients: rows as the contraction axis, transposed and padded per expert
     if (e == cudaSuccess) e = launch_row_tiles(offsets, n, 64, kblk, st);
     if (e == cudaSuccess) e = launch_transpose_pad(dE, d, offsets, kblk, n, S, B.Kcap, bf(B.PdE), st);

@@ -146,6 +146,9 @@ __device__ __forceinline__ bool pair_drain(uint32_t bar, uint32_t parity, int32_
     return true;
 }
 
+// kAMn: the weights are read in their stored layout [n*K, Nout] (rows k of
+// expert e at e*K + k) as an MN-major operand, instead of [n*Nout, K].
+template <bool kAMn>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     ffn_pair_gemm(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ XMaps mapX,
                   const int32_t *__restrict__ tiles, const int4 *__restrict__ tlist, int n,
@@ -232,7 +235,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     const int hrows = u.N >> 1;
                     if (rank == 0)
                         mbar_arrive_expect_tx(full(stage), 2 * (Cfg::kABytes + hrows * 128 * kPairKB));
-                    tma_load_3d_pair(smem_u32(sA + stage * Cfg::kABytes), &mapW, fb, 0, wrow, kb);
+                    if constexpr (kAMn) {
+                        // K rows kb*64 .. +128 of expert e, this CTA's two 64-wide
+                        // blocks of output features
+                        tma_load_3d_pair(smem_u32(sA + stage * Cfg::kABytes), &mapW, fb, 0,
+                                         u.e * K + kb * 64,
+                                         (u.mt * kPairM + static_cast<int>(rank) * 128) / 64);
+                    } else {
+                        tma_load_3d_pair(smem_u32(sA + stage * Cfg::kABytes), &mapW, fb, 0, wrow, kb);
+                    }
                     tma_load_3d_pair(smem_u32(sB + stage * Cfg::kBBytes), &mapX.m[(hrows >> 4) - 1], fb,
                                      0, xrow, kb);
                     if (++stage == STAGES) {
@@ -260,7 +271,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             for (int q = cl; q < total && ok; q += ncl) {
                 const PairUnit u = unit_of(tcur, q % nmt);
                 if (q + ncl < total) tcur = __ldg(tlist + (q + ncl) / nmt);
-                const uint32_t idesc = idesc_bf16_f32(kPairM, u.N);
+                const uint32_t idesc =
+                    kAMn ? idesc_bf16_f32_amn(kPairM, u.N) : idesc_bf16_f32(kPairM, u.N);
                 if (!mbar_wait_bounded(tempty(acc), acc_phase ^ 1u, abort_flag, err, kSiteTcMma))
                     break;
                 tc_fence_after();
@@ -280,7 +292,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc_mma_f16_pair(d_tmem,
-                                            sdesc_kmajor_sw128(a0 + j * Cfg::kKBlockBytes + kk * 32),
+                                            kAMn ? sdesc_mnmajor_sw128(a0 + j * 64 * 128 + kk * 16 * 128,
+                                                                       128 * 128)
+                                                 : sdesc_kmajor_sw128(a0 + j * Cfg::kKBlockBytes + kk * 32),
                                             sdesc_kmajor_sw128(b0 + j * bkb + kk * 32),
                                             idesc, (kb | j | kk) != 0 ? 1u : 0u);
                     }
@@ -419,7 +433,7 @@ static int pair_clusters() {
     cfg.blockDim = dim3(kPairThreads, 1, 1);
     cfg.dynamicSmemBytes = PairCfg::kSmem;
     int num = 0;
-    if (cudaOccupancyMaxActiveClusters(&num, ffn_pair_gemm, &cfg) != cudaSuccess || num <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&num, ffn_pair_gemm<false>, &cfg) != cudaSuccess || num <= 0) {
         cudaGetLastError();
         num = sm_count() / 2;
     }
@@ -435,24 +449,16 @@ cudaError_t launch_pair_tiles(const int32_t *offsets, int n, int32_t *tiles, int
     return cudaGetLastError();
 }
 
-cudaError_t launch_grouped_gemm_pair(const moe_shape &s, const __nv_bfloat16 *X, int K,
-                                     const __nv_bfloat16 *W, int Nout, const float *bias, int relu,
-                                     const int32_t *tiles, const int4 *tlist,
-                                     __nv_bfloat16 *out, int32_t *err, cudaStream_t st) {
+template <bool kAMn>
+static cudaError_t launch_pair(const moe_shape &s, const CUtensorMap &mW, const XMaps &mX,
+                               const int32_t *tiles, const int4 *tlist, int K, int Nout,
+                               const __nv_bfloat16 *W, const __nv_bfloat16 *X, const float *bias,
+                               int relu, __nv_bfloat16 *out, int32_t *err, cudaStream_t st) {
     const int64_t S = slots(s);
-    CUtensorMap mW;
-    XMaps mX;
-    if (!make_kmajor_map(&mW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(s.n) * Nout, 128,
-                         kPairKB))
-        return cudaErrorInvalidValue;
-    for (int i = 0; i < 8; ++i)
-        if (!make_kmajor_map(&mX.m[i], X, static_cast<uint64_t>(K), static_cast<uint64_t>(S),
-                             static_cast<uint32_t>(16 * (i + 1)), kPairKB))
-            return cudaErrorInvalidValue;
     // The opt-in above 48 KB belongs to the current device's context: set it
     // before every launch (a cheap host call).
-    cudaError_t e = cudaFuncSetAttribute(ffn_pair_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PairCfg::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(ffn_pair_gemm<kAMn>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmem);
     if (e != cudaSuccess) return e;
     // Upper bound of the unit count: every expert may add one partial tile.
     const int64_t max_units = ((S + kPairTok - 1) / kPairTok + s.n) * (Nout / kPairM);
@@ -460,9 +466,47 @@ cudaError_t launch_grouped_gemm_pair(const moe_shape &s, const __nv_bfloat16 *X,
     if (pairs > max_units) pairs = max_units;
     if (pairs < 1) pairs = 1;
     const int out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
-    return launch_pdl(ffn_pair_gemm, dim3(static_cast<unsigned>(2 * pairs)), dim3(kPairThreads),
+    return launch_pdl(ffn_pair_gemm<kAMn>, dim3(static_cast<unsigned>(2 * pairs)), dim3(kPairThreads),
                       PairCfg::kSmem, st, mW, mX, tiles, tlist, s.n, K, Nout, W, X, bias, relu, out,
                       out_v8, err);
+}
+
+static bool make_token_maps(XMaps &mX, const moe_shape &s, const __nv_bfloat16 *X, int K) {
+    const int64_t S = slots(s);
+    for (int i = 0; i < 8; ++i)
+        if (!make_kmajor_map(&mX.m[i], X, static_cast<uint64_t>(K), static_cast<uint64_t>(S),
+                             static_cast<uint32_t>(16 * (i + 1)), kPairKB))
+            return false;
+    return true;
+}
+
+cudaError_t launch_grouped_gemm_pair(const moe_shape &s, const __nv_bfloat16 *X, int K,
+                                     const __nv_bfloat16 *W, int Nout, const float *bias, int relu,
+                                     const int32_t *tiles, const int4 *tlist,
+                                     __nv_bfloat16 *out, int32_t *err, cudaStream_t st) {
+    CUtensorMap mW;
+    XMaps mX;
+    if (!make_kmajor_map(&mW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(s.n) * Nout, 128,
+                         kPairKB) ||
+        !make_token_maps(mX, s, X, K))
+        return cudaErrorInvalidValue;
+    return launch_pair<false>(s, mW, mX, tiles, tlist, K, Nout, W, X, bias, relu, out, err, st);
+}
+
+cudaError_t launch_grouped_gemm_pair_wmn(const moe_shape &s, const __nv_bfloat16 *X, int K,
+                                         const __nv_bfloat16 *W, int Nout, const int32_t *tiles,
+                                         const int4 *tlist, __nv_bfloat16 *out, int32_t *err,
+                                         cudaStream_t st) {
+    if (!pair_gemm_supported(Nout) || K % 64 != 0) return cudaErrorInvalidValue;
+    CUtensorMap mW;
+    XMaps mX;
+    // box: 128 K rows (two k-blocks) x this CTA's 128 output features (two
+    // 64-wide blocks)
+    if (!make_mnmajor_map(&mW, W, static_cast<uint64_t>(Nout), static_cast<uint64_t>(s.n) * K,
+                          64 * kPairKB, 2) ||
+        !make_token_maps(mX, s, X, K))
+        return cudaErrorInvalidValue;
+    return launch_pair<true>(s, mW, mX, tiles, tlist, K, Nout, W, X, nullptr, 0, out, err, st);
 }
 
 }  // namespace moe

@@ -367,6 +367,19 @@ bool make_kmajor_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_mnmajor_map(CUtensorMap *m, const void *base, uint64_t M, uint64_t rows,
+                      uint32_t box_rows, uint32_t box_mblocks) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {64, rows, M / 64};
+    cuuint64_t strides[2] = {M * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, box_mblocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int tc_block_n(int N) {
     if (N % 256 == 0) return 256;
     if (N % 128 == 0) return 128;

@@ -249,6 +249,21 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major bf16 tile stored the way a
+// TMA copy with 128-byte swizzle writes a box {64 MN, rows of K, MN blocks}:
+// 64 MN elements (128 bytes) per K row, 8-row swizzle atoms of 1024 bytes
+// (stride dimension: 8 K rows), and the next 64 MN elements `mn_block_bytes`
+// further on (leading dimension).  `saddr` lies on an 8-row boundary.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);          // bits 0-13: start address >> 4
+    d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;   // bits 16-29: MN-block stride
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;                   // bits 32-45: 8-row (K) stride
+    d |= static_cast<uint64_t>(1) << 46;                           // bits 46-48: version 1
+    d |= static_cast<uint64_t>(2) << 61;                           // bits 61-63: 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D,
 // M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
@@ -257,6 +272,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | (1u << 10)                                // B format: bf16
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// The same with A MN-major (bit 15: A transposed).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_amn(int M, int N) {
+    return idesc_bf16_f32(M, N) | (1u << 15);
 }
 
 // ---------------------------------------------------------------------------

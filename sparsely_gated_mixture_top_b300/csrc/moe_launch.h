@@ -248,4 +248,19 @@ cudaError_t launch_ffn_fused(const moe_shape &s, const __nv_bfloat16 *X, const _
 bool make_kmajor_map(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows,
                      uint32_t box_rows, uint32_t box_kblocks = 1);
 
+// Tensor map of a bf16 matrix [rows, M] (M contiguous, M % 64 == 0) read as
+// MN-major operand tiles: a 3-D tensor {64, rows, M/64}; a box of box_rows
+// rows and box_mblocks 64-wide column blocks lands as that many
+// 128-byte-swizzled [box_rows][64] tiles back to back.
+bool make_mnmajor_map(CUtensorMap *m, const void *base, uint64_t M, uint64_t rows,
+                      uint32_t box_rows, uint32_t box_mblocks);
+
+// The pair GEMM out[r, c] = X[r, :] . W[e*K + k, c] summed over k < K: the
+// weights read in their stored layout [n*K, Nout] (MN-major operand) instead
+// of transposed, e.g. dA = dE . W2 with W2 [n*d, h].  Nout % 256 == 0.
+cudaError_t launch_grouped_gemm_pair_wmn(const moe_shape &s, const __nv_bfloat16 *X, int K,
+                                         const __nv_bfloat16 *W, int Nout, const int32_t *tiles,
+                                         const int4 *tlist, __nv_bfloat16 *out, int32_t *err,
+                                         cudaStream_t st);
+
 }  // namespace moe
