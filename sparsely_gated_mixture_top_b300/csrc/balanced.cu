@@ -396,45 +396,97 @@ __global__ void __launch_bounds__(256) bal_weights(const float *__restrict__ H,
     }
 }
 
+// 16-byte pieces of bf16 or fp32 rows as fp32.
+__device__ __forceinline__ void piece_to_f(const uint4 &u, float (&v)[8]) {
+    const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void piece_to_f(const uint4 &u, float (&v)[4]) {
+    v[0] = __uint_as_float(u.x);
+    v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z);
+    v[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ uint4 piece_from_f(const float (&v)[8]) {
+    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+}
+__device__ __forceinline__ uint4 piece_from_f(const float (&v)[4]) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                      __float_as_uint(v[3]));
+}
+
 // One warp per token: y_t = sum over its kept experts, in increasing e, of
-// w Y[row]; fp32 accumulation, one rounding to the output type.
+// w Y[row]; fp32 accumulation, one rounding to the output type.  Each lane
+// owns two 16-byte pieces of every 64-piece span of the row; the kept
+// experts are found 32 at a time by a ballot over the row map, and the rows
+// of up to four of them are requested before any is summed.
 template <typename TY>
 __global__ void __launch_bounds__(256) bal_combine(const TY *__restrict__ Y,
                                                    const int32_t *__restrict__ rowmap,
                                                    const float *__restrict__ row_weight, int64_t T,
                                                    int n, int d, TY *__restrict__ y) {
+    constexpr int V = 16 / static_cast<int>(sizeof(TY));   // elements per 16-byte piece
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
     if (t >= T) return;
     const int32_t *rm = rowmap + t * n;
-    for (int c0 = 0; c0 < d; c0 += 32 * 8) {
-        float acc[8] = {};
+    const int pieces = d / V;
+    for (int p0 = lane; p0 - lane < pieces; p0 += 64) {
+        const int p1 = p0 + 32;
+        const bool has0 = p0 < pieces, has1 = p1 < pieces;
+        float acc0[V], acc1[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc0[i] = acc1[i] = 0.0f;
         for (int eb = 0; eb < n; eb += 32) {
             const int e = eb + lane;
-            const int32_t myrow = e < n ? rm[e] : -1;
+            const int32_t myrow = e < n ? __ldg(rm + e) : -1;
+            const float myw = myrow >= 0 ? __ldg(row_weight + myrow) : 0.0f;
             unsigned bits = __ballot_sync(0xffffffffu, myrow >= 0);
-            while (bits) {
-                const int src = __ffs(bits) - 1;
-                bits &= bits - 1;
-                const int32_t r = __shfl_sync(0xffffffffu, myrow, src);
-                const float w = row_weight[r];
+            while (bits) {   // warp-uniform
+                int32_t r[4];
+                float w[4];
+                uint4 u[4][2];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int c = c0 + lane * 8 + i;
-                    if (c < d) acc[i] = fmaf(w, to_f(Y[static_cast<int64_t>(r) * d + c]), acc[i]);
+                for (int q = 0; q < 4; ++q) {
+                    r[q] = -1;
+                    w[q] = 0.0f;
+                    if (bits) {
+                        const int src = __ffs(bits) - 1;
+                        bits &= bits - 1;
+                        r[q] = __shfl_sync(0xffffffffu, myrow, src);
+                        w[q] = __shfl_sync(0xffffffffu, myw, src);
+                    }
+                    u[q][0] = u[q][1] = make_uint4(0, 0, 0, 0);
+                    if (r[q] >= 0) {
+                        const uint4 *src4 =
+                            reinterpret_cast<const uint4 *>(Y + static_cast<int64_t>(r[q]) * d);
+                        if (has0) u[q][0] = __ldg(src4 + p0);
+                        if (has1) u[q][1] = __ldg(src4 + p1);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (r[q] < 0) continue;
+                    float a[V], b[V];
+                    piece_to_f(u[q][0], a);
+                    piece_to_f(u[q][1], b);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) {
+                        acc0[i] = fmaf(w[q], a[i], acc0[i]);
+                        acc1[i] = fmaf(w[q], b[i], acc1[i]);
+                    }
                 }
             }
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int c = c0 + lane * 8 + i;
-            if (c < d) {
-                if constexpr (sizeof(TY) == 2)
-                    y[t * d + c] = __float2bfloat16_rn(acc[i]);
-                else
-                    y[t * d + c] = acc[i];
-            }
-        }
+        uint4 *dst = reinterpret_cast<uint4 *>(y + t * d);
+        if (has0) dst[p0] = piece_from_f(acc0);
+        if (has1) dst[p1] = piece_from_f(acc1);
     }
 }
 
