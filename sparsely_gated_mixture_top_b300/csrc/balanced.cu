@@ -421,11 +421,43 @@ __device__ __forceinline__ uint4 piece_from_f(const float (&v)[4]) {
                       __float_as_uint(v[3]));
 }
 
+// Sums up to four queued experts' pieces into acc0/acc1 in queue order: all
+// rows are requested before any is summed.
+template <typename TY, int V>
+__device__ __forceinline__ void bal_flush(const TY *__restrict__ Y, int d, int p0, int p1, bool has0,
+                                          bool has1, const int32_t (&r)[4], const float (&w)[4],
+                                          int cnt, float (&acc0)[V], float (&acc1)[V]) {
+    uint4 u[4][2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        u[q][0] = u[q][1] = make_uint4(0, 0, 0, 0);
+        if (q < cnt) {
+            const uint4 *src4 = reinterpret_cast<const uint4 *>(Y + static_cast<int64_t>(r[q]) * d);
+            if (has0) u[q][0] = __ldg(src4 + p0);
+            if (has1) u[q][1] = __ldg(src4 + p1);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (q >= cnt) continue;
+        float a[V], b[V];
+        piece_to_f(u[q][0], a);
+        piece_to_f(u[q][1], b);
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            acc0[i] = fmaf(w[q], a[i], acc0[i]);
+            acc1[i] = fmaf(w[q], b[i], acc1[i]);
+        }
+    }
+}
+
 // One warp per token: y_t = sum over its kept experts, in increasing e, of
 // w Y[row]; fp32 accumulation, one rounding to the output type.  Each lane
-// owns two 16-byte pieces of every 64-piece span of the row; the kept
-// experts are found 32 at a time by a ballot over the row map, and the rows
-// of up to four of them are requested before any is summed.
+// owns two 16-byte pieces of every 64-piece span of the row.  The row map
+// of 256 experts (and the kept ones' weights) is read at once; the kept
+// experts are then found 32 at a time by a ballot and queued (warp-uniform
+// registers), and every four queued experts' rows are requested together
+// before they are summed in order.
 template <typename TY>
 __global__ void __launch_bounds__(256) bal_combine(const TY *__restrict__ Y,
                                                    const int32_t *__restrict__ rowmap,
@@ -443,47 +475,43 @@ __global__ void __launch_bounds__(256) bal_combine(const TY *__restrict__ Y,
         float acc0[V], acc1[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) acc0[i] = acc1[i] = 0.0f;
-        for (int eb = 0; eb < n; eb += 32) {
-            const int e = eb + lane;
-            const int32_t myrow = e < n ? __ldg(rm + e) : -1;
-            const float myw = myrow >= 0 ? __ldg(row_weight + myrow) : 0.0f;
-            unsigned bits = __ballot_sync(0xffffffffu, myrow >= 0);
-            while (bits) {   // warp-uniform
-                int32_t r[4];
-                float w[4];
-                uint4 u[4][2];
+        int32_t qr[4] = {-1, -1, -1, -1};
+        float qw[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        int qn = 0;
+        for (int eb0 = 0; eb0 < n; eb0 += 256) {
+            // 256 experts' row-map entries, then the kept ones' weights, all
+            // requested before the first ballot
+            int32_t mr[8];
+            float mw[8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    r[q] = -1;
-                    w[q] = 0.0f;
-                    if (bits) {
-                        const int src = __ffs(bits) - 1;
-                        bits &= bits - 1;
-                        r[q] = __shfl_sync(0xffffffffu, myrow, src);
-                        w[q] = __shfl_sync(0xffffffffu, myw, src);
-                    }
-                    u[q][0] = u[q][1] = make_uint4(0, 0, 0, 0);
-                    if (r[q] >= 0) {
-                        const uint4 *src4 =
-                            reinterpret_cast<const uint4 *>(Y + static_cast<int64_t>(r[q]) * d);
-                        if (has0) u[q][0] = __ldg(src4 + p0);
-                        if (has1) u[q][1] = __ldg(src4 + p1);
-                    }
-                }
+            for (int i = 0; i < 8; ++i) {
+                const int e = eb0 + 32 * i + lane;
+                mr[i] = e < n ? __ldg(rm + e) : -1;
+            }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (r[q] < 0) continue;
-                    float a[V], b[V];
-                    piece_to_f(u[q][0], a);
-                    piece_to_f(u[q][1], b);
+            for (int i = 0; i < 8; ++i) mw[i] = mr[i] >= 0 ? __ldg(row_weight + mr[i]) : 0.0f;
 #pragma unroll
-                    for (int i = 0; i < V; ++i) {
-                        acc0[i] = fmaf(w[q], a[i], acc0[i]);
-                        acc1[i] = fmaf(w[q], b[i], acc1[i]);
+            for (int i = 0; i < 8; ++i) {
+                unsigned bits = __ballot_sync(0xffffffffu, mr[i] >= 0);
+                while (bits) {   // warp-uniform
+                    const int src = __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    const int32_t rr = __shfl_sync(0xffffffffu, mr[i], src);
+                    const float ww = __shfl_sync(0xffffffffu, mw[i], src);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q == qn) {
+                            qr[q] = rr;
+                            qw[q] = ww;
+                        }
+                    if (++qn == 4) {
+                        bal_flush<TY, V>(Y, d, p0, p1, has0, has1, qr, qw, 4, acc0, acc1);
+                        qn = 0;
                     }
                 }
             }
         }
+        if (qn) bal_flush<TY, V>(Y, d, p0, p1, has0, has1, qr, qw, qn, acc0, acc1);
         uint4 *dst = reinterpret_cast<uint4 *>(y + t * d);
         if (has0) dst[p0] = piece_from_f(acc0);
         if (has1) dst[p1] = piece_from_f(acc1);
