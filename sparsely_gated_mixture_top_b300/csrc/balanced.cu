@@ -188,6 +188,10 @@ __global__ void bal_transpose(const float *__restrict__ H, int64_t T, int n, flo
     }
 }
 
+// Scores a thread keeps in registers across the passes of the per-expert
+// select (up to 16384 tokens; longer columns are read again from memory).
+constexpr int kBalKeys = 16;
+
 // Order-preserving key of a float: larger float, larger key.
 __device__ __forceinline__ uint32_t fkey(float f) {
     const uint32_t u = __float_as_uint(f);
@@ -234,25 +238,70 @@ __global__ void __launch_bounds__(1024) bal_count(const float *__restrict__ HT, 
         }
         return;
     }
+    // Up to kBalKeys scores per thread stay in registers across the passes.
+    const float *col = HT + static_cast<int64_t>(e) * T;
+    const bool cached = T <= static_cast<int64_t>(kBalKeys) * 1024;
+    uint32_t keys[kBalKeys];
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kBalKeys; ++i) {
+            const int64_t t = tid + static_cast<int64_t>(i) * 1024;
+            keys[i] = t < T ? fkey(__ldg(col + t)) : 0u;
+        }
+    }
     uint32_t prefix = 0, pmask = 0;
     int64_t remaining = m;
     for (int p = 3; p >= 0; --p) {
         for (int i = tid; i < 256; i += 1024) hist[i] = 0;
         __syncthreads();
-        for (int64_t t = tid; t < T; t += 1024) {
-            const uint32_t key = fkey(HT[static_cast<int64_t>(e) * T + t]);
-            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> (8 * p)) & 255u], 1u);
+        if (cached) {
+#pragma unroll
+            for (int i = 0; i < kBalKeys; ++i) {
+                const int64_t t = tid + static_cast<int64_t>(i) * 1024;
+                if (t < T && (keys[i] & pmask) == prefix)
+                    atomicAdd(&hist[(keys[i] >> (8 * p)) & 255u], 1u);
+            }
+        } else {
+            for (int64_t t = tid; t < T; t += 1024) {
+                const uint32_t key = fkey(col[t]);
+                if ((key & pmask) == prefix) atomicAdd(&hist[(key >> (8 * p)) & 255u], 1u);
+            }
         }
         __syncthreads();
-        if (tid == 0) {
-            int64_t cum = 0;
-            int dg = 255;
-            for (; dg > 0; --dg) {
-                if (cum + hist[dg] >= remaining) break;
-                cum += hist[dg];
+        if (tid < 32) {
+            // The digit: going down from 255, the first whose count brings
+            // the candidates at or above it to `remaining` (digit 0 if none
+            // before it); sel_above = the candidates above it.  Lane l holds
+            // digits 255 - 8l .. 248 - 8l.
+            const int lane = tid;
+            uint32_t hv[8];
+            uint32_t sl = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                hv[j] = hist[255 - 8 * lane - j];
+                sl += hv[j];
             }
-            sel_digit = static_cast<uint32_t>(dg);
-            sel_above = cum;
+            uint32_t inc = sl;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += u;
+            }
+            const unsigned cross = __ballot_sync(0xffffffffu, static_cast<int64_t>(inc) >= remaining);
+            const int L = cross ? __ffs(cross) - 1 : 31;
+            if (lane == L) {
+                int64_t cum = static_cast<int64_t>(inc - sl);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int dg = 255 - 8 * lane - j;
+                    if (dg == 0 || cum + hv[j] >= remaining) {
+                        sel_digit = static_cast<uint32_t>(dg);
+                        sel_above = cum;
+                        break;
+                    }
+                    cum += hv[j];
+                }
+            }
         }
         __syncthreads();
         remaining -= sel_above;
