@@ -390,6 +390,46 @@ __global__ void __launch_bounds__(1024) bal_write(const float *__restrict__ HT, 
     const int32_t qt = quota[e];
     const float th = thr ? thr[e] : 0.0f;
     const float *col = HT + static_cast<int64_t>(e) * T;
+    const int32_t r0 = offsets[e], r1 = offsets[e + 1];
+    if (per <= kBalKeys) {
+        // the thread's scores (tokens t0 .. t1) in registers for all three passes
+        float v[kBalKeys];
+#pragma unroll
+        for (int i = 0; i < kBalKeys; ++i) v[i] = t0 + i < t1 ? __ldg(col + t0 + i) : 0.0f;
+        int32_t eq = 0;   // ties at the m-th score in this thread's range
+        if (!thr) {
+#pragma unroll
+            for (int i = 0; i < kBalKeys; ++i) eq += (t0 + i < t1 && fkey(v[i]) == ks) ? 1 : 0;
+        }
+        const int32_t eq_base = block_exscan(eq, warp_tot);
+        bool keep[kBalKeys];
+        int32_t cnt = 0, seen = 0;
+#pragma unroll
+        for (int i = 0; i < kBalKeys; ++i) {
+            bool k = false;
+            if (t0 + i < t1) {
+                if (thr) {
+                    k = v[i] > th;
+                } else {
+                    const uint32_t key = fkey(v[i]);
+                    k = key > ks || (key == ks && eq_base + seen++ < qt);
+                }
+            }
+            keep[i] = k;
+            cnt += k ? 1 : 0;
+        }
+        int32_t row = r0 + block_exscan(cnt, warp_tot);
+#pragma unroll
+        for (int i = 0; i < kBalKeys; ++i) {
+            if (!keep[i]) continue;
+            if (row < r1) {  // rows past the capacity were reported by bal_scan
+                row_token[row] = static_cast<int32_t>(t0 + i);
+                rowmap[(t0 + i) * n + e] = row;
+            }
+            ++row;
+        }
+        return;
+    }
     // ties at the m-th score before this thread's range
     int32_t eq = 0;
     if (!thr)
@@ -405,7 +445,6 @@ __global__ void __launch_bounds__(1024) bal_write(const float *__restrict__ HT, 
     int32_t cnt = 0, seen = 0;
     for (int64_t t = t0; t < t1; ++t) cnt += kept(t, seen) ? 1 : 0;
     const int32_t pos = block_exscan(cnt, warp_tot);
-    const int32_t r0 = offsets[e], r1 = offsets[e + 1];
     int32_t row = r0 + pos;
     seen = 0;
     for (int64_t t = t0; t < t1; ++t) {
@@ -429,6 +468,36 @@ __global__ void __launch_bounds__(256) bal_weights(const float *__restrict__ H,
     if (t >= T) return;
     const float *h = H + t * n;
     const int32_t *rm = rowmap + t * n;
+    if (n <= 256) {
+        // the token's row map and scores read once, eight per lane
+        int32_t r[8];
+        float hv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = 32 * i + lane;
+            r[i] = e < n ? __ldg(rm + e) : -1;
+            hv[i] = e < n ? __ldg(h + e) : 0.0f;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (r[i] >= 0) mx = fmaxf(mx, hv[i]);
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (r[i] >= 0) sum += __expf(hv[i] - mx);
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = 32 * i + lane;
+            if (e >= n) continue;
+            const float w = r[i] >= 0 ? __expf(hv[i] - mx) / sum : 0.0f;
+            if (r[i] >= 0) row_weight[r[i]] = w;
+            if (W) W[t * n + e] = w;
+        }
+        return;
+    }
     float mx = -INFINITY;
     for (int e = lane; e < n; e += 32)
         if (rm[e] >= 0) mx = fmaxf(mx, h[e]);
