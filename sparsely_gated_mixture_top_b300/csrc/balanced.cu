@@ -12,10 +12,11 @@
 //   y[t]       sum over those experts, in increasing e, of w E_e(x_t); 0 if none
 // Stages, in launch order:
 //   scores            H [T, n]: noisy bf16 shapes from the tensor-core gate's
-//                     load mode (c and softplus(r) per expert, fp32-faithful),
-//                     then bal_noisy_sum; other shapes bal_scores, fp32 on the
-//                     CUDA cores (64 x 64 tiles)
-//   bal_transpose     HT [n, T], each expert's scores contiguous
+//                     load mode (c and softplus(r) per expert, fp32-faithful,
+//                     H = c + eps * s formed by bal_transpose); other shapes
+//                     bal_scores, fp32 on the CUDA cores (64 x 64 tiles)
+//   bal_transpose     HT [n, T], each expert's scores contiguous; the row map
+//                     reset to -1
 //   bal_count         per expert: the m-th largest score by a 4-pass 8-bit
 //                     radix select on order-preserving keys, and how many of
 //                     the tied scores to keep (batchwise); or the number of
@@ -161,24 +162,31 @@ __global__ void __launch_bounds__(256) bal_scores(const TX *__restrict__ x, cons
     }
 }
 
-// H = c + eps * s in place over c (T*n entries).
-__global__ void __launch_bounds__(256) bal_noisy_sum(float *__restrict__ c, const float *__restrict__ sc,
-                                                     const float *__restrict__ eps, int64_t count) {
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < count;
-         i += static_cast<int64_t>(gridDim.x) * 256)
-        c[i] = fmaf(eps[i], sc[i], c[i]);
-}
-
 // HT[e, t] = H[t, e]: each expert's scores contiguous for the per-expert
-// select and compaction (32 x 32 tiles through shared memory).
-__global__ void bal_transpose(const float *__restrict__ H, int64_t T, int n, float *__restrict__ HT) {
+// select and compaction (32 x 32 tiles through shared memory).  With sc and
+// eps given, H holds the clean scores c on entry and becomes the noisy
+// scores c + eps * s first (in place).  The row map [T, n] is reset to -1 on
+// the way (the compaction then writes the kept entries).
+__global__ void bal_transpose(float *__restrict__ H, const float *__restrict__ sc,
+                              const float *__restrict__ eps, int64_t T, int n,
+                              float *__restrict__ HT, int32_t *__restrict__ rowmap) {
     __shared__ float tile[32][33];
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 32;
     const int e0 = blockIdx.y * 32;
     for (int i = threadIdx.y; i < 32; i += 8) {
         const int64_t t = t0 + i;
         const int e = e0 + threadIdx.x;
-        tile[i][threadIdx.x] = (t < T && e < n) ? H[t * n + e] : 0.0f;
+        float v = 0.0f;
+        if (t < T && e < n) {
+            const int64_t at = t * n + e;
+            v = H[at];
+            if (sc) {
+                v = fmaf(eps[at], sc[at], v);
+                H[at] = v;
+            }
+            rowmap[at] = -1;
+        }
+        tile[i][threadIdx.x] = v;
     }
     __syncthreads();
     for (int i = threadIdx.y; i < 32; i += 8) {
@@ -659,15 +667,14 @@ cudaError_t launch_forward_balanced(const moe_shape &s, const void *x, const flo
     int32_t *offsets = ws_ptr<int32_t>(ws, L.offsets);
     const float *eps_used = s.noisy ? eps : nullptr;
     const dim3 sgrid(static_cast<unsigned>((T + kBT - 1) / kBT), static_cast<unsigned>((n + kBT - 1) / kBT));
+    const float *noisy_sc = nullptr;
     if (bal_tc_scores(s) && eps_used) {
         float *sN = ws_ptr<float>(ws, B.sN);
         cudaError_t ge = launch_gate_tc_load(s, x, Wg, Wn, bg, eps_used, ws_ptr<int32_t>(ws, B.gidx),
                                              ws_ptr<float>(ws, B.gG), H, sN, ws_ptr<float>(ws, B.vk),
                                              ws, L, st);
         if (ge != cudaSuccess) return ge;
-        const int64_t count = T * n;
-        const unsigned g = static_cast<unsigned>(std::min<int64_t>((count + 255) / 256, 148 * 16));
-        bal_noisy_sum<<<g, 256, 0, st>>>(H, sN, eps_used, count);
+        noisy_sc = sN;   // H = c + eps * s is formed by the transpose
     } else if (s.dtype == MOE_BF16)
         bal_scores<__nv_bfloat16><<<sgrid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(x), Wg, Wn,
                                                         bg, eps_used, T, d, n, H);
@@ -676,12 +683,12 @@ cudaError_t launch_forward_balanced(const moe_shape &s, const void *x, const flo
                                                  T, d, n, H);
     float *HT = ws_ptr<float>(ws, B.HT);
     bal_transpose<<<dim3(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>((n + 31) / 32)),
-                    dim3(32, 8), 0, st>>>(H, T, n, HT);
+                    dim3(32, 8), 0, st>>>(H, noisy_sc, noisy_sc ? eps_used : nullptr, T, n, HT,
+                                          rowmap);
     const int64_t m = thr ? 0 : static_cast<int64_t>(s.k) * T / n;
     bal_count<<<n, 1024, 0, st>>>(HT, T, n, m, thr, ws_ptr<uint32_t>(ws, B.kstar),
                                   ws_ptr<int32_t>(ws, B.quota), ws_ptr<int32_t>(ws, B.cnt));
     bal_scan<<<1, 1024, 0, st>>>(ws_ptr<int32_t>(ws, B.cnt), n, rows_cap, offsets, counts, err);
-    cudaMemsetAsync(rowmap, 0xFF, sizeof(int32_t) * static_cast<size_t>(T) * n, st);  // -1
     bal_write<<<n, 1024, 0, st>>>(HT, T, n, thr, ws_ptr<uint32_t>(ws, B.kstar),
                                   ws_ptr<int32_t>(ws, B.quota), offsets, row_token, rowmap);
     bal_weights<<<static_cast<unsigned>((T + 7) / 8), 256, 0, st>>>(H, rowmap, T, n, row_weight, W);
