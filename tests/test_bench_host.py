@@ -72,3 +72,30 @@ def test_clock_sampler_summary_without_a_gpu():
     r = c.stop()
     assert r["sm_mhz"] == 2000.0 and r["sm_mhz_min"] == 1900.0 and r["sm_max_mhz"] == 2032.0
     assert r["samples"] == 3 and r["reasons"] == ["sw_power_cap"] and r["power_w_max"] == 900.0
+
+
+def test_every_pass_and_workload_parses(monkeypatch):
+    import sys
+    for which in ("forward", "backward", "balanced", "ep"):
+        for name in wl.WORKLOADS:
+            monkeypatch.setattr(sys, "argv", ["bench.py", "--pass", which, "--workload", name])
+            args = bench.parse()
+            assert args.which == which and args.workload == name
+            assert args.gpus == 1 and args.warmup >= 3
+
+
+def test_launch_counts_follow_the_expert_stage_choice():
+    """The counts the GPU graph tests confirm: the fused two-layer expert
+    kernel (one launch) serves bf16 shapes with d in {256, 512}, h a multiple
+    of 256 and at most 128 rows per expert on average; otherwise two GEMMs."""
+    W = wl.WORKLOADS
+    assert not bench.fused_ffn(W["flat_n256_k4"])            # 256 rows per expert
+    assert bench.launches_per_step(W["flat_n256_k4"]) == 8
+    assert bench.fused_ffn(W["hier_4096h_16x256"])           # 32 rows per expert
+    assert bench.launches_per_step(W["hier_4096h_16x256"]) == 14
+    assert bench.fused_ffn(W["sparse_n2048_T32768"])
+    assert bench.launches_per_step(W["sparse_n2048_T32768"]) == 7
+    assert not bench.fused_ffn(W["skewed_zipf_n64"])          # d = 1024
+    assert not bench.fused_ffn(W["tiny_flat_fp32"])           # fp32
+    assert bench.backward_launches(W["flat_n256_k4"]) == 29
+    assert bench.backward_launches(W["hier_4096h_16x256"]) == 36
