@@ -10,8 +10,11 @@
 // with fp32 accumulation and one round-to-nearest-even rounding of each
 // layer's output, the same arithmetic as the two separate grouped GEMMs
 // (ffn_pair.cu), which write H to memory and read it back.  Here H never
-// leaves the pair: about a third of the expert stage's DRAM traffic at the
-// widths this kernel serves (d = 256 or 512, h a multiple of 256).
+// leaves the pair, a quarter to a third of the expert stage's DRAM traffic
+// at the widths this kernel serves (d = 256 or 512, h a multiple of 256).
+// Each token tile takes in its expert's weights again, so the library uses
+// this kernel only where experts average at most 128 rows
+// (fused_ffn_supported).
 //
 // Unit of work: one token tile of one expert, at most 128 rows (the tile
 // table's entries {expert, first row, rows, N = rows rounded up to 32}).
@@ -34,9 +37,9 @@
 // The pair split: CTA s holds accumulator rows (features) s*128 .. +128 of
 // every M tile, all N token columns, while each CTA must supply its own N/2
 // tokens as layer 2's B rows.  So the epilogue of CTA s writes the values of
-// tokens in the other CTA's half straight into that CTA's H buffer (16-bit
-// stores to distributed shared memory), fences them for the tensor core and
-// arrives on the issuing CTA's barrier.
+// tokens in the other CTA's half straight into that CTA's H buffer (32-bit
+// stores of two neighbouring features to distributed shared memory), fences
+// them for the tensor core and arrives on the issuing CTA's barrier.
 //
 // Warps (576 threads per CTA, one CTA per SM, clusters of two):
 //   warp 0     TMA producer (each CTA): the tile's X rows, then every weight
